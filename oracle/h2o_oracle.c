@@ -1,0 +1,289 @@
+/* h2o_oracle.c — plain fp64 CPU oracle of H2O (Heavy-Hitter Oracle) KV-cache
+ * eviction.  TEST INFRASTRUCTURE ONLY (parity tests, smoke check, CPU baseline);
+ * the CUDA library never links or calls it and shares no code with it.
+ *
+ * The steps follow the H2O summary page ("H2O: Heavy-Hitter Oracle for
+ * Efficient Generative Inference", "The mechanism" and "Algorithm / figure
+ * walkthrough") in its notation: a cache set S of at most k = k_heavy + k_local
+ * entries, each carrying its accumulated attention score F_score.  Nothing is
+ * blocked, fused or reordered: every softmax is formed in full from its
+ * definition, in double precision, one query at a time.
+ *
+ * Parity pins (what ties this file to something other than itself) live in
+ * tests/test_oracle_pins.py: closed-form harmonic scores for identical keys,
+ * a library attention routine for the Full (k >= length) and Local
+ * (k_heavy = 0) special cases, Definition 4.3's invariants, conservation of
+ * score mass, and brute-force enumeration on tiny inputs.
+ */
+#include "h2o_oracle.h"
+
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+static double dot(const double *a, const double *b, int d) {
+  double s = 0.0;
+  for (int c = 0; c < d; ++c) s += a[c] * b[c];
+  return s;
+}
+
+/* ---------------------------------------------------------------- prefill */
+
+typedef struct {
+  double colsum;
+  int j;
+} cand_t;
+
+/* Order for the heavy-hitter choice: larger colsum first; equal colsums put the
+ * higher position first (the reading adopted for ties: the newer one stays). */
+static int cand_cmp(const void *pa, const void *pb) {
+  const cand_t *a = (const cand_t *)pa, *b = (const cand_t *)pb;
+  if (a->colsum > b->colsum) return -1;
+  if (a->colsum < b->colsum) return 1;
+  return (a->j > b->j) ? -1 : (a->j < b->j) ? 1 : 0;
+}
+
+static int int_cmp(const void *pa, const void *pb) {
+  int a = *(const int *)pa, b = *(const int *)pb;
+  return (a > b) - (a < b);
+}
+
+/* Step 1 of the walkthrough ("prefill the prompt ... begin scoring if the
+ * prompt already exceeds k"), read as: every prompt query attends causally to
+ * the prompt (no eviction inside the prompt), each key's F_score is the sum
+ * of the softmax weights it received (its causal column sum), and if L > k the
+ * cache keeps the k_local most recent positions (the protected local block)
+ * plus the k_heavy largest F_scores among the older ones. */
+static void prefill_head(int d, int L, int kh, int kl, const double *Q, const double *K,
+                         const double *V, double *O, double *lse, double *colsum,
+                         int32_t *pos, double *score, double *Ks, double *Vs,
+                         int32_t *n_valid, double *margin, double *dropped_mass) {
+  const int k = kh + kl;
+  const double scale = 1.0 / sqrt((double)d);
+  double *e = (double *)malloc(sizeof(double) * (size_t)L);
+  double *F = (double *)calloc((size_t)L, sizeof(double)); /* F_score per position */
+
+  for (int i = 0; i < L; ++i) {
+    const double *qi = Q + (size_t)i * d;
+    double m = -INFINITY;
+    for (int j = 0; j <= i; ++j) {
+      e[j] = scale * dot(qi, K + (size_t)j * d, d);
+      if (e[j] > m) m = e[j];
+    }
+    double l = 0.0;
+    for (int j = 0; j <= i; ++j) {
+      e[j] = exp(e[j] - m);
+      l += e[j];
+    }
+    if (O) {
+      double *oi = O + (size_t)i * d;
+      for (int c = 0; c < d; ++c) oi[c] = 0.0;
+      for (int j = 0; j <= i; ++j) {
+        const double w = e[j] / l;
+        const double *vj = V + (size_t)j * d;
+        for (int c = 0; c < d; ++c) oi[c] += w * vj[c];
+      }
+    }
+    if (lse) lse[i] = m + log(l);
+    for (int j = 0; j <= i; ++j) F[j] += e[j] / l;
+  }
+  if (colsum) memcpy(colsum, F, sizeof(double) * (size_t)L);
+
+  /* Choose S_0. */
+  int *keep = (int *)malloc(sizeof(int) * (size_t)(k > 0 ? k : 1));
+  int n = 0;
+  double mg = INFINITY, dropped = 0.0;
+  if (L <= k) {
+    for (int j = 0; j < L; ++j) keep[n++] = j;
+  } else {
+    const int nc = L - kl; /* candidates for the heavy-hitter slots: 0 .. L-kl-1 */
+    cand_t *c = (cand_t *)malloc(sizeof(cand_t) * (size_t)nc);
+    for (int j = 0; j < nc; ++j) {
+      c[j].colsum = F[j];
+      c[j].j = j;
+    }
+    qsort(c, (size_t)nc, sizeof(cand_t), cand_cmp);
+    for (int r = 0; r < kh; ++r) keep[n++] = c[r].j;
+    for (int r = kh; r < nc; ++r) dropped += c[r].colsum;
+    if (kh > 0 && nc > kh) mg = c[kh - 1].colsum - c[kh].colsum;
+    for (int j = L - kl; j < L; ++j) keep[n++] = j;
+    free(c);
+    qsort(keep, (size_t)n, sizeof(int), int_cmp);
+  }
+  for (int s = 0; s < k; ++s) {
+    double *ks = Ks + (size_t)s * d, *vs = Vs + (size_t)s * d;
+    if (s < n) {
+      const int j = keep[s];
+      pos[s] = j;
+      score[s] = F[j];
+      memcpy(ks, K + (size_t)j * d, sizeof(double) * (size_t)d);
+      memcpy(vs, V + (size_t)j * d, sizeof(double) * (size_t)d);
+    } else {
+      pos[s] = -1;
+      score[s] = 0.0;
+      memset(ks, 0, sizeof(double) * (size_t)d);
+      memset(vs, 0, sizeof(double) * (size_t)d);
+    }
+  }
+  *n_valid = n;
+  if (margin) *margin = mg;
+  if (dropped_mass) *dropped_mass = dropped;
+  free(keep);
+  free(e);
+  free(F);
+}
+
+int h2o_oracle_prefill(int nh, int d, int L, int k_heavy, int k_local,
+                       const double *Q, const double *K, const double *V,
+                       double *O, double *lse, double *colsum,
+                       int32_t *pos, double *score, double *Ks, double *Vs,
+                       int32_t *n_valid, double *margin, double *dropped_mass) {
+  if (nh < 0 || d < 1 || L < 1 || k_heavy < 0 || k_local < 0 || k_heavy + k_local < 1)
+    return -1;
+  if (!Q || !K || !V || !pos || !score || !Ks || !Vs || !n_valid) return -1;
+  const int k = k_heavy + k_local;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int h = 0; h < nh; ++h) {
+    const size_t hl = (size_t)h * L;
+    prefill_head(d, L, k_heavy, k_local, Q + hl * d, K + hl * d, V + hl * d,
+                 O ? O + hl * d : NULL, lse ? lse + hl : NULL, colsum ? colsum + hl : NULL,
+                 pos + (size_t)h * k, score + (size_t)h * k, Ks + (size_t)h * k * d,
+                 Vs + (size_t)h * k * d, n_valid + h, margin ? margin + h : NULL,
+                 dropped_mass ? dropped_mass + h : NULL);
+  }
+  return 0;
+}
+
+/* ----------------------------------------------------------------- decode */
+
+/* Steps 2-4 of the walkthrough for one head.  At position p the query attends
+ * over C = S ∪ {p}; each member of C adds its softmax weight to its F_score
+ * (the new entry starts at its own weight).  If |C| <= k the new entry is
+ * admitted; otherwise the entry with the lowest (F_score, position) among
+ * those not in the local block (positions <= p - k_local) leaves the cache. */
+static void decode_head(int d, int kh, int kl, int64_t p0, int T, int nh, int h,
+                        int32_t *pos, double *score, double *Ks, double *Vs, int32_t *n_valid,
+                        const double *q, const double *kn, const double *vn, double *out,
+                        int32_t *evicted, double *margin, double *evicted_mass) {
+  const int k = kh + kl;
+  const double scale = 1.0 / sqrt((double)d);
+  double *w = (double *)malloc(sizeof(double) * (size_t)(k + 1));
+  for (int t = 0; t < T; ++t) {
+    const int64_t p = p0 + t;
+    const size_t row = ((size_t)t * nh + h) * d;
+    const double *qt = q + row, *kt = kn + row, *vt = vn + row;
+    const int n = *n_valid;
+
+    /* Softmax over C: slots 0..n-1 then the new entry at index n. */
+    double m = -INFINITY;
+    for (int j = 0; j < n; ++j) {
+      w[j] = scale * dot(qt, Ks + (size_t)j * d, d);
+      if (w[j] > m) m = w[j];
+    }
+    w[n] = scale * dot(qt, kt, d);
+    if (w[n] > m) m = w[n];
+    double l = 0.0;
+    for (int j = 0; j <= n; ++j) {
+      w[j] = exp(w[j] - m);
+      l += w[j];
+    }
+    for (int j = 0; j <= n; ++j) w[j] /= l;
+
+    if (out) {
+      double *o = out + row;
+      for (int c = 0; c < d; ++c) o[c] = 0.0;
+      for (int j = 0; j < n; ++j) {
+        const double *vj = Vs + (size_t)j * d;
+        for (int c = 0; c < d; ++c) o[c] += w[j] * vj[c];
+      }
+      for (int c = 0; c < d; ++c) o[c] += w[n] * vt[c];
+    }
+
+    /* Accumulate F_score. */
+    for (int j = 0; j < n; ++j) score[j] += w[j];
+    const double w_new = w[n];
+
+    int32_t ev = -1;
+    double mg = INFINITY;
+    if (n + 1 <= k) {
+      /* |S| < k: admit. */
+      pos[n] = (int32_t)p;
+      score[n] = w_new;
+      memcpy(Ks + (size_t)n * d, kt, sizeof(double) * (size_t)d);
+      memcpy(Vs + (size_t)n * d, vt, sizeof(double) * (size_t)d);
+      *n_valid = n + 1;
+    } else {
+      /* Full: lowest (F_score, position) outside the local block leaves. */
+      int best = -2; /* slot index, -1 = the new entry, -2 = none yet */
+      double best_s = INFINITY, second_s = INFINITY;
+      int64_t best_p = 0;
+      for (int j = -1; j < n; ++j) {
+        const int64_t pj = (j < 0) ? p : (int64_t)pos[j];
+        if (pj > p - kl) continue; /* protected: one of the k_local newest */
+        const double sj = (j < 0) ? w_new : score[j];
+        if (best == -2 || sj < best_s || (sj == best_s && pj < best_p)) {
+          if (best != -2) second_s = best_s;
+          best = j;
+          best_s = sj;
+          best_p = pj;
+        } else if (sj < second_s) {
+          second_s = sj;
+        }
+      }
+      /* best == -2 cannot happen: with k_heavy + k_local = k and k+1 entries,
+       * at least k_heavy + 1 >= 1 lie outside the local block. */
+      if (best >= 0) {
+        ev = pos[best];
+        if (evicted_mass) *evicted_mass += score[best];
+        pos[best] = (int32_t)p;
+        score[best] = w_new;
+        memcpy(Ks + (size_t)best * d, kt, sizeof(double) * (size_t)d);
+        memcpy(Vs + (size_t)best * d, vt, sizeof(double) * (size_t)d);
+      } else {
+        ev = (int32_t)p; /* the new entry itself (only when k_local = 0) */
+        if (evicted_mass) *evicted_mass += w_new;
+      }
+      mg = second_s - best_s;
+    }
+    if (evicted) evicted[(size_t)t * nh + h] = ev;
+    if (margin) margin[(size_t)t * nh + h] = mg;
+  }
+  free(w);
+}
+
+int h2o_oracle_decode(int nh, int d, int k_heavy, int k_local, int64_t p0, int T,
+                      int32_t *pos, double *score, double *Ks, double *Vs, int32_t *n_valid,
+                      const double *q, const double *kn, const double *vn,
+                      double *out, int32_t *evicted, double *margin, double *evicted_mass) {
+  if (nh < 0 || d < 1 || T < 0 || k_heavy < 0 || k_local < 0 || k_heavy + k_local < 1 || p0 < 0)
+    return -1;
+  if (p0 + (int64_t)T > (int64_t)0x7fffffff) return -1;
+  if (!pos || !score || !Ks || !Vs || !n_valid || (T > 0 && (!q || !kn || !vn))) return -1;
+  const int k = k_heavy + k_local;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int h = 0; h < nh; ++h) {
+    decode_head(d, k_heavy, k_local, p0, T, nh, h, pos + (size_t)h * k, score + (size_t)h * k,
+                Ks + (size_t)h * k * d, Vs + (size_t)h * k * d, n_valid + h, q, kn, vn, out,
+                evicted, margin, evicted_mass ? evicted_mass + h : NULL);
+  }
+  return 0;
+}
+
+void h2o_oracle_set_threads(int n) {
+#ifdef _OPENMP
+  if (n > 0) omp_set_num_threads(n);
+#else
+  (void)n;
+#endif
+}
+
+int h2o_oracle_max_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}

@@ -1,0 +1,428 @@
+#!/usr/bin/env python
+"""Benchmark of the H2O decode/prefill hot path on GB300.
+
+One bench step = one whole job of the workload: create the cache, prefill the
+prompt (causal attention + column sums + heavy-hitter selection), then T
+decode steps (attend, accumulate scores, evict, write in place), all through
+the C ABI with inputs already resident in HBM.  L2 is flushed (a 256 MB write)
+before every step, outside the timed events.
+
+Printed JSON line (rank 0):
+  value     generated tokens/s of the whole job (B*T per job, per layer),
+            summed over ranks (weak scaling: each rank runs its own job);
+  decode    decode-only tokens/s, KV-read GB/s and fractions of HBM peak;
+  prefill   score-pass (column sums) and attention-pass TFLOP/s;
+  roofline  the kernel with the largest share of the step, measured live with
+            CUDA events on the launching stream (the C ABI's phase timer);
+  e2e       the same metric with host (pinned) buffers, copies timed;
+  cpu_baseline  the fp64 oracle on the host cores on a sample of heads.
+
+`--impl reference` times the oracle alone (the reference arm of this build).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 256 << 20
+METRIC = "H2O decode tokens/s and KV-read GB/s vs HBM peak; prefill score TFLOP/s"
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {k: float(d[k]) for k in FALLBACK}, "measured"
+    return dict(FALLBACK), "fallback"
+
+
+def esize(w):
+    return 2 if w.dtype == "bf16" else 4
+
+
+def decode_alg_bytes(w):
+    """Algorithmic HBM bytes of one decode step: K and V slots, position tags,
+    score read+write, the step's q/k/v inputs and its output."""
+    e = esize(w)
+    return w.nh * (2 * w.k * w.d * e + 12 * w.k) + 4 * w.nh * w.d * e
+
+
+def kv_read_bytes(w):
+    return w.nh * 2 * w.k * w.d * esize(w)
+
+
+def score_pass_flops(w):
+    """Causal QK^T of the column-sum pass: d*L*(L+1) per head."""
+    return w.nh * w.d * w.L * (w.L + 1)
+
+
+def attn_pass_flops(w):
+    return 2 * score_pass_flops(w)
+
+
+def workload_config(w, extra=None):
+    c = {"workload": w.name, "B": w.B, "H": w.H, "d": w.d, "prompt_L": w.L, "decode_T": w.T,
+         "k_heavy": w.k_heavy, "k_local": w.k_local, "cache_dtype": w.dtype,
+         "global_batch": w.B, "seq_len": w.L + w.T, "parallelism": "none (heads independent)",
+         "l2": "flushed before every step (256 MB write)"}
+    if extra:
+        c.update(extra)
+    return c
+
+
+def src_sha(rel):
+    return hashlib.sha256(open(os.path.join(ROOT, rel), "rb").read()).hexdigest()[:16]
+
+
+def traffic_for(kernel_key):
+    """DRAM bytes per launch from a committed ncu capture, or None if none was
+    taken or the kernel source changed since."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p)).get(kernel_key)
+    if not d:
+        return None
+    if d.get("source_sha") != src_sha(d["source"]):
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------------ clocks
+
+class Clocks:
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"h2o_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 8:
+                try:
+                    rows.append((float(parts[0]), float(parts[1]), float(parts[2]), parts[4:8]))
+                except ValueError:
+                    pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = np.array([r[0] for r in rows])
+        load = sm[sm > 0.5 * sm.max()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i, v in enumerate(r[3]) if v.lower() == "active"})
+        return {"sm_mhz": float(np.median(load)), "sm_max_mhz": float(rows[0][1]), "reasons": reasons,
+                "samples": len(rows), "power_w_max": float(max(r[2] for r in rows))}
+
+
+# --------------------------------------------------------------- our arm
+
+def run_ours(args, w, rank, world, local_rank):
+    import torch
+    import h2o_heavy_hitter_decode_gb300 as h2o
+    from h2o_heavy_hitter_decode_gb300 import H2OCache
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    else:
+        torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    h2o.lib()
+    pk, pk_src = peaks()
+
+    Qs, Ks, Vs = synth.prompt(w)
+    qs, ks, vs = synth.decode(w, 0, w.T)
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+
+    def host(x, shape):
+        t = torch.from_numpy(np.ascontiguousarray(x.view(np.int16) if w.dtype == "bf16" else x))
+        if w.dtype == "bf16":
+            t = t.view(torch.bfloat16)
+        return t.reshape(shape)
+
+    shp_p, shp_d = (w.B, w.H, w.L, w.d), (w.T, w.B, w.H, w.d)
+    hQ, hK, hV = host(Qs, shp_p), host(Ks, shp_p), host(Vs, shp_p)
+    hq, hk, hv = host(qs, shp_d), host(ks, shp_d), host(vs, shp_d)
+    Qd, Kd, Vd, qd, kd, vd = (x.to(dev) for x in (hQ, hK, hV, hq, hk, hv))
+    O = torch.empty(shp_p, dtype=tdt, device=dev)
+    lse = torch.empty((w.B, w.H, w.L), dtype=torch.float32, device=dev)
+    colsum = torch.empty_like(lse)
+    out = torch.empty(shp_d, dtype=tdt, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def job():
+        c = H2OCache(w.B, w.H, w.d, w.k_heavy, w.k_local, tdt, device=dev)
+        c.profile(True)
+        c.prefill(Qd, Kd, Vd, O=O, lse=lse, colsum=colsum)
+        c.steps(qd, kd, vd, out=out)
+        return c
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        job().profile_read()
+    torch.cuda.synchronize()
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    phases = {p: [0.0, 0] for p in H2OCache.PHASES}
+    caches = []
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with Clocks(local_rank) as clk:
+        t_wall = time.perf_counter()
+        for i in range(args.steps):
+            flush.zero_()
+            ev[i][0].record(stream)
+            caches.append(job())
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall
+    if dist:
+        dist.barrier()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    for c in caches:
+        for p, (ms, n) in c.profile_read().items():
+            phases[p][0] += ms
+            phases[p][1] += n
+    caches[-1].check_device_error()
+    tot_ms = float(np.sum(step_ms))
+    if dist:
+        t = torch.tensor([tot_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        tot_ms = float(t.item())
+    ms_per_step = tot_ms / args.steps
+    K = args.steps
+    tokens = w.B * w.T * world
+    value = tokens / (ms_per_step / 1e3)
+
+    dec_ms = phases["decode"][0] / K
+    dec_launch_ms = phases["decode"][0] / max(1, phases["decode"][1])
+    kv_gbs = kv_read_bytes(w) / (dec_launch_ms / 1e3) / 1e9
+    dec_alg_gbs = decode_alg_bytes(w) / (dec_launch_ms / 1e3) / 1e9
+    cs_ms = phases["prefill_colsum"][0] / K
+    at_ms = phases["prefill_attn"][0] / K
+    sel_ms = phases["prefill_select"][0] / K
+    cs_tf = score_pass_flops(w) / (cs_ms / 1e3) / 1e12
+    at_tf = attn_pass_flops(w) / (at_ms / 1e3) / 1e12
+
+    shares = {"decode": dec_ms, "prefill_colsum": cs_ms, "prefill_attn": at_ms, "prefill_select": sel_ms}
+    top = max(shares, key=shares.get)
+    if top == "decode":
+        roof = {"kernel": "decode_step_kernel", "bound": "hbm", "achieved": dec_alg_gbs, "peak": pk["hbm_gbs"],
+                "unit": "GB/s", "traffic": traffic_for("decode_step_kernel"),
+                "algorithmic_bytes_per_launch": decode_alg_bytes(w), "avg_launch_ms": dec_launch_ms}
+    elif top == "prefill_colsum":
+        roof = {"kernel": "prefill_colsum", "bound": "tensor", "achieved": cs_tf, "peak": pk["bf16_tflops"],
+                "unit": "TFLOP/s", "traffic": traffic_for("prefill_colsum"),
+                "algorithmic_flops_per_launch": score_pass_flops(w), "avg_launch_ms": cs_ms}
+    else:
+        roof = {"kernel": top, "bound": "tensor", "achieved": at_tf if top == "prefill_attn" else None,
+                "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "traffic": traffic_for(top),
+                "algorithmic_flops_per_launch": attn_pass_flops(w), "avg_launch_ms": shares[top]}
+    roof["frac"] = (roof["achieved"] / roof["peak"]) if roof.get("achieved") else None
+    roof["peak_source"] = pk_src
+    roof["share_of_step"] = shares[top] / ms_per_step
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.dtype, "impl": "ours",
+        "data": "synthetic: seeded per-head generator (Pareto-shifted keys along a hidden direction)",
+        "config": workload_config(w),
+        "decode": {"tokens_per_s": w.B * world / (dec_launch_ms / 1e3), "us_per_step": dec_launch_ms * 1e3,
+                   "kv_read_gbs": kv_gbs, "alg_gbs": dec_alg_gbs,
+                   "kv_read_frac_measured_hbm": kv_gbs / pk["hbm_gbs"],
+                   "kv_read_frac_nominal_8tbs": kv_gbs / NOMINAL_HBM_GBS,
+                   "cache_bytes": kv_read_bytes(w), "l2_resident": kv_read_bytes(w) < 120e6},
+        "prefill": {"score_pass_tflops": cs_tf, "score_pass_frac_measured_bf16": cs_tf / pk["bf16_tflops"],
+                    "attn_pass_tflops": at_tf, "attn_pass_frac_measured_bf16": at_tf / pk["bf16_tflops"],
+                    "ms": {"attn": at_ms, "colsum": cs_ms, "select_gather": sel_ms}},
+        "phase_ms_per_step": shares,
+        "roofline": roof,
+        "gpu_launches": int(phases["prefill_attn"][1] + phases["prefill_colsum"][1] + phases["prefill_select"][1]
+                            + phases["decode"][1]),
+        "wall_s_timed": t_wall,
+        "clocks": clk.summary(),
+        "peaks": {**pk, "source": pk_src},
+    }
+
+    if not args.no_e2e:
+        line["e2e"] = e2e(args, w, dev, hQ, hK, hV, hq, hk, hv, tdt, stream, world, dist)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, args)
+    if dist:
+        dist.destroy_process_group()
+    return line if rank == 0 else None
+
+
+def e2e(args, w, dev, hQ, hK, hV, hq, hk, hv, tdt, stream, world, dist):
+    """Same job from pinned host buffers: H2D of every input, prefill, decode,
+    D2H of the decode outputs, all inside the timed events."""
+    import torch
+    from h2o_heavy_hitter_decode_gb300 import H2OCache
+    pin = [x.pin_memory() for x in (hQ, hK, hV, hq, hk, hv)]
+    dbuf = [torch.empty_like(x, device=dev) for x in pin]
+    O = torch.empty(hQ.shape, dtype=tdt, device=dev)
+    lse = torch.empty((w.B, w.H, w.L), dtype=torch.float32, device=dev)
+    colsum = torch.empty_like(lse)
+    out = torch.empty(hq.shape, dtype=tdt, device=dev)
+    hout = torch.empty(hq.shape, dtype=tdt).pin_memory()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def job():
+        for d, h in zip(dbuf, pin):
+            d.copy_(h, non_blocking=True)
+        c = H2OCache(w.B, w.H, w.d, w.k_heavy, w.k_local, tdt, device=dev)
+        c.prefill(dbuf[0], dbuf[1], dbuf[2], O=O, lse=lse, colsum=colsum)
+        c.steps(dbuf[3], dbuf[4], dbuf[5], out=out)
+        hout.copy_(out, non_blocking=True)
+        return c
+
+    for _ in range(max(1, min(args.warmup, 3))):
+        job()
+    torch.cuda.synchronize()
+    n = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    if dist:
+        dist.barrier()
+    for i in range(n):
+        flush.zero_()
+        ev[i][0].record(stream)
+        job()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    ms = float(np.sum([a.elapsed_time(b) for a, b in ev]))
+    if dist:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    h2d = sum(x.numel() * x.element_size() for x in pin)
+    d2h = hout.numel() * hout.element_size()
+    return {"value": w.B * w.T * world / (ms / n / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms / n}
+
+
+# ------------------------------------------------------------ oracle timing
+
+def oracle_sample(w, n_heads):
+    """Inputs of the first n_heads heads (a bounded sample of the workload)."""
+    hs = list(range(min(n_heads, w.nh)))
+    Q, K, V = (synth.as_f64(x, w.dtype) for x in synth.prompt(w, heads=hs))
+    q, k, v = (synth.as_f64(x, w.dtype) for x in synth.decode(w, 0, w.T, heads=hs))
+    return hs, (Q, K, V, q, k, v)
+
+
+def oracle_job(w, data):
+    import oracle
+    Q, K, V, q, k, v = data
+    t = time.perf_counter()
+    r = oracle.prefill(Q, K, V, w.k_heavy, w.k_local)
+    oracle.decode(r["state"], w.L, q, k, v, w.k_heavy, w.k_local)
+    return time.perf_counter() - t
+
+
+def cpu_baseline(w, args):
+    import oracle
+    cores = os.cpu_count() or 1
+    oracle.set_threads(cores)
+    hs, data = oracle_sample(w, cores)
+    secs = oracle_job(w, data)
+    scale = w.nh / len(hs)
+    return {"value": w.B * w.T / (secs * scale), "unit": "tokens/s", "cores": int(oracle.max_threads()),
+            "kind": "oracle",
+            "sample": f"{len(hs)} of {w.nh} heads, full job (prefill L={w.L} + {w.T} decode steps), "
+                      f"{secs:.2f} s; rate extrapolated linearly to all heads"}
+
+
+def run_reference(args, w):
+    import oracle
+    cores = os.cpu_count() or 1
+    oracle.set_threads(cores)
+    hs, data = oracle_sample(w, cores)
+    for _ in range(args.warmup):
+        oracle_job(w, data)
+    secs = [oracle_job(w, data) for _ in range(args.steps)]
+    scale = w.nh / len(hs)
+    per_job = float(np.mean(secs)) * scale
+    value = w.B * w.T / per_job
+    sample = (f"each step: {len(hs)} of {w.nh} heads, full job (prefill L={w.L} + {w.T} decode steps); "
+              "rate extrapolated linearly to all heads")
+    return {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": per_job * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "impl": "reference",
+            "data": "synthetic: seeded per-head generator", "config": workload_config(w),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": int(oracle.max_threads()),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", type=int, default=1, help="workload index (0 tiny, 1 OPT-6.7B-shaped, ...)")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    w = synth.CONFIGS[args.config]
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        print(json.dumps(run_reference(args, w)), flush=True)
+        return
+    line = run_ours(args, w, rank, world, local_rank)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,396 @@
+// api.cu — the C ABI declared in include/h2o.h.
+//
+// Host-side bookkeeping only: argument checks, the workspace carve-up, the
+// per-cache counters (next position, filled slots) and the launch sequence.
+// Every step of the method runs in the kernels of decode.cu, prefill_*.cu and
+// select.cu.
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "../../include/h2o.h"
+#include "internal.h"
+
+namespace h2o {
+cudaError_t launch_prefill_attn_simt(const CacheView &c, const void *Q, const void *K, const void *V,
+                                     void *O, float *lse, int L, cudaStream_t st);
+cudaError_t launch_prefill_colsum_simt(const CacheView &c, const void *Q, const void *K, const float *lse,
+                                       float *colsum, int L, cudaStream_t st);
+bool prefill_tc_supported(const CacheView &c, int L);
+cudaError_t launch_prefill_attn_tc(const CacheView &c, const void *Q, const void *K, const void *V,
+                                   void *O, float *lse, int L, cudaStream_t st);
+cudaError_t launch_prefill_colsum_tc(const CacheView &c, const void *Q, const void *K, const float *lse,
+                                     float *colsum, int L, cudaStream_t st);
+}  // namespace h2o
+
+using namespace h2o;
+
+struct h2o_cache {
+  int B, H, d, kh, kl, k, nh;
+  h2o_dtype dtype;
+  int esize;
+  int64_t next_pos;
+  int n_valid;
+  bool prefilled;
+  cudaStream_t stream;
+  int device;
+  CacheView view;
+  // phase timing (h2o_profile_enable / h2o_profile_read)
+  bool profiling = false;
+  struct Mark {
+    int phase;
+    int64_t launches;
+    cudaEvent_t a, b;
+  };
+  std::vector<Mark> marks;
+};
+
+namespace {
+
+thread_local int g_last_cuda = 0;
+
+constexpr size_t kAlign = 256;
+constexpr int kMaxSplit = 64;
+constexpr int kMaxRowsPerSplit = 8192;
+constexpr int64_t kMaxPos = 0x7fffffffLL;  // positions are int32 tags
+
+size_t align_up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
+
+bool shape_ok(int B, int H, int d, int kh, int kl, h2o_dtype dt) {
+  if (B < 1 || H < 1 || kh < 0 || kl < 0) return false;
+  if ((int64_t)kh + kl < 1 || (int64_t)kh + kl > (int64_t)kMaxSplit * kMaxRowsPerSplit - 1) return false;
+  if ((int64_t)B * H > (1LL << 24)) return false;
+  if (dt != H2O_F32 && dt != H2O_BF16) return false;
+  return d >= 1;
+}
+
+bool d_supported(int d) { return d == 64 || d == 128; }
+
+// Splits per head for the decode launch: enough CTAs to give every SM about
+// eight, but no split shorter than 32 slot rows and none longer than
+// kMaxRowsPerSplit (the logits of a split live in shared memory).
+int choose_nsplit(int nh, int k, int sms) {
+  const int rows = k + 1;
+  int ns = (8 * sms + nh - 1) / nh;
+  const int by_rows = (rows + 31) / 32;
+  if (ns > by_rows) ns = by_rows;
+  const int min_ns = (rows + kMaxRowsPerSplit - 1) / kMaxRowsPerSplit;
+  if (ns < min_ns) ns = min_ns;
+  if (ns < 1) ns = 1;
+  if (ns > kMaxSplit) ns = kMaxSplit;
+  return ns;
+}
+
+struct Layout {
+  size_t K, V, pos, score, part, logits, counter, err, total;
+};
+
+Layout layout(int nh, int k, int d, int esize, int nsplit) {
+  Layout l;
+  size_t o = 0;
+  l.K = o;       o = align_up(o + (size_t)nh * k * d * esize);
+  l.V = o;       o = align_up(o + (size_t)nh * k * d * esize);
+  l.pos = o;     o = align_up(o + (size_t)nh * k * sizeof(int32_t));
+  l.score = o;   o = align_up(o + (size_t)nh * k * sizeof(float));
+  l.part = o;    o = align_up(o + (size_t)nh * nsplit * (2 + d) * sizeof(float));
+  l.logits = o;  o = align_up(o + (size_t)nh * (k + 1) * sizeof(float));
+  l.counter = o; o = align_up(o + (size_t)nh * sizeof(int));
+  l.err = o;     o = align_up(o + sizeof(int));
+  l.total = o;
+  return l;
+}
+
+h2o_status cuda_fail(cudaError_t e) {
+  g_last_cuda = (int)e;
+  return H2O_ECUDA;
+}
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+// Brackets one phase with events on the cache's stream when profiling is on.
+struct PhaseTimer {
+  h2o_cache *c;
+  h2o_cache::Mark m{};
+  bool on = false;
+  PhaseTimer(h2o_cache *c_, int phase, int64_t launches) : c(c_) {
+    if (!c->profiling) return;
+    m.phase = phase;
+    m.launches = launches;
+    if (cudaEventCreate(&m.a) != cudaSuccess) return;
+    if (cudaEventCreate(&m.b) != cudaSuccess) {
+      cudaEventDestroy(m.a);
+      return;
+    }
+    on = cudaEventRecord(m.a, c->stream) == cudaSuccess;
+  }
+  void done() {
+    if (!on) return;
+    cudaEventRecord(m.b, c->stream);
+    c->marks.push_back(m);
+    on = false;
+  }
+  ~PhaseTimer() {
+    if (on) {  // error path: nothing to keep
+      cudaEventDestroy(m.a);
+      cudaEventDestroy(m.b);
+    }
+  }
+};
+
+}  // namespace
+
+namespace h2o {
+int num_sms_current_device() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return sms;
+}
+}  // namespace h2o
+
+extern "C" {
+
+size_t h2o_cache_workspace_bytes(int B, int H, int d, int k_heavy, int k_local, h2o_dtype dtype) {
+  if (!shape_ok(B, H, d, k_heavy, k_local, dtype) || !d_supported(d)) return 0;
+  const int sms = num_sms_current_device();
+  if (sms <= 0) return 0;
+  const int nh = B * H, k = k_heavy + k_local;
+  const int esize = dtype == H2O_BF16 ? 2 : 4;
+  return layout(nh, k, d, esize, choose_nsplit(nh, k, sms)).total;
+}
+
+h2o_status h2o_cache_create(int B, int H, int d, int k_heavy, int k_local, h2o_dtype dtype,
+                            void *workspace, void *cuda_stream, h2o_cache_t *out) {
+  if (!out) return H2O_EINVAL;
+  *out = nullptr;
+  if (!shape_ok(B, H, d, k_heavy, k_local, dtype)) return H2O_EINVAL;
+  if (!d_supported(d)) return H2O_EUNSUPPORTED;
+  if (!workspace || ((uintptr_t)workspace & (kAlign - 1))) return H2O_EINVAL;
+  const int sms = num_sms_current_device();
+  if (sms <= 0) return cuda_fail(cudaGetLastError());
+  h2o_cache *c = new (std::nothrow) h2o_cache();
+  if (!c) return H2O_ENOMEM;
+  c->B = B; c->H = H; c->d = d; c->kh = k_heavy; c->kl = k_local;
+  c->k = k_heavy + k_local; c->nh = B * H; c->dtype = dtype;
+  c->esize = dtype == H2O_BF16 ? 2 : 4;
+  c->next_pos = 0; c->n_valid = 0; c->prefilled = false;
+  c->stream = (cudaStream_t)cuda_stream;
+  cudaGetDevice(&c->device);
+  const int ns = choose_nsplit(c->nh, c->k, sms);
+  const Layout l = layout(c->nh, c->k, d, c->esize, ns);
+  char *w = (char *)workspace;
+  CacheView &v = c->view;
+  v.nh = c->nh; v.d = d; v.k = c->k; v.kh = k_heavy; v.kl = k_local;
+  v.dtype = dtype == H2O_BF16 ? 1 : 0;
+  v.K = w + l.K; v.V = w + l.V;
+  v.pos = (int32_t *)(w + l.pos); v.score = (float *)(w + l.score);
+  v.part = (float *)(w + l.part); v.logits = (float *)(w + l.logits);
+  v.counter = (int *)(w + l.counter); v.err = (int *)(w + l.err);
+  v.nsplit = ns;
+  // Empty slots: pos = -1 (all bits set), score = 0, counters and flag 0.
+  cudaError_t e = cudaMemsetAsync(v.pos, 0xff, (size_t)c->nh * c->k * sizeof(int32_t), c->stream);
+  if (e == cudaSuccess) e = cudaMemsetAsync(v.score, 0, (size_t)c->nh * c->k * sizeof(float), c->stream);
+  if (e == cudaSuccess) e = cudaMemsetAsync(v.counter, 0, (size_t)c->nh * sizeof(int), c->stream);
+  if (e == cudaSuccess) e = cudaMemsetAsync(v.err, 0, sizeof(int), c->stream);
+  if (e != cudaSuccess) {
+    delete c;
+    return cuda_fail(e);
+  }
+  *out = c;
+  return H2O_OK;
+}
+
+h2o_status h2o_cache_destroy(h2o_cache_t c) {
+  if (c) {
+    for (auto &m : c->marks) {
+      cudaEventDestroy(m.a);
+      cudaEventDestroy(m.b);
+    }
+  }
+  delete c;
+  return H2O_OK;
+}
+
+h2o_status h2o_profile_enable(h2o_cache_t c, int on) {
+  if (!c) return H2O_EINVAL;
+  c->profiling = on != 0;
+  return H2O_OK;
+}
+
+h2o_status h2o_profile_read(h2o_cache_t c, double *ms, int64_t *launches) {
+  if (!c) return H2O_EINVAL;
+  double acc[4] = {0, 0, 0, 0};
+  int64_t cnt[4] = {0, 0, 0, 0};
+  h2o_status st = H2O_OK;
+  for (auto &m : c->marks) {
+    float t = 0.f;
+    cudaError_t e = cudaEventSynchronize(m.b);
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&t, m.a, m.b);
+    if (e != cudaSuccess && st == H2O_OK) st = cuda_fail(e);
+    acc[m.phase] += t;
+    cnt[m.phase] += m.launches;
+    cudaEventDestroy(m.a);
+    cudaEventDestroy(m.b);
+  }
+  c->marks.clear();
+  for (int i = 0; i < 4; ++i) {
+    if (ms) ms[i] = acc[i];
+    if (launches) launches[i] = cnt[i];
+  }
+  return st;
+}
+
+h2o_status h2o_set_stream(h2o_cache_t c, void *s) {
+  if (!c) return H2O_EINVAL;
+  c->stream = (cudaStream_t)s;
+  return H2O_OK;
+}
+
+h2o_status h2o_prefill(h2o_cache_t c, const void *Q, const void *K, const void *V, int L, void *O,
+                       float *lse, float *colsum) {
+  if (!c || !Q || !K || !V || !lse || !colsum) return H2O_EINVAL;
+  if (L < 1 || (int64_t)L >= kMaxPos) return H2O_EINVAL;
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || (O && !aligned16(O)) || !aligned16(lse) ||
+      !aligned16(colsum))
+    return H2O_EINVAL;
+  if (c->prefilled) return H2O_ESTATE;
+  const CacheView &v = c->view;
+  cudaError_t e;
+  const bool tc = prefill_tc_supported(v, L);
+  {
+    PhaseTimer pt(c, 0, 1);
+    e = tc ? launch_prefill_attn_tc(v, Q, K, V, O, lse, L, c->stream)
+           : launch_prefill_attn_simt(v, Q, K, V, O, lse, L, c->stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+    pt.done();
+  }
+  {
+    PhaseTimer pt(c, 1, 1);
+    e = tc ? launch_prefill_colsum_tc(v, Q, K, lse, colsum, L, c->stream)
+           : launch_prefill_colsum_simt(v, Q, K, lse, colsum, L, c->stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+    pt.done();
+  }
+  {
+    PhaseTimer pt(c, 2, 1);
+    e = launch_prefill_select(v, K, V, colsum, L, c->stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+    pt.done();
+  }
+  c->next_pos = L;
+  c->n_valid = L < c->k ? L : c->k;
+  c->prefilled = true;
+  return H2O_OK;
+}
+
+h2o_status h2o_decode_steps(h2o_cache_t c, int n, const void *q, const void *k, const void *v, void *out,
+                            int32_t *evicted) {
+  if (!c || n < 0) return H2O_EINVAL;
+  if (n == 0) return H2O_OK;
+  if (!q || !k || !v || !out) return H2O_EINVAL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || ((uintptr_t)evicted & 3u))
+    return H2O_EINVAL;
+  if (!c->prefilled) return H2O_ESTATE;
+  if (c->next_pos + n > kMaxPos) return H2O_EINVAL;
+  const size_t step = (size_t)c->nh * c->d * c->esize;
+  PhaseTimer pt(c, 3, n);
+  for (int i = 0; i < n; ++i) {
+    DecodeStep s;
+    s.q = (const char *)q + i * step;
+    s.kn = (const char *)k + i * step;
+    s.vn = (const char *)v + i * step;
+    s.out = (char *)out + i * step;
+    s.evicted = evicted ? evicted + (size_t)i * c->nh : nullptr;
+    s.n_valid = c->n_valid;
+    s.p = (int)c->next_pos;
+    cudaError_t e = launch_decode_step(c->view, s, c->stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+    c->next_pos += 1;
+    if (c->n_valid < c->k) c->n_valid += 1;
+  }
+  pt.done();
+  return H2O_OK;
+}
+
+h2o_status h2o_decode_step(h2o_cache_t c, const void *q, const void *k, const void *v, void *out) {
+  return h2o_decode_steps(c, 1, q, k, v, out, nullptr);
+}
+
+h2o_status h2o_cache_export(h2o_cache_t c, int32_t *pos, float *score, void *K, void *V, int64_t *next_pos,
+                            int *n_valid) {
+  if (!c) return H2O_EINVAL;
+  const CacheView &v = c->view;
+  const size_t slots = (size_t)c->nh * c->k;
+  cudaError_t e = cudaSuccess;
+  if (pos) e = cudaMemcpyAsync(pos, v.pos, slots * sizeof(int32_t), cudaMemcpyDefault, c->stream);
+  if (e == cudaSuccess && score)
+    e = cudaMemcpyAsync(score, v.score, slots * sizeof(float), cudaMemcpyDefault, c->stream);
+  if (e == cudaSuccess && K) e = cudaMemcpyAsync(K, v.K, slots * c->d * c->esize, cudaMemcpyDefault, c->stream);
+  if (e == cudaSuccess && V) e = cudaMemcpyAsync(V, v.V, slots * c->d * c->esize, cudaMemcpyDefault, c->stream);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (next_pos) *next_pos = c->next_pos;
+  if (n_valid) *n_valid = c->n_valid;
+  return H2O_OK;
+}
+
+h2o_status h2o_cache_import(h2o_cache_t c, const int32_t *pos, const float *score, const void *K,
+                            const void *V, int64_t next_pos, int n_valid) {
+  if (!c || !pos || !score || !K || !V) return H2O_EINVAL;
+  if (next_pos < 0 || next_pos >= kMaxPos || n_valid < 0 || n_valid > c->k) return H2O_EINVAL;
+  const CacheView &v = c->view;
+  const size_t slots = (size_t)c->nh * c->k;
+  cudaError_t e = cudaMemcpyAsync(v.pos, pos, slots * sizeof(int32_t), cudaMemcpyDefault, c->stream);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(v.score, score, slots * sizeof(float), cudaMemcpyDefault, c->stream);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(v.K, K, slots * c->d * c->esize, cudaMemcpyDefault, c->stream);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(v.V, V, slots * c->d * c->esize, cudaMemcpyDefault, c->stream);
+  if (e != cudaSuccess) return cuda_fail(e);
+  c->next_pos = next_pos;
+  c->n_valid = n_valid;
+  c->prefilled = true;
+  return H2O_OK;
+}
+
+h2o_status h2o_cache_info(h2o_cache_t c, int *B, int *H, int *d, int *k_heavy, int *k_local, int *dtype,
+                          int64_t *next_pos, int *n_valid, int *n_split) {
+  if (!c) return H2O_EINVAL;
+  if (B) *B = c->B;
+  if (H) *H = c->H;
+  if (d) *d = c->d;
+  if (k_heavy) *k_heavy = c->kh;
+  if (k_local) *k_local = c->kl;
+  if (dtype) *dtype = (int)c->dtype;
+  if (next_pos) *next_pos = c->next_pos;
+  if (n_valid) *n_valid = c->n_valid;
+  if (n_split) *n_split = c->view.nsplit;
+  return H2O_OK;
+}
+
+h2o_status h2o_get_error(h2o_cache_t c) {
+  if (!c) return H2O_EINVAL;
+  int flag = 0;
+  cudaError_t e = cudaMemcpyAsync(&flag, c->view.err, sizeof(int), cudaMemcpyDeviceToHost, c->stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(c->stream);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return flag ? H2O_EDEVICE : H2O_OK;
+}
+
+const char *h2o_status_str(h2o_status s) {
+  switch (s) {
+    case H2O_OK: return "ok";
+    case H2O_EINVAL: return "invalid argument";
+    case H2O_ESTATE: return "invalid state";
+    case H2O_ECUDA: return "CUDA error";
+    case H2O_ENOMEM: return "out of host memory";
+    case H2O_EDEVICE: return "device-side inconsistency";
+    case H2O_EUNSUPPORTED: return "unsupported shape";
+  }
+  return "unknown status";
+}
+
+int h2o_last_cuda_error(void) { return g_last_cuda; }
+
+int h2o_build_arch(void) { return 1030; }
+
+}  // extern "C"

@@ -1,0 +1,154 @@
+/* h2o.h — C ABI of libh2o.so: H2O (Heavy-Hitter Oracle) KV-cache eviction on
+ * one NVIDIA GB300 (sm_103a).
+ *
+ * The method is the one of "H2O: Heavy-Hitter Oracle for Efficient Generative
+ * Inference of Large Language Models" as summarised on its explainer page
+ * ("The mechanism"; "Algorithm / figure walkthrough" steps 1-5;
+ * Definition 4.3).  Each (batch b, head h) pair owns an independent cache set
+ * S of k = k_heavy + k_local slots.  Every cached key carries F_score, the sum
+ * of the softmax attention weights it has received.  At a decode step the new
+ * query attends over S plus the new token (k+1 entries, scale 1/sqrt(d)); the
+ * exact weights are added to the scores (the new token starts at its own
+ * weight); the entry with the lowest (score, position) outside the k_local
+ * newest positions is evicted and the new token takes its slot in place.
+ * Prefill scores the prompt by causal-softmax column sums and keeps the last
+ * k_local positions plus the k_heavy largest column sums of the rest.
+ *
+ * Conventions for every call below:
+ *   - Pointers named as device pointers must be device memory of the device
+ *     the cache was created on (or memory that device can address); host
+ *     pointers are ordinary host memory.  The caller owns all memory: the
+ *     library allocates nothing on the device.
+ *   - Tensors are dense row-major in the cache's dtype (fp32, or bf16 stored as
+ *     uint16 bit patterns), with the head index flattened as b*H + h:
+ *     prompt tensors [B][H][L][d]; one decode step [B][H][d]; n decode steps
+ *     [n][B][H][d].  Device pointers must be 16-byte aligned.
+ *   - Work is enqueued asynchronously on the cache's stream (set at create or
+ *     with h2o_set_stream); no call synchronises unless it says so.
+ *   - Errors are returned as h2o_status and never abort; arguments are checked
+ *     on the host before anything is launched, and on error nothing is
+ *     launched and the cache is unchanged.
+ */
+#ifndef H2O_H
+#define H2O_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct h2o_cache *h2o_cache_t; /* opaque host-side handle */
+
+typedef enum {
+  H2O_OK = 0,
+  H2O_EINVAL = 1,   /* bad argument (shape, null or misaligned pointer, range) */
+  H2O_ESTATE = 2,   /* call not valid in the cache's state (e.g. decode before prefill) */
+  H2O_ECUDA = 3,    /* a CUDA runtime call failed; h2o_last_cuda_error() has the code */
+  H2O_ENOMEM = 4,   /* host allocation failed */
+  H2O_EDEVICE = 5,  /* the device flagged an internal inconsistency (h2o_get_error) */
+  H2O_EUNSUPPORTED = 6 /* valid request this build does not handle (e.g. d not 64/128) */
+} h2o_status;
+
+typedef enum { H2O_F32 = 0, H2O_BF16 = 1 } h2o_dtype;
+
+/* Bytes of device workspace a cache of this shape needs (0 if the shape is
+ * invalid).  The workspace holds, per head: the K and V slots [k][d], the
+ * position tags [k] (int32, -1 = empty), the scores [k] (fp32), and the
+ * decode step's split partials and counters.  Shape rules: B, H >= 1;
+ * d in {64, 128}; k_heavy, k_local >= 0; k = k_heavy + k_local >= 1. */
+size_t h2o_cache_workspace_bytes(int B, int H, int d, int k_heavy, int k_local, h2o_dtype dtype);
+
+/* Create a cache over caller-owned device memory `workspace` (at least
+ * h2o_cache_workspace_bytes(...) bytes, 256-byte aligned, owned by the caller
+ * until h2o_cache_destroy).  `cuda_stream` is a cudaStream_t (NULL = legacy
+ * default stream).  Enqueues the initialisation of the workspace (all slots
+ * empty).  On success *out receives the handle. */
+h2o_status h2o_cache_create(int B, int H, int d, int k_heavy, int k_local, h2o_dtype dtype,
+                            void *workspace, void *cuda_stream, h2o_cache_t *out);
+
+/* Free the host-side handle (the workspace stays the caller's).  NULL is OK. */
+h2o_status h2o_cache_destroy(h2o_cache_t cache);
+
+/* Change the stream later calls enqueue on. */
+h2o_status h2o_set_stream(h2o_cache_t cache, void *cuda_stream);
+
+/* Prefill ("Algorithm / figure walkthrough" step 1): causal attention over the
+ * L prompt positions, then the initial cache set.
+ *   Q, K, V  device [B][H][L][d], cache dtype.
+ *   O        device [B][H][L][d] attention output, or NULL to skip it.
+ *   lse      device [B][H][L] fp32, required: natural-log log-sum-exp of each
+ *            query row's scaled logits.
+ *   colsum   device [B][H][L] fp32, required: colsum_j = sum_{i>=j}
+ *            softmax_i(j), the prompt's accumulated attention score.
+ * If L <= k every position is kept (slots 0..L-1); otherwise the last k_local
+ * positions plus the k_heavy largest column sums among positions
+ * 0..L-k_local-1 (equal sums: the higher position is kept).  Kept positions
+ * fill slots 0..n-1 in ascending order with score = colsum.  Valid once per
+ * cache (H2O_ESTATE otherwise).  L >= 1 and L < 2^31 - 1. */
+h2o_status h2o_prefill(h2o_cache_t cache, const void *Q, const void *K, const void *V, int L,
+                       void *O, float *lse, float *colsum);
+
+/* One decode step ("Algorithm / figure walkthrough" steps 2-4) for every head,
+ * one kernel launch: attend over the cached entries plus the new token,
+ * add the exact weights into the scores, evict, write the new token in place.
+ *   q_t, k_t, v_t  device [B][H][d]; out device [B][H][d].
+ * H2O_ESTATE before prefill/import. */
+h2o_status h2o_decode_step(h2o_cache_t cache, const void *q_t, const void *k_t, const void *v_t,
+                           void *out);
+
+/* n decode steps in sequence (n launches on the stream, or one persistent
+ * launch for small B*H), inputs [n][B][H][d], out [n][B][H][d].
+ * evicted: device [n][B][H] int32 or NULL; receives the position evicted at
+ * each step (-1 when the new token was admitted without eviction; the new
+ * position itself when it was the lowest-scoring candidate, which can only
+ * happen with k_local = 0). */
+h2o_status h2o_decode_steps(h2o_cache_t cache, int n, const void *q, const void *k, const void *v,
+                            void *out, int32_t *evicted);
+
+/* Copy the cache state out to device buffers: pos [B][H][k] int32,
+ * score [B][H][k] fp32, K, V [B][H][k][d] (any may be NULL); next_pos and
+ * n_valid (host, may be NULL) receive the position the next decode token
+ * takes and the number of filled slots.  Asynchronous like every call. */
+h2o_status h2o_cache_export(h2o_cache_t cache, int32_t *pos, float *score, void *K, void *V,
+                            int64_t *next_pos, int *n_valid);
+
+/* Replace the cache state with caller data (device pos, score, K, V in the
+ * layouts of h2o_cache_export, all required; slots >= n_valid must hold
+ * pos = -1).  Marks the cache as prefilled.  next_pos >= 0,
+ * 0 <= n_valid <= k. */
+h2o_status h2o_cache_import(h2o_cache_t cache, const int32_t *pos, const float *score,
+                            const void *K, const void *V, int64_t next_pos, int n_valid);
+
+/* Shape and counters of a cache (host pointers, any may be NULL). */
+h2o_status h2o_cache_info(h2o_cache_t cache, int *B, int *H, int *d, int *k_heavy, int *k_local,
+                          int *dtype, int64_t *next_pos, int *n_valid, int *n_split);
+
+/* Phase timing.  While enabled, each prefill pass and each h2o_decode_steps
+ * call is bracketed by CUDA events recorded on the cache's stream:
+ * phase 0 = prefill attention (pass 1), 1 = prefill column sums (pass 2),
+ * 2 = prefill select + gather, 3 = decode steps.  h2o_profile_read
+ * synchronises on the recorded events and returns, per phase, the summed
+ * elapsed milliseconds (ms[4]) and the number of kernel launches covered
+ * (launches[4]); it then clears the record.  Either output may be NULL. */
+h2o_status h2o_profile_enable(h2o_cache_t cache, int on);
+h2o_status h2o_profile_read(h2o_cache_t cache, double *ms, int64_t *launches);
+
+/* Synchronises the stream and reads the device-side error flag: H2O_OK, or
+ * H2O_EDEVICE if a kernel found an inconsistency (for example no eviction
+ * candidate).  The flag is sticky. */
+h2o_status h2o_get_error(h2o_cache_t cache);
+
+/* Human-readable name of a status; the last CUDA error code seen by the
+ * library (0 = none). */
+const char *h2o_status_str(h2o_status s);
+int h2o_last_cuda_error(void);
+
+/* Compiled-in target, for checks: returns 1030 for sm_103a. */
+int h2o_build_arch(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

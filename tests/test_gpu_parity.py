@@ -1,0 +1,98 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle on the
+same seeded inputs (tolerances in parity_helpers).
+
+Small cases compare every head with resynchronisation after permitted
+near-tie divergences; they span several 32-row tiles with ragged tails and the
+method's degenerate cases (prompt shorter than the budget, k_local = 0,
+k_heavy = 0, L = 1, k = 1).  The full-size workloads compare a seeded sample of
+heads in the same launch configuration the bench times."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import synth
+from parity_helpers import run_parity
+
+pytestmark = pytest.mark.gpu
+
+W = synth.Workload
+
+
+def small(name, B, H, d, L, T, kh, kl, dt, seed=77, planted=0.0):
+    return W(name, B, H, d, L, T, kh, kl, dt, seed, planted)
+
+
+SMALL = [
+    synth.CONFIGS[0],
+    small("bf16_multitile_ragged", 2, 3, 128, 300, 40, 64, 64, "bf16"),
+    small("bf16_d64_prompt_shorter_than_budget", 1, 4, 64, 50, 80, 40, 30, "bf16"),
+    small("bf16_no_local_block", 1, 2, 128, 100, 50, 32, 0, "bf16"),
+    small("f32_local_only", 1, 2, 64, 90, 50, 0, 24, "f32"),
+    small("f32_d128", 2, 2, 128, 130, 30, 20, 12, "f32"),
+    small("bf16_single_token_prompt", 1, 2, 64, 1, 20, 4, 4, "bf16"),
+    small("bf16_k1_heavy", 1, 2, 128, 40, 20, 1, 0, "bf16"),
+    small("bf16_k1_local", 1, 2, 128, 40, 20, 0, 1, "bf16"),
+    small("bf16_planted_hitters", 2, 2, 128, 257, 64, 30, 30, "bf16", planted=0.05),
+    small("f32_many_heads_splits", 4, 8, 64, 200, 24, 50, 40, "f32"),
+]
+
+
+@pytest.mark.parametrize("w", SMALL, ids=lambda w: w.name)
+def test_small_all_heads(w):
+    rep, cache = run_parity(w)
+    print(w.name, rep)
+    assert rep.steps_compared >= w.T
+
+
+def _sample(w, count, seed=5):
+    rng = np.random.default_rng(seed)
+    return sorted(rng.choice(w.nh, size=min(count, w.nh), replace=False).tolist())
+
+
+@pytest.mark.parametrize("idx,count", [(1, 8), (2, 12), (3, 3)])
+def test_full_size_sampled_heads(idx, count):
+    w = synth.CONFIGS[idx]
+    rep, cache = run_parity(w, heads=_sample(w, count), resync=False)
+    print(w.name, rep)
+    assert rep.steps_compared >= w.T
+
+
+def test_long_stream_first_steps():
+    """The long-stream workload, checked on its first 65,536 decode steps."""
+    w = synth.CONFIGS[4]
+    rep, cache = run_parity(w, T=65536)
+    print(w.name, rep)
+    assert rep.steps_compared >= 65536
+
+
+def test_decode_before_prefill_is_a_state_error():
+    from h2o_heavy_hitter_decode_gb300 import H2OCache, H2OError
+    c = H2OCache(1, 2, 64, 4, 4, torch.bfloat16)
+    x = torch.zeros((1, 2, 64), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(H2OError) as e:
+        c.step(x, x, x)
+    assert e.value.status == 2
+
+
+def test_second_prefill_is_a_state_error():
+    from h2o_heavy_hitter_decode_gb300 import H2OCache, H2OError
+    c = H2OCache(1, 1, 64, 4, 4, torch.float32)
+    Q = torch.randn((1, 1, 8, 64), device="cuda")
+    c.prefill(Q, Q, Q)
+    with pytest.raises(H2OError) as e:
+        c.prefill(Q, Q, Q)
+    assert e.value.status == 2
+
+
+def test_position_overflow_rejected():
+    from h2o_heavy_hitter_decode_gb300 import H2OCache, H2OError
+    c = H2OCache(1, 1, 64, 2, 2, torch.float32)
+    st = c.export()
+    c.import_state(st["pos"], st["score"], st["K"], st["V"], 2**31 - 3, 0)
+    x = torch.zeros((4, 1, 1, 64), device="cuda")
+    with pytest.raises(H2OError):
+        c.steps(x, x, x)
+    c.steps(x[:2], x[:2], x[:2])  # the last two positions still fit
+    torch.cuda.synchronize()

@@ -88,13 +88,13 @@ def src_sha(rel):
     return hashlib.sha256(open(os.path.join(ROOT, rel), "rb").read()).hexdigest()[:16]
 
 
-def traffic_for(kernel_key):
-    """DRAM bytes per launch from a committed ncu capture, or None if none was
-    taken or the kernel source changed since."""
+def traffic_for(kernel, w):
+    """DRAM bytes per launch of `kernel` on workload `w` from a committed ncu
+    capture, or None if none was taken or the kernel source changed since."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
-    d = json.load(open(p)).get(kernel_key)
+    d = json.load(open(p)).get(f"{kernel}@{w.name}")
     if not d:
         return None
     if d.get("source_sha") != src_sha(d["source"]):
@@ -251,15 +251,15 @@ def run_ours(args, w, rank, world, local_rank):
     top = max(shares, key=shares.get)
     if top == "decode":
         roof = {"kernel": "decode_step_kernel", "bound": "hbm", "achieved": dec_alg_gbs, "peak": pk["hbm_gbs"],
-                "unit": "GB/s", "traffic": traffic_for("decode_step_kernel"),
+                "unit": "GB/s", "traffic": traffic_for("decode_step_kernel", w),
                 "algorithmic_bytes_per_launch": decode_alg_bytes(w), "avg_launch_ms": dec_launch_ms}
     elif top == "prefill_colsum":
         roof = {"kernel": "prefill_colsum", "bound": "tensor", "achieved": cs_tf, "peak": pk["bf16_tflops"],
-                "unit": "TFLOP/s", "traffic": traffic_for("prefill_colsum"),
+                "unit": "TFLOP/s", "traffic": traffic_for("prefill_colsum", w),
                 "algorithmic_flops_per_launch": score_pass_flops(w), "avg_launch_ms": cs_ms}
     else:
         roof = {"kernel": top, "bound": "tensor", "achieved": at_tf if top == "prefill_attn" else None,
-                "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "traffic": traffic_for(top),
+                "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "traffic": traffic_for(top, w),
                 "algorithmic_flops_per_launch": attn_pass_flops(w), "avg_launch_ms": shares[top]}
     roof["frac"] = (roof["achieved"] / roof["peak"]) if roof.get("achieved") else None
     roof["peak_source"] = pk_src
@@ -405,12 +405,18 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", type=int, default=1, help="workload index (0 tiny, 1 OPT-6.7B-shaped, ...)")
+    ap.add_argument("--prompt-len", type=int, default=None, help="override L (profiling captures)")
+    ap.add_argument("--decode-steps", type=int, default=None, help="override T (profiling captures)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     w = synth.CONFIGS[args.config]
+    if args.prompt_len is not None or args.decode_steps is not None:
+        L = w.L if args.prompt_len is None else args.prompt_len
+        T = w.T if args.decode_steps is None else args.decode_steps
+        w = w.with_(name=f"{w.name}[L={L},T={T}]", L=L, T=T)
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))

@@ -135,6 +135,48 @@ h2o_status h2o_cache_info(h2o_cache_t cache, int *B, int *H, int *d, int *k_heav
 h2o_status h2o_profile_enable(h2o_cache_t cache, int on);
 h2o_status h2o_profile_read(h2o_cache_t cache, double *ms, int64_t *launches);
 
+/* Allocation-free decode step (no counterpart in the H2O paper: it is a
+ * deployment convenience of this library).
+ *
+ * Some callers cannot allocate device memory: inference servers that reserve
+ * all of HBM up front and hand a plugin only its input and output tensors, C
+ * hosts that receive device pointers from another runtime and hold no
+ * allocator, and latency-critical loops where a cudaMalloc (which may
+ * synchronise the device) is not acceptable.  This entry point runs one decode
+ * step for every head — the same kernel and arithmetic as h2o_decode_step —
+ * with its scratch (split partials, logits, arrival counters) in a fixed
+ * array compiled into the library, so it allocates nothing and needs no
+ * h2o_cache_t.
+ *
+ *   K, V       device [B][H][k][d] cache slots (cache dtype), read and updated.
+ *   pos        device [B][H][k] int32 position tags (-1 = empty), updated.
+ *   score      device [B][H][k] fp32 accumulated scores, updated.
+ *   n_valid    filled slots before this step (0..k), the same for every head.
+ *   position   position of the new token (0 <= position < 2^31 - 1).
+ *   q_t, k_t, v_t  device [B][H][d]; out device [B][H][d];
+ *   evicted    device [B][H] int32 or NULL (as in h2o_decode_steps).
+ *   cuda_stream    cudaStream_t to enqueue on (NULL = legacy default stream).
+ * The caller advances n_valid (while < k) and position after each call.
+ * Layouts are those of h2o_cache_export, so a cache's exported state can be
+ * continued here.
+ *
+ * Limits and sharing: the scratch array holds H2O_STATIC_SCRATCH_BYTES; a
+ * shape whose scratch would not fit is rejected with H2O_EINVAL before
+ * anything is launched.  Every GPU that loads the library holds the array
+ * until the process exits.  All calls share it and it keeps the last call's
+ * contents (each call clears what must start at zero), so calls that overlap
+ * on the GPU — on different streams, or from different host threads — race
+ * and must be serialised by the caller.  The first call on a device looks up
+ * the array's device address (cudaGetSymbolAddress, with that device
+ * current); make that first call before any stream capture on that device.
+ * A CUDA failure returns H2O_ECUDA; the kernel's own consistency flag lives
+ * in the shared scratch and is not reported here. */
+#define H2O_STATIC_SCRATCH_BYTES (16u << 20)
+h2o_status h2o_decode_step_static(int B, int H, int d, int k_heavy, int k_local, h2o_dtype dtype,
+                                  void *K, void *V, int32_t *pos, float *score, int n_valid,
+                                  int64_t position, const void *q_t, const void *k_t,
+                                  const void *v_t, void *out, int32_t *evicted, void *cuda_stream);
+
 /* Synchronises the stream and reads the device-side error flag: H2O_OK, or
  * H2O_EDEVICE if a kernel found an inconsistency (for example no eviction
  * candidate).  The flag is sticky. */

@@ -1,17 +1,343 @@
-// prefill_tc.cu — tensor-core (tcgen05 / TMEM) prefill passes for bf16.
+// prefill_tc.cu — tensor-core prefill passes for bf16 caches (sm_103a:
+// tcgen05.mma with TMEM accumulators, TMA tile loads, mbarrier pipeline).
+//
+// H2O summary page, "Algorithm / figure walkthrough" step 1: the prompt's
+// accumulated attention score of key j is its causal column sum
+//   colsum_j = sum_{i >= j} exp(q_i.k_j / sqrt(d) - LSE_i).
+//
+// Column-sum pass (the score pass).  One CTA owns a tile of 128 keys, which is
+// the MMA's A operand (M = 128 TMEM lanes, one key per thread) and stays in
+// shared memory; query tiles of 128 stream in through a two-stage TMA ring as
+// the B operand (N = 128).  S^T = K Q^T lands in one of two TMEM accumulator
+// buffers, so the MMA of query tile j+1 runs while the four warps turn tile j
+// into exp2(s * log2(e)/sqrt(d) - LSE_i * log2(e)) and add it along their TMEM
+// row: every key's sum stays in one thread, deterministic and atomic-free.
+// Only the first query tile touches the diagonal and needs the causal mask;
+// query rows past L are zero-filled by TMA and masked by LSE = +inf.
+//
+// LSE pass.  The same pipeline with the roles swapped: a CTA owns 128 queries
+// (A operand, TMEM lanes) and streams the key tiles 0..diagonal; each thread
+// keeps an online (max, sum) of its row in base 2.
+//
+// Warp roles: thread 0 issues TMA and MMA; all four warps run the epilogue
+// (warp w reads TMEM lanes 32w..32w+31).  Every mbarrier wait is bounded; on
+// a timeout the CTA flags the cache's error word, drains what it issued and
+// frees its TMEM before returning.
+#include <cudaTypedefs.h>
+
 #include "common.cuh"
+#include "sm100.cuh"
 
 namespace h2o {
+namespace {
 
-bool prefill_tc_supported(const CacheView &, int) { return false; }
+using namespace sm100;
 
-cudaError_t launch_prefill_attn_tc(const CacheView &, const void *, const void *, const void *, void *,
-                                   float *, int, cudaStream_t) {
-  return cudaErrorNotSupported;
+constexpr int kRows = 128;            // tile rows (TMEM lanes / MMA M and N)
+constexpr int kBox = kRows * 128;     // bytes of one 64-column bf16 box
+constexpr int kStages = 2;            // streamed-tile ring depth
+constexpr int kThreads = 128;
+
+template <int D> struct TileGeo {
+  static constexpr int kBoxes = D / 64;
+  static constexpr int kTileBytes = kBox * kBoxes;
+  static constexpr int kKSteps = D / 16;  // UMMA K = 16 for bf16
+  // resident tile + ring, each 1024-aligned, then the small state
+  static constexpr int kSmem = kTileBytes * (1 + kStages) + 2 * kRows * 4 + 256 + 1024;
+};
+
+struct __align__(8) SmallState {
+  uint64_t res_bar;
+  uint64_t ld_bar[kStages];
+  uint64_t mma_bar[2];
+  uint32_t tmem_base;
+  int abort;
+};
+
+__device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
+  return (uint8_t *)(((uintptr_t)p + 1023) & ~(uintptr_t)1023);
 }
-cudaError_t launch_prefill_colsum_tc(const CacheView &, const void *, const void *, const float *, float *,
-                                     int, cudaStream_t) {
-  return cudaErrorNotSupported;
+
+// Issue the K-loop of one 128x128 tile product: acc = A * B^T over d.
+template <int D>
+__device__ __forceinline__ void mma_tile(uint32_t acc, uint32_t a_base, uint32_t b_base) {
+  constexpr uint32_t idesc = idesc_bf16_f32(128, 128, false);
+#pragma unroll
+  for (int kk = 0; kk < TileGeo<D>::kKSteps; ++kk) {
+    const uint32_t off = (uint32_t)((kk >> 2) * kBox + (kk & 3) * 32);
+    umma_bf16(acc, sdesc_sw128(a_base + off, 16, 1024), sdesc_sw128(b_base + off, 16, 1024), idesc, kk > 0);
+  }
+}
+
+template <int D>
+__device__ __forceinline__ void load_tile(uint8_t *dst, const CUtensorMap *map, uint64_t *bar, int row, int h) {
+  mbar_expect_tx(bar, TileGeo<D>::kTileBytes);
+#pragma unroll
+  for (int b = 0; b < TileGeo<D>::kBoxes; ++b) tma_load_3d(dst + b * kBox, map, bar, b * 64, row, h);
+}
+
+// Shared skeleton: the resident tile (A) at row r0 of `mapA`, streamed tiles
+// j = 0..n-1 of `mapB` at rows s0 + 128 j.  `Epi` is called by all threads with
+// (j, TMEM address of this warp's lanes for tile j) and must read the tile.
+template <int D, class Prep, class Epi>
+__device__ __forceinline__ bool tile_pipeline(uint8_t *smem, SmallState &st, const CUtensorMap *mapA,
+                                              const CUtensorMap *mapB, int r0, int s0, int n, int h,
+                                              Prep &&prep, Epi &&epi) {
+  using G = TileGeo<D>;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  uint8_t *sA = smem;
+  uint8_t *sB = smem + G::kTileBytes;
+  if (tid == 0) {
+    mbar_init(&st.res_bar, 1);
+    for (int s = 0; s < kStages; ++s) mbar_init(&st.ld_bar[s], 1);
+    for (int b = 0; b < 2; ++b) mbar_init(&st.mma_bar[b], 1);
+    st.abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&st.tmem_base, 256);
+    tmem_relinquish();
+  }
+  prep(0);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = st.tmem_base;
+
+  int loads = 0, mmas = 0;  // issued by thread 0
+  if (tid == 0) {
+    load_tile<D>(sA, mapA, &st.res_bar, r0, h);
+    for (; loads < n && loads < kStages; ++loads)
+      load_tile<D>(sB + loads * G::kTileBytes, mapB, &st.ld_bar[loads], s0 + kRows * loads, h);
+  }
+  auto issue = [&](int j) -> bool {  // thread 0
+    if (!mbar_wait(&st.ld_bar[j % kStages], (j / kStages) & 1)) return false;
+    tc_fence_after();
+    mma_tile<D>(tbase + (uint32_t)(j & 1) * 128, smem_u32(sA), smem_u32(sB + (j % kStages) * G::kTileBytes));
+    umma_commit(&st.mma_bar[j & 1]);
+    return true;
+  };
+  if (tid == 0) {
+    if (mbar_wait(&st.res_bar, 0) && issue(0))
+      mmas = 1;
+    else
+      st.abort = 1;
+  }
+  int done = 0;  // tiles whose MMA this thread saw complete
+  for (int j = 0; j < n; ++j) {
+    if (tid == 0 && !st.abort && j + 1 < n) {
+      if (issue(j + 1))
+        mmas = j + 2;
+      else
+        st.abort = 1;
+    }
+    const bool ready = (j < mmas || tid != 0) && mbar_wait(&st.mma_bar[j & 1], (j >> 1) & 1);
+    if (!ready) st.abort = 1;
+    tc_fence_after();
+    if (ready) {
+      done = j + 1;
+      if (tid == 0 && loads < n && loads == j + kStages) {
+        load_tile<D>(sB + (j % kStages) * G::kTileBytes, mapB, &st.ld_bar[j % kStages], s0 + kRows * loads, h);
+        ++loads;
+      }
+      epi(j, tbase + ((uint32_t)(warp * 32) << 16) + (uint32_t)(j & 1) * 128);
+    }
+    if (j + 1 < n) prep(j + 1);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (st.abort) break;
+  }
+  const bool ok = !st.abort;
+  if (!ok && tid == 0) {
+    // Drain: tensor-core work and TMA copies this CTA started must land
+    // before its shared memory and TMEM are released.
+    for (int j = done; j < mmas; ++j) mbar_wait(&st.mma_bar[j & 1], (j >> 1) & 1);
+    for (int j = mmas; j < loads; ++j) mbar_wait(&st.ld_bar[j % kStages], (j / kStages) & 1);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tbase, 256);
+  return ok;
+}
+
+// ------------------------------------------------------------- column sums
+template <int D>
+__global__ void __launch_bounds__(kThreads, 2)
+    colsum_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+              const float *__restrict__ lse, float *__restrict__ colsum, int L, int nh, float qscale, int *err) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = align1024(smem_raw);
+  using G = TileGeo<D>;
+  float *nl2 = (float *)(smem + G::kTileBytes * (1 + kStages));  // [2][128]: -LSE*log2(e) per query
+  SmallState &st = *(SmallState *)(nl2 + 2 * kRows);
+  if (*(volatile int *)err) return;
+  // Heaviest CTAs (first key tiles: most query tiles) get the lowest indices.
+  const int kt = blockIdx.x / nh, h = blockIdx.x % nh;
+  const int k0 = kt * kRows;
+  const int nq = (L - k0 + kRows - 1) / kRows;
+  const int tid = threadIdx.x;
+  const float *lse_h = lse + (size_t)h * L;
+  auto prep = [&](int j) {
+    const int q = k0 + kRows * j + tid;
+    nl2[(j & 1) * kRows + tid] = q < L ? -__ldg(lse_h + q) * kLog2e : -INFINITY;
+  };
+  float acc = 0.f;
+  auto epi = [&](int j, uint32_t taddr) {
+    const float *nl = nl2 + (j & 1) * kRows;
+#pragma unroll 1
+    for (int c0 = 0; c0 < kRows; c0 += 32) {
+      uint32_t r[32];
+      tmem_ld32(taddr + c0, r);
+      tmem_ld_wait();
+      if (j == 0) {  // diagonal tile: query column c contributes iff c >= key row
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float e = ex2(fmaf(__uint_as_float(r[i]), qscale, nl[c0 + i]));
+          acc += (c0 + i >= tid) ? e : 0.f;
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) acc += ex2(fmaf(__uint_as_float(r[i]), qscale, nl[c0 + i]));
+      }
+    }
+  };
+  const bool ok = tile_pipeline<D>(smem, st, &tmK, &tmQ, k0, k0, nq, h, prep, epi);
+  if (ok) {
+    if (k0 + tid < L) colsum[(size_t)h * L + k0 + tid] = acc;
+  } else if (tid == 0) {
+    atomicOr(err, 4);
+  }
+}
+
+// ---------------------------------------------------------- row log-sum-exp
+template <int D>
+__global__ void __launch_bounds__(kThreads, 2)
+    lse_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+           float *__restrict__ lse, int L, int nh, int nqt, float qscale, int *err) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = align1024(smem_raw);
+  using G = TileGeo<D>;
+  SmallState &st = *(SmallState *)(smem + G::kTileBytes * (1 + kStages) + 2 * kRows * 4);
+  if (*(volatile int *)err) return;
+  // Heaviest CTAs (last query tiles: most key tiles) first.
+  const int qt = nqt - 1 - blockIdx.x / nh, h = blockIdx.x % nh;
+  const int q0 = qt * kRows;
+  const int nk = qt + 1;  // key tiles 0 .. diagonal
+  const int tid = threadIdx.x;
+  float m = -INFINITY, l = 0.f;  // base-2 running max and sum of this query row
+  auto prep = [](int) {};
+  auto epi = [&](int j, uint32_t taddr) {
+    const bool diag = (j == nk - 1);
+#pragma unroll 1
+    for (int c0 = 0; c0 < kRows; c0 += 32) {
+      uint32_t r[32];
+      tmem_ld32(taddr + c0, r);
+      tmem_ld_wait();
+      float x[32];
+      float cm = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        x[i] = __uint_as_float(r[i]) * qscale;
+        if (diag && c0 + i > tid) x[i] = -INFINITY;  // key after the query
+        cm = fmaxf(cm, x[i]);
+      }
+      const float mn = fmaxf(m, cm);
+      float s = 0.f;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) s += ex2(x[i] - mn);
+      l = l * ex2(m - mn) + s;
+      m = mn;
+    }
+  };
+  const bool ok = tile_pipeline<D>(smem, st, &tmQ, &tmK, q0, 0, nk, h, prep, epi);
+  if (ok) {
+    if (q0 + tid < L) lse[(size_t)h * L + q0 + tid] = (m + __log2f(l)) * kLn2;
+  } else if (tid == 0) {
+    atomicOr(err, 8);
+  }
+}
+
+// ----------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (PFN_cuTensorMapEncodeTiled_v12000)p;
+  }
+  return fn;
+}
+
+// [nh][L][d] bf16 viewed as a 3-D tensor; boxes of 64 columns x 128 rows of
+// one head, 128-byte swizzle; rows past L read as zero.
+bool make_map(CUtensorMap *m, const void *base, int d, int L, int nh) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)L, (cuuint64_t)nh};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)L * d * 2};
+  cuuint32_t box[3] = {64, (cuuint32_t)kRows, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D>
+cudaError_t colsum_t(const CacheView &c, const void *Q, const void *K, const float *lse, float *colsum, int L,
+                     cudaStream_t st) {
+  CUtensorMap mq, mk;
+  if (!make_map(&mq, Q, D, L, c.nh) || !make_map(&mk, K, D, L, c.nh)) return cudaErrorInvalidValue;
+  const int smem = TileGeo<D>::kSmem;
+  cudaError_t e = cudaFuncSetAttribute(colsum_tc<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const int nkt = (L + kRows - 1) / kRows;
+  const long long grid = (long long)nkt * c.nh;
+  colsum_tc<D><<<(unsigned)grid, kThreads, smem, st>>>(mq, mk, lse, colsum, L, c.nh, kLog2e / sqrtf((float)D),
+                                                      c.err);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t lse_t(const CacheView &c, const void *Q, const void *K, float *lse, int L, cudaStream_t st) {
+  CUtensorMap mq, mk;
+  if (!make_map(&mq, Q, D, L, c.nh) || !make_map(&mk, K, D, L, c.nh)) return cudaErrorInvalidValue;
+  const int smem = TileGeo<D>::kSmem;
+  cudaError_t e = cudaFuncSetAttribute(lse_tc<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const int nqt = (L + kRows - 1) / kRows;
+  const long long grid = (long long)nqt * c.nh;
+  lse_tc<D><<<(unsigned)grid, kThreads, smem, st>>>(mq, mk, lse, L, c.nh, nqt, kLog2e / sqrtf((float)D), c.err);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_attn_simt(const CacheView &c, const void *Q, const void *K, const void *V, void *O,
+                                     float *lse, int L, cudaStream_t st);
+
+bool prefill_tc_supported(const CacheView &c, int L) {
+  return c.dtype == 1 && (c.d == 64 || c.d == 128) && L >= 1 && (long long)c.nh * ((L + 127) / 128) < (1LL << 31) &&
+         encode_fn() != nullptr;
+}
+
+// Pass 1.  Without an O output only the row log-sum-exp is needed and runs on
+// the tensor cores; with O the FMA-pipe attention kernel produces both.
+cudaError_t launch_prefill_attn_tc(const CacheView &c, const void *Q, const void *K, const void *V, void *O,
+                                   float *lse, int L, cudaStream_t st) {
+  if (O) return launch_prefill_attn_simt(c, Q, K, V, O, lse, L, st);
+  return c.d == 128 ? lse_t<128>(c, Q, K, lse, L, st) : lse_t<64>(c, Q, K, lse, L, st);
+}
+
+cudaError_t launch_prefill_colsum_tc(const CacheView &c, const void *Q, const void *K, const float *lse,
+                                     float *colsum, int L, cudaStream_t st) {
+  return c.d == 128 ? colsum_t<128>(c, Q, K, lse, colsum, L, st) : colsum_t<64>(c, Q, K, lse, colsum, L, st);
 }
 
 }  // namespace h2o

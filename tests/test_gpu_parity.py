@@ -46,15 +46,30 @@ def test_small_all_heads(w):
     assert rep.steps_compared >= w.T
 
 
+NO_O = [w for w in SMALL if w.dtype == "bf16"] + [
+    small("bf16_no_O_long_prompt", 1, 3, 128, 1000, 16, 100, 60, "bf16"),
+    small("bf16_no_O_d64_ragged", 2, 2, 64, 333, 16, 40, 40, "bf16"),
+]
+
+
+@pytest.mark.parametrize("w", NO_O, ids=lambda w: w.name)
+def test_small_all_heads_without_O(w):
+    """Prefill without the attention output: the row log-sum-exp comes from
+    the tensor-core pass instead of the attention kernel."""
+    rep, cache = run_parity(w, want_O=False)
+    print(w.name, rep)
+    assert rep.steps_compared >= w.T
+
+
 def _sample(w, count, seed=5):
     rng = np.random.default_rng(seed)
     return sorted(rng.choice(w.nh, size=min(count, w.nh), replace=False).tolist())
 
 
-@pytest.mark.parametrize("idx,count", [(1, 8), (2, 12), (3, 3)])
-def test_full_size_sampled_heads(idx, count):
+@pytest.mark.parametrize("idx,count,want_O", [(1, 8, True), (2, 12, True), (3, 3, True), (3, 3, False)])
+def test_full_size_sampled_heads(idx, count, want_O):
     w = synth.CONFIGS[idx]
-    rep, cache = run_parity(w, heads=_sample(w, count), resync=False)
+    rep, cache = run_parity(w, heads=_sample(w, count), resync=False, want_O=want_O)
     print(w.name, rep)
     assert rep.steps_compared >= w.T
 

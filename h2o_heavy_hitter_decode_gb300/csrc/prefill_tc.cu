@@ -54,6 +54,12 @@ struct __align__(8) SmallState {
   int abort;
 };
 
+// Bounded wait whose outcome is the same for the whole warp (so the warp's
+// collective TMEM loads after it stay uniform even on a timeout).
+__device__ __forceinline__ bool wait_warp(uint64_t *bar, uint32_t parity) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity));
+}
+
 __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
   return (uint8_t *)(((uintptr_t)p + 1023) & ~(uintptr_t)1023);
 }
@@ -131,7 +137,8 @@ __device__ __forceinline__ bool tile_pipeline(uint8_t *smem, SmallState &st, con
       else
         st.abort = 1;
     }
-    const bool ready = (j < mmas || tid != 0) && mbar_wait(&st.mma_bar[j & 1], (j >> 1) & 1);
+    // Warp-uniform: the epilogue's TMEM loads are warp-collective.
+    const bool ready = __all_sync(0xffffffffu, (j < mmas || tid != 0) && mbar_wait(&st.mma_bar[j & 1], (j >> 1) & 1));
     if (!ready) st.abort = 1;
     tc_fence_after();
     if (ready) {
@@ -259,6 +266,205 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
 }
 
+// ------------------------------------------------------- attention output
+// O_i = sum_j P_ij V_j with the exact probabilities P_ij = exp2(s_ij*c -
+// LSE_i*log2(e)) (LSE from the pass above), so no online rescaling is needed.
+// One CTA per 128 queries; warps 0-3 turn S = Q K^T (TMEM) into bf16 P in
+// shared memory (128-byte swizzled K-major layout, the A operand of the next
+// MMA); warp 4 is the producer: TMA for Q (resident) and the K and V rings,
+// the S MMAs and the O += P V MMAs (V is the MN-major B operand).  S is
+// double-buffered in TMEM, O accumulates in TMEM and is written out at the
+// end.  Barriers: kfull/vfull (TMA landed), sfull (S_j computed), sfree (S_j
+// read), pfull (P_j written), pvdone (O += P_j V_j done: P buffer and V stage
+// free).
+template <int D> struct OutGeo {
+  static constexpr int kTile = TileGeo<D>::kTileBytes;  // 128 rows x D bf16
+  static constexpr int kP = 128 * 128 * 2;               // P tile: 128 queries x 128 keys
+  static constexpr int kSmem = kTile * 5 + kP * 2 + 256 + 1024;
+};
+
+struct __align__(8) OutState {
+  uint64_t res, kfull[2], vfull[2], sfull[2], sfree[2], pfull[2], pvdone[2], drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+template <int D>
+__global__ void __launch_bounds__(160, 1)
+    attn_out_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                const __grid_constant__ CUtensorMap tmV, const float *__restrict__ lse, __nv_bfloat16 *__restrict__ O,
+                int L, int nh, int nqt, float qscale, int *err) {
+  using G = OutGeo<D>;
+  constexpr int kT = G::kTile;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = align1024(smem_raw);
+  uint8_t *sV = smem;              // 2 stages (first: keeps MMA reads of V inside the tile area)
+  uint8_t *sK = smem + 2 * kT;     // 2 stages
+  uint8_t *sQ = smem + 4 * kT;     // resident
+  uint8_t *sP = smem + 5 * kT;     // 2 buffers of kP
+  OutState &st = *(OutState *)(sP + 2 * G::kP);
+  if (*(volatile int *)err) return;
+  const int qt = nqt - 1 - blockIdx.x / nh, h = blockIdx.x % nh;
+  const int q0 = qt * kRows;
+  const int n = qt + 1;  // key tiles 0 .. diagonal
+  const int tid = threadIdx.x, warp = tid >> 5;
+
+  if (tid == 0) {
+    mbar_init(&st.res, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&st.kfull[b], 1);
+      mbar_init(&st.vfull[b], 1);
+      mbar_init(&st.sfull[b], 1);
+      mbar_init(&st.sfree[b], 128);
+      mbar_init(&st.pfull[b], 128);
+      mbar_init(&st.pvdone[b], 1);
+    }
+    mbar_init(&st.drain, 1);
+    st.abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&st.tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = st.tmem_base;  // S buffers at columns 0 and 128, O at 256
+  const uint32_t tO = tbase + 256;
+
+  if (warp == 4) {
+    if ((tid & 31) == 0) {
+      constexpr uint32_t idO = idesc_bf16_f32(128, D, true);
+      int kl = 0, vl = 0, mS = 0, mPV = 0;  // TMA loads and MMAs issued
+      bool ok = true;
+      load_tile<D>(sQ, &tmQ, &st.res, q0, h);
+      for (; kl < n && kl < 2; ++kl) load_tile<D>(sK + kl * kT, &tmK, &st.kfull[kl], kRows * kl, h);
+      for (; vl < n && vl < 2; ++vl) load_tile<D>(sV + vl * kT, &tmV, &st.vfull[vl], kRows * vl, h);
+      ok = mbar_wait(&st.res, 0);
+      auto issue_S = [&](int j) -> bool {
+        if (!mbar_wait(&st.kfull[j & 1], (j >> 1) & 1)) return false;
+        if (j >= 2 && !mbar_wait(&st.sfree[j & 1], ((j - 2) >> 1) & 1)) return false;
+        tc_fence_after();
+        mma_tile<D>(tbase + (uint32_t)(j & 1) * 128, smem_u32(sQ), smem_u32(sK + (j & 1) * kT));
+        umma_commit(&st.sfull[j & 1]);
+        return true;
+      };
+      if (ok) ok = issue_S(0);
+      if (ok) mS = 1;
+      for (int j = 0; ok && j < n; ++j) {
+        if (j + 1 < n) {
+          if (!(ok = issue_S(j + 1))) break;
+          mS = j + 2;
+        }
+        if (j >= 1 && vl < n) {  // V stage of tile j-1 frees when its PV is done
+          if (!(ok = mbar_wait(&st.pvdone[(j - 1) & 1], ((j - 1) >> 1) & 1))) break;
+          load_tile<D>(sV + (vl & 1) * kT, &tmV, &st.vfull[vl & 1], kRows * vl, h);
+          ++vl;
+        }
+        if (kl < n) {  // K stage of tile j frees when S_j is done
+          if (!(ok = mbar_wait(&st.sfull[j & 1], (j >> 1) & 1))) break;
+          load_tile<D>(sK + (kl & 1) * kT, &tmK, &st.kfull[kl & 1], kRows * kl, h);
+          ++kl;
+        }
+        if (!(ok = mbar_wait(&st.pfull[j & 1], (j >> 1) & 1))) break;
+        if (!(ok = mbar_wait(&st.vfull[j & 1], (j >> 1) & 1))) break;
+        tc_fence_after();
+        const uint32_t pa = smem_u32(sP + (j & 1) * G::kP), va = smem_u32(sV + (j & 1) * kT);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {  // 128 keys, 16 per MMA
+          const uint64_t ad = sdesc_sw128(pa + (uint32_t)((kk >> 2) * kBox + (kk & 3) * 32), 16, 1024);
+          const uint64_t bd = sdesc_sw128(va + (uint32_t)(kk * 2048), kBox, 1024);
+          umma_bf16(tO, ad, bd, idO, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        umma_commit(&st.pvdone[j & 1]);
+        mPV = j + 1;
+      }
+      if (!ok) {
+        st.abort = 1;
+        // Drain every MMA and TMA copy this CTA issued before releasing
+        // shared memory and TMEM.
+        umma_commit(&st.drain);
+        mbar_wait(&st.drain, 0);
+        for (int j = mS; j < kl; ++j) mbar_wait(&st.kfull[j & 1], (j >> 1) & 1);
+        for (int j = mPV; j < vl; ++j) mbar_wait(&st.vfull[j & 1], (j >> 1) & 1);
+      }
+      (void)mPV;
+    }
+  } else {
+    // Softmax warps: thread tid owns query row q0 + tid (TMEM lane tid).
+    const int q = q0 + tid;
+    const float nl2 = q < L ? -__ldg(lse + (size_t)h * L + q) * kLog2e : 0.f;
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const int sw = tid & 7;
+    bool ok = true;
+    for (int j = 0; j < n; ++j) {
+      if (j >= 2 && !(ok = wait_warp(&st.pvdone[j & 1], ((j - 2) >> 1) & 1))) break;
+      if (!(ok = wait_warp(&st.sfull[j & 1], (j >> 1) & 1))) break;
+      tc_fence_after();
+      const bool diag = (j == n - 1);
+      uint8_t *prow = sP + (j & 1) * G::kP + tid * 128;
+#pragma unroll 1
+      for (int c0 = 0; c0 < 128; c0 += 32) {
+        uint32_t r[32];
+        tmem_ld32(tbase + lane_off + (uint32_t)(j & 1) * 128 + c0, r);
+        tmem_ld_wait();
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          float a = ex2(fmaf(__uint_as_float(r[2 * i]), qscale, nl2));
+          float b = ex2(fmaf(__uint_as_float(r[2 * i + 1]), qscale, nl2));
+          if (diag && c0 + 2 * i > tid) a = 0.f;
+          if (diag && c0 + 2 * i + 1 > tid) b = 0.f;
+          __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+          pk[i] = *reinterpret_cast<uint32_t *>(&v);
+        }
+        // 32 keys = four 16-byte chunks of box c0/64, swizzled by row.
+        uint8_t *box = prow + (c0 >> 6) * kBox;
+#pragma unroll
+        for (int cch = 0; cch < 4; ++cch) {
+          const int logical = ((c0 & 63) >> 3) + cch;
+          *reinterpret_cast<uint4 *>(box + ((logical ^ sw) << 4)) =
+              make_uint4(pk[4 * cch], pk[4 * cch + 1], pk[4 * cch + 2], pk[4 * cch + 3]);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&st.sfree[j & 1]);
+      fence_proxy_async_smem();
+      mbar_arrive(&st.pfull[j & 1]);
+    }
+    if (ok) ok = wait_warp(&st.pvdone[(n - 1) & 1], ((n - 1) >> 1) & 1);
+    if (ok) {
+      tc_fence_after();
+      __nv_bfloat16 *orow = O + ((size_t)h * L + (q < L ? q : 0)) * D;
+#pragma unroll 1
+      for (int c0 = 0; c0 < D; c0 += 32) {  // collective loads: every lane, every chunk
+        uint32_t r[32];
+        tmem_ld32(tO + lane_off + c0, r);
+        tmem_ld_wait();
+        if (q < L) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            __nv_bfloat162 v = __floats2bfloat162_rn(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+            pk[i] = *reinterpret_cast<uint32_t *>(&v);
+          }
+          uint4 *dst = reinterpret_cast<uint4 *>(orow + c0);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+        }
+      }
+    } else {
+      st.abort = 1;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (st.abort && tid == 0) atomicOr(err, 16);
+  if (warp == 0) tmem_dealloc(tbase, 512);
+}
+
 // ----------------------------------------------------------------- host side
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -305,6 +511,22 @@ cudaError_t colsum_t(const CacheView &c, const void *Q, const void *K, const flo
 }
 
 template <int D>
+cudaError_t attn_out_t(const CacheView &c, const void *Q, const void *K, const void *V, const float *lse, void *O,
+                       int L, cudaStream_t st) {
+  CUtensorMap mq, mk, mv;
+  if (!make_map(&mq, Q, D, L, c.nh) || !make_map(&mk, K, D, L, c.nh) || !make_map(&mv, V, D, L, c.nh))
+    return cudaErrorInvalidValue;
+  const int smem = OutGeo<D>::kSmem;
+  cudaError_t e = cudaFuncSetAttribute(attn_out_tc<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const int nqt = (L + kRows - 1) / kRows;
+  const long long grid = (long long)nqt * c.nh;
+  attn_out_tc<D><<<(unsigned)grid, 160, smem, st>>>(mq, mk, mv, lse, (__nv_bfloat16 *)O, L, c.nh, nqt,
+                                                     kLog2e / sqrtf((float)D), c.err);
+  return cudaGetLastError();
+}
+
+template <int D>
 cudaError_t lse_t(const CacheView &c, const void *Q, const void *K, float *lse, int L, cudaStream_t st) {
   CUtensorMap mq, mk;
   if (!make_map(&mq, Q, D, L, c.nh) || !make_map(&mk, K, D, L, c.nh)) return cudaErrorInvalidValue;
@@ -319,20 +541,18 @@ cudaError_t lse_t(const CacheView &c, const void *Q, const void *K, float *lse, 
 
 }  // namespace
 
-cudaError_t launch_prefill_attn_simt(const CacheView &c, const void *Q, const void *K, const void *V, void *O,
-                                     float *lse, int L, cudaStream_t st);
-
 bool prefill_tc_supported(const CacheView &c, int L) {
   return c.dtype == 1 && (c.d == 64 || c.d == 128) && L >= 1 && (long long)c.nh * ((L + 127) / 128) < (1LL << 31) &&
          encode_fn() != nullptr;
 }
 
-// Pass 1.  Without an O output only the row log-sum-exp is needed and runs on
-// the tensor cores; with O the FMA-pipe attention kernel produces both.
+// Pass 1: the row log-sum-exp, then (if O is wanted) the attention output
+// from the exact probabilities; both on the tensor cores.
 cudaError_t launch_prefill_attn_tc(const CacheView &c, const void *Q, const void *K, const void *V, void *O,
                                    float *lse, int L, cudaStream_t st) {
-  if (O) return launch_prefill_attn_simt(c, Q, K, V, O, lse, L, st);
-  return c.d == 128 ? lse_t<128>(c, Q, K, lse, L, st) : lse_t<64>(c, Q, K, lse, L, st);
+  cudaError_t e = c.d == 128 ? lse_t<128>(c, Q, K, lse, L, st) : lse_t<64>(c, Q, K, lse, L, st);
+  if (e != cudaSuccess || !O) return e;
+  return c.d == 128 ? attn_out_t<128>(c, Q, K, V, lse, O, L, st) : attn_out_t<64>(c, Q, K, V, lse, O, L, st);
 }
 
 cudaError_t launch_prefill_colsum_tc(const CacheView &c, const void *Q, const void *K, const float *lse,

@@ -194,6 +194,7 @@ def run_ours(args, w, rank, world, local_rank):
 
     def job():
         c = H2OCache(w.B, w.H, w.d, w.k_heavy, w.k_local, tdt, device=dev)
+        c.set_decode_form(args.decode_form)
         c.profile(True)
         c.prefill(Qd, Kd, Vd, O=O, lse=lse, colsum=colsum)
         c.steps(qd, kd, vd, out=out)
@@ -270,7 +271,7 @@ def run_ours(args, w, rank, world, local_rank):
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": w.dtype, "impl": "ours",
         "data": "synthetic: seeded per-head generator (Pareto-shifted keys along a hidden direction)",
-        "config": workload_config(w),
+        "config": workload_config(w, {"decode_form": args.decode_form}),
         "decode": {"tokens_per_s": w.B * world / (dec_launch_ms / 1e3), "us_per_step": dec_launch_ms * 1e3,
                    "kv_read_gbs": kv_gbs, "alg_gbs": dec_alg_gbs,
                    "kv_read_frac_measured_hbm": kv_gbs / pk["hbm_gbs"],
@@ -315,6 +316,7 @@ def e2e(args, w, dev, hQ, hK, hV, hq, hk, hv, tdt, stream, world, dist):
         for d, h in zip(dbuf, pin):
             d.copy_(h, non_blocking=True)
         c = H2OCache(w.B, w.H, w.d, w.k_heavy, w.k_local, tdt, device=dev)
+        c.set_decode_form(args.decode_form)
         c.prefill(dbuf[0], dbuf[1], dbuf[2], O=O, lse=lse, colsum=colsum)
         c.steps(dbuf[3], dbuf[4], dbuf[5], out=out)
         hout.copy_(out, non_blocking=True)
@@ -407,6 +409,7 @@ def main():
     ap.add_argument("--config", type=int, default=1, help="workload index (0 tiny, 1 OPT-6.7B-shaped, ...)")
     ap.add_argument("--prompt-len", type=int, default=None, help="override L (profiling captures)")
     ap.add_argument("--decode-steps", type=int, default=None, help="override T (profiling captures)")
+    ap.add_argument("--decode-form", default="auto", choices=["auto", "per_step", "cooperative", "cluster"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

@@ -69,6 +69,7 @@ def lib():
         L.h2o_cache_info.argtypes = [vp] + [C.POINTER(i32)] * 6 + [C.POINTER(i64)] + [C.POINTER(i32)] * 2
         L.h2o_get_error.argtypes = [vp]
         L.h2o_profile_enable.argtypes = [vp, i32]
+        L.h2o_set_decode_form.argtypes = [vp, i32]
         L.h2o_profile_read.argtypes = [vp, C.POINTER(C.c_double), C.POINTER(i64)]
         L.h2o_status_str.argtypes = [i32]
         L.h2o_status_str.restype = C.c_char_p
@@ -76,7 +77,7 @@ def lib():
         L.h2o_build_arch.restype = i32
         for f in ("h2o_cache_create", "h2o_cache_destroy", "h2o_set_stream", "h2o_prefill", "h2o_decode_step",
                   "h2o_decode_steps", "h2o_cache_export", "h2o_cache_import", "h2o_cache_info",
-                  "h2o_get_error", "h2o_profile_enable", "h2o_profile_read"):
+                  "h2o_get_error", "h2o_profile_enable", "h2o_profile_read", "h2o_set_decode_form"):
             getattr(L, f).restype = i32
         _lib = L
     return _lib
@@ -226,6 +227,13 @@ class H2OCache:
                     n_split=ns.value)
 
     PHASES = ("prefill_attn", "prefill_colsum", "prefill_select", "decode")
+    DECODE_FORMS = {"auto": 0, "per_step": 1, "cooperative": 2, "cluster": 3}
+
+    def set_decode_form(self, form):
+        """How multi-step decode runs: "auto", "per_step", "cooperative" or
+        "cluster" (see h2o_set_decode_form)."""
+        f = self.DECODE_FORMS[form] if isinstance(form, str) else int(form)
+        _check(lib().h2o_set_decode_form(self._h, f), "h2o_set_decode_form")
 
     def profile(self, on: bool = True):
         """Bracket each phase with CUDA events on the cache's stream."""

@@ -37,6 +37,7 @@ struct h2o_cache {
   cudaStream_t stream;
   int device;
   CacheView view;
+  int decode_form = 0;  // h2o_set_decode_form
   // phase timing (h2o_profile_enable / h2o_profile_read)
   bool profiling = false;
   struct Mark {
@@ -52,15 +53,13 @@ namespace {
 thread_local int g_last_cuda = 0;
 
 constexpr size_t kAlign = 256;
-constexpr int kMaxSplit = 64;
-constexpr int kMaxRowsPerSplit = 8192;
 constexpr int64_t kMaxPos = 0x7fffffffLL;  // positions are int32 tags
 
 size_t align_up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
 
 bool shape_ok(int B, int H, int d, int kh, int kl, h2o_dtype dt) {
   if (B < 1 || H < 1 || kh < 0 || kl < 0) return false;
-  if ((int64_t)kh + kl < 1 || (int64_t)kh + kl > (int64_t)kMaxSplit * kMaxRowsPerSplit - 1) return false;
+  if ((int64_t)kh + kl < 1 || (int64_t)kh + kl > (1 << 24)) return false;
   if ((int64_t)B * H > (1LL << 24)) return false;
   if (dt != H2O_F32 && dt != H2O_BF16) return false;
   return d >= 1;
@@ -68,23 +67,10 @@ bool shape_ok(int B, int H, int d, int kh, int kl, h2o_dtype dt) {
 
 bool d_supported(int d) { return d == 64 || d == 128; }
 
-// Splits per head for the decode launch: enough CTAs to give every SM about
-// eight, but no split shorter than 32 slot rows and none longer than
-// kMaxRowsPerSplit (the logits of a split live in shared memory).
-int choose_nsplit(int nh, int k, int sms) {
-  const int rows = k + 1;
-  int ns = (8 * sms + nh - 1) / nh;
-  const int by_rows = (rows + 31) / 32;
-  if (ns > by_rows) ns = by_rows;
-  const int min_ns = (rows + kMaxRowsPerSplit - 1) / kMaxRowsPerSplit;
-  if (ns < min_ns) ns = min_ns;
-  if (ns < 1) ns = 1;
-  if (ns > kMaxSplit) ns = kMaxSplit;
-  return ns;
-}
+int choose_nsplit(int nh, int k, int sms) { return h2o::decode_splits(nh, k, sms); }
 
 struct Layout {
-  size_t K, V, pos, score, part, logits, counter, err, total;
+  size_t K, V, pos, score, part, logits, counter, done, err, total;
 };
 
 Layout layout(int nh, int k, int d, int esize, int nsplit) {
@@ -97,6 +83,7 @@ Layout layout(int nh, int k, int d, int esize, int nsplit) {
   l.part = o;    o = align_up(o + (size_t)nh * nsplit * (2 + d) * sizeof(float));
   l.logits = o;  o = align_up(o + (size_t)nh * (k + 1) * sizeof(float));
   l.counter = o; o = align_up(o + (size_t)nh * sizeof(int));
+  l.done = o;    o = align_up(o + (size_t)nh * sizeof(int));
   l.err = o;     o = align_up(o + sizeof(int));
   l.total = o;
   return l;
@@ -188,6 +175,7 @@ h2o_status h2o_cache_create(int B, int H, int d, int k_heavy, int k_local, h2o_d
   v.pos = (int32_t *)(w + l.pos); v.score = (float *)(w + l.score);
   v.part = (float *)(w + l.part); v.logits = (float *)(w + l.logits);
   v.counter = (int *)(w + l.counter); v.err = (int *)(w + l.err);
+  v.done = (int *)(w + l.done);
   v.nsplit = ns;
   // Empty slots: pos = -1 (all bits set), score = 0, counters and flag 0.
   cudaError_t e = cudaMemsetAsync(v.pos, 0xff, (size_t)c->nh * c->k * sizeof(int32_t), c->stream);
@@ -295,7 +283,67 @@ h2o_status h2o_decode_steps(h2o_cache_t c, int n, const void *q, const void *k, 
   if (!c->prefilled) return H2O_ESTATE;
   if (c->next_pos + n > kMaxPos) return H2O_EINVAL;
   const size_t step = (size_t)c->nh * c->d * c->esize;
+  CacheView vc = c->view;  // cluster form: one cluster of <= 8 CTAs per head
+  if (vc.nsplit > 8) vc.nsplit = 8;
+  // Automatic choice (measured on GB300): the cluster form when every CTA's
+  // K/V rows stay resident in shared memory, else the cooperative grid when
+  // all (head, split) CTAs fit on the GPU at once, else the streaming cluster
+  // form, else one launch per step.
+  const int form = c->decode_form;
+  const bool cluster_ok = n >= 2 && decode_cluster_supported(vc);
+  const bool coop_ok = n >= 2 && (form == 0 || form == 2) && decode_persistent_fits(c->view);
+  bool use_cluster = false, use_coop = false;
+  if (form == 3) {
+    use_cluster = cluster_ok;
+  } else if (form == 2) {
+    use_coop = coop_ok;
+  } else if (form == 0) {
+    if (cluster_ok && decode_cluster_resident(vc))
+      use_cluster = true;
+    else if (coop_ok)
+      use_coop = true;
+    else
+      use_cluster = cluster_ok;
+  }
+  if (n >= 2 && ((form == 3 && !use_cluster) || (form == 2 && !use_coop))) return H2O_EUNSUPPORTED;
   PhaseTimer pt(c, 3, n);
+  if (use_cluster) {
+    DecodeStep s;
+    s.q = q;
+    s.kn = k;
+    s.vn = v;
+    s.out = out;
+    s.evicted = evicted;
+    s.n_valid = c->n_valid;
+    s.p = (int)c->next_pos;
+    cudaError_t e = launch_decode_cluster(vc, s, n, c->stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+    c->next_pos += n;
+    c->n_valid = (int)((int64_t)c->n_valid + n < c->k ? c->n_valid + n : c->k);
+    pt.done();
+    return H2O_OK;
+  }
+  if (use_coop) {
+    // One cooperative launch per chunk of steps (bounded launch length).
+    constexpr int kChunk = 16384;
+    for (int i0 = 0; i0 < n; i0 += kChunk) {
+      const int m = n - i0 < kChunk ? n - i0 : kChunk;
+      DecodeStep s;
+      s.q = (const char *)q + i0 * step;
+      s.kn = (const char *)k + i0 * step;
+      s.vn = (const char *)v + i0 * step;
+      s.out = (char *)out + i0 * step;
+      s.evicted = evicted ? evicted + (size_t)i0 * c->nh : nullptr;
+      s.n_valid = c->n_valid;
+      s.p = (int)c->next_pos;
+      cudaError_t e = launch_decode_persistent(c->view, s, m, c->view.done, c->stream);
+      if (e != cudaSuccess) return cuda_fail(e);
+      c->next_pos += m;
+      c->n_valid = (int)((int64_t)c->n_valid + m < c->k ? c->n_valid + m : c->k);
+    }
+    pt.done();
+    return H2O_OK;
+  }
   for (int i = 0; i < n; ++i) {
     DecodeStep s;
     s.q = (const char *)q + i * step;
@@ -316,6 +364,12 @@ h2o_status h2o_decode_steps(h2o_cache_t c, int n, const void *q, const void *k, 
 
 h2o_status h2o_decode_step(h2o_cache_t c, const void *q, const void *k, const void *v, void *out) {
   return h2o_decode_steps(c, 1, q, k, v, out, nullptr);
+}
+
+h2o_status h2o_set_decode_form(h2o_cache_t c, int form) {
+  if (!c || form < 0 || form > 3) return H2O_EINVAL;
+  c->decode_form = form;
+  return H2O_OK;
 }
 
 h2o_status h2o_cache_export(h2o_cache_t c, int32_t *pos, float *score, void *K, void *V, int64_t *next_pos,

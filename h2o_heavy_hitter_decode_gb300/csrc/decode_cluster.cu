@@ -1,0 +1,535 @@
+// decode_cluster.cu — many H2O decode steps in one launch, one thread-block
+// cluster per (batch, head).
+//
+// Same method as decode.cu (H2O summary page, "Algorithm / figure
+// walkthrough" steps 2-4): attend over the cache plus the new token, add each
+// exact weight to its entry's accumulated score, evict the lowest (score,
+// position) outside the k_local newest positions, write the new token in place.
+//
+// Layout of the work: the cluster's P CTAs split the head's k slots into
+// fixed ranges of `chunk` slots; CTA r owns slots [r*chunk, (r+1)*chunk).
+// Scores, position tags and the step's logits of its slots live in the CTA's
+// shared memory for the whole launch (read at the start, written back at the
+// end); K/V rows are streamed from HBM each step (4 KB cp.async.bulk slabs in
+// a 3-stage ring fed by a producer warp) or, when a CTA's rows fit, loaded
+// once and kept in shared memory.  Per step:
+//   1. consumer warps: logits of the owned rows (and, on rank 0, of the new
+//      token), per-warp online softmax -> the CTA's (m, l, acc[d]);
+//   2. cluster barrier; every CTA reads all (m, l) over DSMEM -> global (M, L);
+//      rank 0 merges the acc[d] partials into the output row;
+//   3. every CTA turns its logits into exact weights exp2(s - M) / L, adds them
+//      to its scores and takes its local (score, position) argmin over
+//      eligible slots (warp shuffles); cluster barrier;
+//   4. rank 0 reduces the P candidates, decides (admit / evict / drop the new
+//      token) and publishes the decision; cluster barrier;
+//   5. the owner of the chosen slot writes the new token's K/V row (HBM, and
+//      its resident copy) and its position tag and score.
+// All synchronisation is the cluster's hardware barrier or a CTA mbarrier
+// (bounded waits); there is no global atomic, fence round trip or spin between
+// CTAs, and clusters never wait on one another.
+#include <cooperative_groups.h>
+
+#include <climits>
+
+#include "common.cuh"
+#include "sm100.cuh"
+
+namespace cg = cooperative_groups;
+
+namespace h2o {
+namespace {
+
+using namespace sm100;
+
+constexpr int kConsumers = 4;
+constexpr int kConsumerThreads = 32 * kConsumers;
+constexpr int kThreads = kConsumerThreads + 32;  // + one producer warp
+constexpr int kMaxCluster = 8;
+constexpr int kStageBytes = 4096;  // per operand per slab
+constexpr int ring_bytes(int stages) { return stages * 2 * kStageBytes; }
+constexpr int kResidentMaxBytes = 96 * 1024;  // K+V rows of one CTA kept in shared memory
+
+template <typename T, int D> struct Geo {
+  static constexpr int EPL = VecN<T>::N;
+  static constexpr int LPR = D / EPL;
+  static constexpr int RPW = 32 / LPR;
+  static constexpr int ROWB = D * (int)sizeof(T);
+  static constexpr int TR = kStageBytes / ROWB;  // rows per slab
+  static constexpr int ITER = TR / (kConsumers * RPW);
+  static_assert(ITER >= 1 && TR % (kConsumers * RPW) == 0, "slab must split evenly over warps");
+};
+
+// Exchanged over DSMEM.
+struct __align__(16) Xchg {
+  float m, l;         // this CTA's softmax partial
+  float cand_s;       // local argmin candidate: score, position, slot (-2 none, -1 new token)
+  int cand_p, cand_slot;
+  int dec_e;          // rank 0: slot that takes the new token (-1: none)
+  float dec_w;        // rank 0: the new token's weight (its initial score)
+  int pad;
+};
+
+struct CArgs {
+  CacheView c;
+  DecodeStep s;  // first step; step i adds i * nh * d elements to q/k/v/out, i * nh to evicted
+  int nsteps;
+  int chunk;     // slots per CTA
+  float qscale;  // log2(e) / sqrt(d)
+};
+
+__device__ __forceinline__ void consumers_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+template <typename T, int D, bool kResident, int kStages>
+__global__ void __launch_bounds__(kThreads) decode_cluster_kernel(const CArgs a) {
+  using G = Geo<T, D>;
+  constexpr int EPL = G::EPL, LPR = G::LPR, RPW = G::RPW, ROWB = G::ROWB, TR = G::TR, ITER = G::ITER;
+  cg::cluster_group cluster = cg::this_cluster();
+  extern __shared__ __align__(1024) uint8_t smem[];
+  __shared__ uint64_t s_full[kStages], s_empty[kStages];
+  __shared__ float s_wm[kConsumers], s_wl[kConsumers];
+  __shared__ float s_wacc[kConsumers][D];
+  __shared__ __align__(16) float s_acc[D];  // this CTA's merged acc (read by rank 0 over DSMEM)
+  __shared__ Xchg s_x;
+  __shared__ float s_ML[2], s_lgnew, s_f[kMaxCluster];
+  __shared__ ArgMin s_am[kConsumers];
+  __shared__ int s_abort;
+
+  const CacheView &c = a.c;
+  const int P = (int)cluster.num_blocks();
+  const int rank = (int)cluster.block_rank();
+  const int h = blockIdx.x / P;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int sub = lane % LPR, grp = lane / LPR;
+  const int chunk = a.chunk;
+  const int s0 = rank * chunk;
+  const int own = max(0, min(c.k, s0 + chunk) - s0);  // slots owned
+  const size_t hk = (size_t)h * c.k;
+  const size_t step_elems = (size_t)c.nh * D;
+
+  // dynamic shared memory: [ring or resident K|V][score][pos][logit]
+  uint8_t *kv = smem;
+  const int kv_bytes = kResident ? 2 * chunk * ROWB : ring_bytes(kStages);
+  float *sc = (float *)(smem + kv_bytes);
+  int *ps = (int *)(sc + chunk);
+  float *lg = (float *)(ps + chunk);
+
+  if (tid == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_empty[i], kConsumers);
+    }
+    s_abort = 0;
+    fence_mbar_init();
+  }
+  for (int j = tid; j < own; j += kThreads) {
+    sc[j] = c.score[hk + s0 + j];
+    ps[j] = c.pos[hk + s0 + j];
+  }
+  __syncthreads();
+  if (kResident) {  // all owned rows, once
+    if (tid == 0 && own > 0) {
+      mbar_expect_tx(&s_full[0], 2u * own * ROWB);
+      bulk_load(kv, (const uint8_t *)c.K + (hk + s0) * ROWB, own * ROWB, &s_full[0]);
+      bulk_load(kv + chunk * ROWB, (const uint8_t *)c.V + (hk + s0) * ROWB, own * ROWB, &s_full[0]);
+    }
+    if (own > 0 && !__all_sync(0xffffffffu, mbar_wait(&s_full[0], 0)) && lane == 0) s_abort = 1;
+    __syncthreads();
+  }
+
+  // Step inputs do not depend on the cache: each step's q (consumers) and
+  // k_t/v_t (warp 0) are loaded one step ahead so their latency hides
+  // behind the current step.
+  uint4 q_next = make_uint4(0u, 0u, 0u, 0u), k_next = q_next, v_next = q_next;
+  if (warp < kConsumers) q_next = ld_nc16((const T *)a.s.q + (size_t)h * D + sub * EPL);
+  if (warp == 0) {
+    k_next = ld_nc16((const T *)a.s.kn + (size_t)h * D + sub * EPL);
+    v_next = ld_nc16((const T *)a.s.vn + (size_t)h * D + sub * EPL);
+  }
+
+  int g = 0;  // slabs streamed (ring position)
+  for (int step = 0; step < a.nsteps; ++step) {
+    const uint4 q_cur = q_next, k_cur = k_next, v_cur = v_next;
+    if (step + 1 < a.nsteps) {
+      const size_t nxt = (size_t)(step + 1) * step_elems + (size_t)h * D + sub * EPL;
+      if (warp < kConsumers) q_next = ld_nc16((const T *)a.s.q + nxt);
+      if (warp == 0) {
+        k_next = ld_nc16((const T *)a.s.kn + nxt);
+        v_next = ld_nc16((const T *)a.s.vn + nxt);
+      }
+    }
+    const int n = min(a.s.n_valid + step, c.k);
+    const int p = a.s.p + step;
+    const int nrows = max(0, min(own, n - s0));  // owned slots already filled
+    const int nst = kResident ? 0 : (nrows + TR - 1) / TR;
+    const bool aborted = *(volatile int *)&s_abort;
+    if (warp == kConsumers) {
+      // ---- producer (streaming form only)
+      if (!kResident && lane == 0 && !aborted) {
+        int issued = 0;
+        bool ok = true;
+        for (; issued < nst; ++issued) {
+          const int gi = g + issued, st = gi % kStages;
+          if (gi >= kStages && !(ok = mbar_wait(&s_empty[st], ((gi / kStages) - 1) & 1))) break;
+          const uint32_t bytes = (uint32_t)(min(TR, nrows - issued * TR) * ROWB);
+          const size_t off = (hk + s0 + (size_t)issued * TR) * ROWB;
+          mbar_expect_tx(&s_full[st], 2 * bytes);
+          bulk_load(kv + st * 2 * kStageBytes, (const uint8_t *)c.K + off, bytes, &s_full[st]);
+          bulk_load(kv + st * 2 * kStageBytes + kStageBytes, (const uint8_t *)c.V + off, bytes, &s_full[st]);
+        }
+        if (!ok) {
+          s_abort = 1;
+          atomicOr(c.err, 1);
+          for (int j = max(0, issued - kStages); j < issued; ++j)
+            mbar_wait(&s_full[(g + j) % kStages], ((g + j) / kStages) & 1);
+        }
+      }
+      g += nst;
+    } else if (!aborted) {
+      // ---- consumers: logits and per-warp online softmax over the owned rows
+      float qv[EPL];
+      Unpack<T>::run(q_cur, qv);
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) qv[e] *= a.qscale;
+      float m = -INFINITY, l = 0.f, acc[EPL];
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
+      const int nslab = kResident ? (nrows + TR - 1) / TR : nst;
+      bool ok = true;
+      for (int i = 0; i < nslab; ++i) {
+        const uint8_t *ks, *vs;
+        int st = 0;
+        if (kResident) {
+          ks = kv + (size_t)i * TR * ROWB;
+          vs = kv + (size_t)chunk * ROWB + (size_t)i * TR * ROWB;
+        } else {
+          st = g % kStages;
+          if (!(ok = __all_sync(0xffffffffu, mbar_wait(&s_full[st], (g / kStages) & 1)))) break;
+          ks = kv + st * 2 * kStageBytes;
+          vs = ks + kStageBytes;
+        }
+        const int rows = min(TR, nrows - i * TR);
+        float x[ITER];
+        float wmax = -INFINITY;
+#pragma unroll
+        for (int it = 0; it < ITER; ++it) {
+          const int r = warp * RPW + grp + it * kConsumers * RPW;
+          float kx[EPL];
+          Unpack<T>::run(*(const uint4 *)(ks + (r < rows ? r : 0) * ROWB + sub * 16), kx);
+          float dot = 0.f;
+#pragma unroll
+          for (int e = 0; e < EPL; ++e) dot = fmaf(qv[e], kx[e], dot);
+#pragma unroll
+          for (int o = LPR / 2; o; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+          x[it] = (r < rows) ? dot : -INFINITY;
+          if (r < rows && sub == 0) lg[i * TR + r] = dot;
+          wmax = fmaxf(wmax, x[it]);
+        }
+#pragma unroll
+        for (int o = LPR; o < 32; o <<= 1) wmax = fmaxf(wmax, __shfl_xor_sync(0xffffffffu, wmax, o));
+        if (wmax != -INFINITY) {
+          const float mn = fmaxf(m, wmax);
+          const float sc_ = exp2f(m - mn);
+          l *= sc_;
+#pragma unroll
+          for (int e = 0; e < EPL; ++e) acc[e] *= sc_;
+          m = mn;
+#pragma unroll
+          for (int it = 0; it < ITER; ++it) {
+            const int r = warp * RPW + grp + it * kConsumers * RPW;
+            if (r < rows) {
+              const float pr = exp2f(x[it] - m);
+              l += pr;
+              float vx[EPL];
+              Unpack<T>::run(*(const uint4 *)(vs + r * ROWB + sub * 16), vx);
+#pragma unroll
+              for (int e = 0; e < EPL; ++e) acc[e] = fmaf(pr, vx[e], acc[e]);
+            }
+          }
+        }
+        if (!kResident) {
+          ++g;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&s_empty[st]);
+        }
+      }
+      if (!ok && lane == 0) {
+        s_abort = 1;
+        atomicOr(c.err, 1);
+      }
+      if (rank == 0 && warp == 0) {  // the new token, from the step inputs
+        float kx[EPL];
+        Unpack<T>::run(k_cur, kx);
+        float dot = 0.f;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) dot = fmaf(qv[e], kx[e], dot);
+#pragma unroll
+        for (int o = LPR / 2; o; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+        if (lane == 0) s_lgnew = dot;
+        const float mn = fmaxf(m, dot);
+        const float sc_ = exp2f(m - mn);
+        l *= sc_;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) acc[e] *= sc_;
+        m = mn;
+        if (grp == 0) {
+          const float pr = exp2f(dot - m);
+          l += pr;
+          float vx[EPL];
+          Unpack<T>::run(v_cur, vx);
+#pragma unroll
+          for (int e = 0; e < EPL; ++e) acc[e] = fmaf(pr, vx[e], acc[e]);
+        }
+      }
+#pragma unroll
+      for (int o = LPR; o < 32; o <<= 1) {
+        l += __shfl_xor_sync(0xffffffffu, l, o);
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], o);
+      }
+      if (grp == 0) {
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) s_wacc[warp][sub * EPL + e] = acc[e];
+      }
+      if (lane == 0) {
+        s_wm[warp] = m;
+        s_wl[warp] = l;
+      }
+      consumers_sync();
+      // merge the warps into this CTA's partial (published for rank 0)
+      float M = s_wm[0];
+#pragma unroll
+      for (int w = 1; w < kConsumers; ++w) M = fmaxf(M, s_wm[w]);
+      float f[kConsumers];
+#pragma unroll
+      for (int w = 0; w < kConsumers; ++w) f[w] = (s_wm[w] == -INFINITY) ? 0.f : exp2f(s_wm[w] - M);
+      for (int col = tid; col < D; col += kConsumerThreads) {
+        float t = 0.f;
+#pragma unroll
+        for (int w = 0; w < kConsumers; ++w) t = fmaf(f[w], s_wacc[w][col], t);
+        s_acc[col] = t;
+      }
+      if (tid == 0) {
+        float ls = 0.f;
+#pragma unroll
+        for (int w = 0; w < kConsumers; ++w) ls = fmaf(f[w], s_wl[w], ls);
+        s_x.m = M;
+        s_x.l = ls;
+      }
+    }
+    cluster.sync();  // #1: every CTA's (m, l, acc) published
+
+    // ---- global softmax statistics (identical in every CTA); lane r reads rank r
+    if (warp == 0) {
+      float mr = -INFINITY, lr = 0.f;
+      if (lane < P) {
+        const Xchg *x = cluster.map_shared_rank(&s_x, lane);
+        mr = x->m;
+        lr = x->l;
+      }
+      const float Mg = warp_max(mr);
+      const float fr = (mr == -INFINITY) ? 0.f : exp2f(mr - Mg);
+      const float Lg = warp_sum(fr * lr);
+      if (lane < P) s_f[lane] = fr;
+      if (lane == 0) {
+        s_ML[0] = Mg;
+        s_ML[1] = Lg;
+      }
+    }
+    __syncthreads();
+    const float Mg = s_ML[0], invL = 1.f / s_ML[1];
+    if (rank == 0) {  // the step's output row
+      T *out = (T *)a.s.out + step * step_elems + (size_t)h * D;
+      for (int col = tid; col < D; col += kThreads) {
+        float o = 0.f;
+#pragma unroll
+        for (int r = 0; r < kMaxCluster; ++r)
+          if (r < P && s_f[r] != 0.f) o = fmaf(s_f[r], cluster.map_shared_rank(s_acc, r)[col], o);
+        out[col] = from_f32<T>(o * invL);
+      }
+    }
+
+    // ---- exact weights into the owned scores; local argmin
+    const long long lim = (long long)p - c.kl;  // eligible iff pos <= p - k_local
+    ArgMin best{INFINITY, INT_MAX, -2};
+    if (warp < kConsumers) {
+      for (int j = tid; j < nrows; j += kConsumerThreads) {
+        const float w = exp2f(lg[j] - Mg) * invL;
+        const float s_new = sc[j] + w;
+        sc[j] = s_new;
+        if ((long long)ps[j] <= lim) {
+          const ArgMin cand{s_new, ps[j], s0 + j};
+          if (am_less(cand, best)) best = cand;
+        }
+      }
+    }
+    const float w_new = (rank == 0) ? exp2f(s_lgnew - Mg) * invL : 0.f;
+    if (rank == 0 && tid == 0 && c.kl == 0) {
+      const ArgMin cand{w_new, p, -1};
+      if (am_less(cand, best)) best = cand;
+    }
+    if (warp < kConsumers) {
+      best = warp_argmin(best);
+      if (lane == 0) s_am[warp] = best;
+    }
+    __syncthreads();
+    if (tid == 0) {
+      ArgMin b = s_am[0];
+      for (int w = 1; w < kConsumers; ++w)
+        if (am_less(s_am[w], b)) b = s_am[w];
+      s_x.cand_s = b.s;
+      s_x.cand_p = b.p;
+      s_x.cand_slot = b.slot;
+    }
+    cluster.sync();  // #2: candidates published
+
+    if (rank == 0 && warp == 0) {  // lane r reads rank r's candidate
+      ArgMin b{INFINITY, INT_MAX, -2};
+      if (lane < P) {
+        const Xchg *x = cluster.map_shared_rank(&s_x, lane);
+        b = ArgMin{x->cand_s, x->cand_p, x->cand_slot};
+      }
+      b = warp_argmin(b);
+      if (lane == 0) {
+        int e = -1, ev = -1;
+        if (n < c.k) {
+          e = n;  // |S| < k: admit into the next free slot
+        } else if (b.slot == -2) {
+          atomicOr(c.err, 1);  // no eviction candidate: inconsistent state
+        } else if (b.slot == -1) {
+          ev = p;  // the new token itself scores lowest (k_local = 0)
+        } else {
+          e = b.slot;
+          ev = b.p;
+        }
+        if (a.s.evicted) a.s.evicted[(size_t)step * c.nh + h] = ev;
+        s_x.dec_e = e;
+        s_x.dec_w = w_new;
+      }
+    }
+    cluster.sync();  // #3: decision published
+
+    {
+      const Xchg *d0 = cluster.map_shared_rank(&s_x, 0);
+      const int e = d0->dec_e;
+      if (e >= s0 && e < s0 + own) {  // this CTA owns the slot that takes the new token
+        const int j = e - s0;
+        if (tid == 0) {
+          ps[j] = p;
+          sc[j] = d0->dec_w;
+        }
+        if (warp == 0 && grp == 0) {  // lanes 0..LPR-1 hold the whole k_t / v_t row
+          const int i = sub;
+          const uint4 kq = k_cur, vq = v_cur;
+          ((uint4 *)((T *)c.K + (hk + e) * D))[i] = kq;
+          ((uint4 *)((T *)c.V + (hk + e) * D))[i] = vq;
+          if (kResident) {
+            ((uint4 *)(kv + (size_t)j * ROWB))[i] = kq;
+            ((uint4 *)(kv + (size_t)chunk * ROWB + (size_t)j * ROWB))[i] = vq;
+          }
+        }
+        fence_proxy_async_smem();
+        asm volatile("fence.proxy.async.global;" ::: "memory");  // before our next bulk reads of row e
+      }
+    }
+    __syncthreads();
+  }
+  // write back the owned scores and tags; the cluster stays alive until every
+  // CTA is done reading rank 0's shared memory
+  for (int j = tid; j < own; j += kThreads) {
+    c.score[hk + s0 + j] = sc[j];
+    c.pos[hk + s0 + j] = ps[j];
+  }
+  cluster.sync();
+}
+
+template <typename T, int D>
+int resident_rows_ok(int chunk) {
+  return 2 * chunk * Geo<T, D>::ROWB <= kResidentMaxBytes;
+}
+
+template <typename T, int D, bool R, int S>
+int smem_bytes(int chunk) {
+  return (R ? 2 * chunk * Geo<T, D>::ROWB : ring_bytes(S)) + 3 * chunk * 4;
+}
+
+template <typename T, int D, bool R, int S>
+cudaError_t launch_cluster_t(const CacheView &c, const DecodeStep &s, int nsteps, cudaStream_t st) {
+  const int P = c.nsplit;
+  CArgs a{c, s, nsteps, (c.k + P - 1) / P, kLog2e / sqrtf((float)D)};
+  const int smem = smem_bytes<T, D, R, S>(a.chunk);
+  if (smem > 200 * 1024) return cudaErrorInvalidValue;
+  static bool attr_done[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 || !attr_done[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(decode_cluster_kernel<T, D, R, S>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_done[dev] = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(c.nh * P));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)P;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_cluster_kernel<T, D, R, S>, a);
+}
+
+// Resident K/V when a CTA's rows fit.  Otherwise a 3-stage ring, unless two
+// stages are what lets every CTA of the grid be resident at once (a partial
+// last wave of whole-run CTAs would stream at a fraction of the bandwidth).
+template <typename T, int D>
+cudaError_t dispatch_t(const CacheView &c, const DecodeStep &s, int nsteps, cudaStream_t st) {
+  const int chunk = (c.k + c.nsplit - 1) / c.nsplit;
+  if (resident_rows_ok<T, D>(chunk)) return launch_cluster_t<T, D, true, 1>(c, s, nsteps, st);
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const long long ctas = (long long)c.nh * c.nsplit;
+  auto fits = [&](auto kernel, int smem) {
+    int per_sm = 0;
+    cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, smem) != cudaSuccess) return false;
+    return ctas <= (long long)per_sm * sms;
+  };
+  if (!fits(decode_cluster_kernel<T, D, false, 3>, smem_bytes<T, D, false, 3>(chunk)) &&
+      fits(decode_cluster_kernel<T, D, false, 2>, smem_bytes<T, D, false, 2>(chunk)))
+    return launch_cluster_t<T, D, false, 2>(c, s, nsteps, st);
+  return launch_cluster_t<T, D, false, 3>(c, s, nsteps, st);
+}
+
+}  // namespace
+
+bool decode_cluster_resident(const CacheView &c) {
+  if (c.nsplit < 1 || c.nsplit > kMaxCluster) return false;
+  const int chunk = (c.k + c.nsplit - 1) / c.nsplit;
+  return 2 * chunk * c.d * (c.dtype == 1 ? 2 : 4) <= kResidentMaxBytes;
+}
+
+bool decode_cluster_supported(const CacheView &c) {
+  if (c.nsplit < 1 || c.nsplit > kMaxCluster) return false;
+  const int chunk = (c.k + c.nsplit - 1) / c.nsplit;
+  const int row = c.d * (c.dtype == 1 ? 2 : 4);
+  const int kv = (2 * chunk * row <= kResidentMaxBytes) ? 2 * chunk * row : ring_bytes(3);
+  return kv + 3 * chunk * 4 <= 200 * 1024;
+}
+
+cudaError_t launch_decode_cluster(const CacheView &c, const DecodeStep &s, int nsteps, cudaStream_t st) {
+  if (!decode_cluster_supported(c) || nsteps < 1) return cudaErrorInvalidValue;
+  if (c.dtype == 1) {
+    if (c.d == 128) return dispatch_t<__nv_bfloat16, 128>(c, s, nsteps, st);
+    if (c.d == 64) return dispatch_t<__nv_bfloat16, 64>(c, s, nsteps, st);
+  } else {
+    if (c.d == 128) return dispatch_t<float, 128>(c, s, nsteps, st);
+    if (c.d == 64) return dispatch_t<float, 64>(c, s, nsteps, st);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace h2o

@@ -14,8 +14,6 @@ namespace {
 
 constexpr size_t kScratchBytes = H2O_STATIC_SCRATCH_BYTES;
 constexpr size_t kAlign = 256;
-constexpr int kMaxSplit = 64;
-constexpr int kMaxRowsPerSplit = 8192;
 constexpr int kMaxDevices = 256;
 
 // Split partials, logits, arrival counters and the flag of one call.  Shared by
@@ -27,20 +25,6 @@ std::mutex g_setup_mu;
 void *g_scratch_addr[kMaxDevices];  // device address of g_scratch, per device
 
 size_t up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
-
-// Same split rule as a cache's decode launch: ~8 CTAs per SM, >= 32 rows per
-// split, <= kMaxRowsPerSplit rows per split.
-int splits(int nh, int k, int sms) {
-  const int rows = k + 1;
-  int ns = (8 * sms + nh - 1) / nh;
-  const int by_rows = (rows + 31) / 32;
-  if (ns > by_rows) ns = by_rows;
-  const int min_ns = (rows + kMaxRowsPerSplit - 1) / kMaxRowsPerSplit;
-  if (ns < min_ns) ns = min_ns;
-  if (ns < 1) ns = 1;
-  if (ns > kMaxSplit) ns = kMaxSplit;
-  return ns;
-}
 
 bool a16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
@@ -54,7 +38,7 @@ extern "C" h2o_status h2o_decode_step_static(int B, int H, int d, int k_heavy, i
   if (B < 1 || H < 1 || k_heavy < 0 || k_local < 0) return H2O_EINVAL;
   if ((int64_t)B * H > (1LL << 24)) return H2O_EINVAL;
   const int64_t k64 = (int64_t)k_heavy + k_local;
-  if (k64 < 1 || k64 > (int64_t)kMaxSplit * kMaxRowsPerSplit - 1) return H2O_EINVAL;
+  if (k64 < 1 || k64 > (1 << 24)) return H2O_EINVAL;
   if (dtype != H2O_F32 && dtype != H2O_BF16) return H2O_EINVAL;
   if (d != 64 && d != 128) return H2O_EUNSUPPORTED;
   if (!K || !V || !pos || !score || !q_t || !k_t || !v_t || !out) return H2O_EINVAL;
@@ -69,7 +53,7 @@ extern "C" h2o_status h2o_decode_step_static(int B, int H, int d, int k_heavy, i
   if (dev < 0 || dev >= kMaxDevices) return H2O_EUNSUPPORTED;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
     return H2O_ECUDA;
-  const int ns = splits(nh, k, sms);
+  const int ns = h2o::decode_splits(nh, k, sms);
 
   // Carve the fixed array like a cache workspace's scratch sections.
   const size_t off_part = 0;
@@ -100,6 +84,7 @@ extern "C" h2o_status h2o_decode_step_static(int B, int H, int d, int k_heavy, i
   c.logits = (float *)(s + off_logits);
   c.counter = (int *)(s + off_counter);
   c.err = (int *)(s + off_err);
+  c.done = nullptr;  // single steps only
   c.nsplit = ns;
 
   // The arrival counters (and the flag right after them) must start at zero;

@@ -18,6 +18,7 @@ struct CacheView {
   float *logits;     // [nh][k + 1]           log2-domain logits of the step
   int *counter;      // [nh]                  split arrival counters (zero between launches)
   int *err;          // [1]                   sticky device error flag
+  int *done;         // [nh]                  per-head step flags of a persistent decode launch
   int nsplit;
 };
 
@@ -32,6 +33,22 @@ struct DecodeStep {
 // Decode: one launch per step (split-K + last-arriver combine, score
 // update, argmin, in-place write).
 cudaError_t launch_decode_step(const CacheView &c, const DecodeStep &s, cudaStream_t st);
+// Persistent multi-step decode: one cooperative grid runs `nsteps` steps
+// (all (head, split) CTAs resident; per-head release/acquire step flags in
+// `done`, zeroed by the launcher).  decode_persistent_fits says whether the
+// grid can be co-resident on the current device.
+bool decode_persistent_fits(const CacheView &c);
+cudaError_t launch_decode_persistent(const CacheView &c, const DecodeStep &s, int nsteps, int *done,
+                                     cudaStream_t st);
+// Multi-step decode with one thread-block cluster per head (c.nsplit CTAs,
+// at most 8): scores/tags/logits in shared memory, DSMEM exchange, hardware
+// cluster barriers; no global scratch.
+bool decode_cluster_supported(const CacheView &c);
+bool decode_cluster_resident(const CacheView &c);  // each CTA's K/V rows stay in shared memory
+cudaError_t launch_decode_cluster(const CacheView &c, const DecodeStep &s, int nsteps, cudaStream_t st);
+// Split count of the decode launch for nh heads of k slots on `sms` SMs
+// (fixes the size of the split-partial scratch).
+int decode_splits(int nh, int k, int sms);
 
 // Prefill pass 1 (causal attention -> O, lse) and pass 2 (column sums).
 cudaError_t launch_prefill_attn(const CacheView &c, const void *Q, const void *K, const void *V,

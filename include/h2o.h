@@ -107,6 +107,19 @@ h2o_status h2o_decode_step(h2o_cache_t cache, const void *q_t, const void *k_t, 
 h2o_status h2o_decode_steps(h2o_cache_t cache, int n, const void *q, const void *k, const void *v,
                             void *out, int32_t *evicted);
 
+/* How h2o_decode_steps runs n >= 2 steps (all forms compute the same thing;
+ * single steps always use form 1):
+ *   0  automatic (default): 3 if the shape allows it, else 2, else 1;
+ *   1  one launch per step, chained with programmatic dependent launch;
+ *   2  one cooperative launch: each (head, split) CTA loops over the steps,
+ *      waiting (bounded, acquire) only on its own head's previous step;
+ *   3  one launch with a thread-block cluster of up to 8 CTAs per head:
+ *      scores and tags stay in shared memory, partials and the eviction
+ *      decision move over distributed shared memory, cluster barriers only.
+ * A form the shape or device cannot run makes h2o_decode_steps return
+ * H2O_EUNSUPPORTED (nothing launched). */
+h2o_status h2o_set_decode_form(h2o_cache_t cache, int form);
+
 /* Copy the cache state out to device buffers: pos [B][H][k] int32,
  * score [B][H][k] fp32, K, V [B][H][k][d] (any may be NULL); next_pos and
  * n_valid (host, may be NULL) receive the position the next decode token

@@ -96,7 +96,8 @@ def compare_scores(rep: Report, g_pos, g_score, o_st: oracle.State, heads):
         rep.max_score_rel = max(rep.max_score_rel, _rel(np.array([gm[p] for p in keys]), np.array([om[p] for p in keys])))
 
 
-def run_parity(w, T=None, heads=None, resync=True, check=True, prompt=None, dec=None, want_O=True):
+def run_parity(w, T=None, heads=None, resync=True, check=True, prompt=None, dec=None, want_O=True,
+               decode_form="auto"):
     """Prefill + T decode steps on the GPU through the C ABI, against the
     oracle on `heads` (all heads when None; resynchronisation needs all)."""
     T = w.T if T is None else T
@@ -108,6 +109,7 @@ def run_parity(w, T=None, heads=None, resync=True, check=True, prompt=None, dec=
     Qs, Ks, Vs = prompt if prompt is not None else synth.prompt(w)
 
     cache = H2OCache(w.B, w.H, w.d, w.k_heavy, w.k_local, tdtype(w))
+    cache.set_decode_form(decode_form)
     shp = (w.B, w.H, w.L, w.d)
     O, lse, colsum = cache.prefill(to_dev(Qs, w, shp), to_dev(Ks, w, shp), to_dev(Vs, w, shp), want_O=want_O)
     torch.cuda.synchronize()

@@ -61,6 +61,20 @@ def test_small_all_heads_without_O(w):
     assert rep.steps_compared >= w.T
 
 
+FORM_CASES = [SMALL[0], SMALL[1], SMALL[2], SMALL[3], SMALL[6], SMALL[9],
+              small("bf16_many_heads_long_budget", 4, 6, 128, 700, 40, 200, 100, "bf16")]
+
+
+@pytest.mark.parametrize("form", ["per_step", "cooperative", "cluster"])
+@pytest.mark.parametrize("w", FORM_CASES, ids=lambda w: w.name)
+def test_decode_forms(w, form):
+    """Every multi-step decode form (per-step launches, cooperative
+    persistent grid, one cluster per head) matches the oracle."""
+    rep, cache = run_parity(w, decode_form=form)
+    print(w.name, form, rep)
+    assert rep.steps_compared >= w.T
+
+
 def _sample(w, count, seed=5):
     rng = np.random.default_rng(seed)
     return sorted(rng.choice(w.nh, size=min(count, w.nh), replace=False).tolist())

@@ -59,16 +59,6 @@ template <typename T, int D> struct Geo {
   static_assert(ITER >= 1 && TR % (kConsumers * RPW) == 0, "slab must split evenly over warps");
 };
 
-// Exchanged over DSMEM.
-struct __align__(16) Xchg {
-  float m, l;         // this CTA's softmax partial
-  float cand_s;       // local argmin candidate: score, position, slot (-2 none, -1 new token)
-  int cand_p, cand_slot;
-  int dec_e;          // rank 0: slot that takes the new token (-1: none)
-  float dec_w;        // rank 0: the new token's weight (its initial score)
-  int pad;
-};
-
 struct CArgs {
   CacheView c;
   DecodeStep s;  // first step; step i adds i * nh * d elements to q/k/v/out, i * nh to evicted
@@ -80,16 +70,23 @@ struct CArgs {
 __device__ __forceinline__ void consumers_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
 template <typename T, int D, bool kResident, int kStages>
-__global__ void __launch_bounds__(kThreads) decode_cluster_kernel(const CArgs a) {
+__global__ void __launch_bounds__(kThreads, 7) decode_cluster_kernel(const CArgs a) {
   using G = Geo<T, D>;
   constexpr int EPL = G::EPL, LPR = G::LPR, RPW = G::RPW, ROWB = G::ROWB, TR = G::TR, ITER = G::ITER;
   cg::cluster_group cluster = cg::this_cluster();
   extern __shared__ __align__(1024) uint8_t smem[];
   __shared__ uint64_t s_full[kStages], s_empty[kStages];
+  __shared__ uint64_t s_inbar[2];                      // step inputs landed (one phase per use)
+  __shared__ __align__(16) T s_in[2][3][D];            // q, k_t, v_t of two steps
   __shared__ float s_wm[kConsumers], s_wl[kConsumers];
   __shared__ float s_wacc[kConsumers][D];
-  __shared__ __align__(16) float s_acc[D];  // this CTA's merged acc (read by rank 0 over DSMEM)
-  __shared__ Xchg s_x;
+  // Exchange buffers, filled by the peers' DSMEM stores (pushes) before a
+  // cluster barrier and read locally after it.
+  __shared__ float s_mlx[kMaxCluster][2];                  // every rank's (m, l), in every CTA
+  __shared__ __align__(16) float s_accx[kMaxCluster][D];   // every rank's acc row (used on rank 0)
+  __shared__ ArgMin s_candx[kMaxCluster];                  // every rank's candidate (used on rank 0)
+  __shared__ int s_dec_e;                                  // rank 0's decision, in every CTA
+  __shared__ float s_dec_w;
   __shared__ float s_ML[2], s_lgnew, s_f[kMaxCluster];
   __shared__ ArgMin s_am[kConsumers];
   __shared__ int s_abort;
@@ -118,6 +115,8 @@ __global__ void __launch_bounds__(kThreads) decode_cluster_kernel(const CArgs a)
       mbar_init(&s_full[i], 1);
       mbar_init(&s_empty[i], kConsumers);
     }
+    mbar_init(&s_inbar[0], 1);
+    mbar_init(&s_inbar[1], 1);
     s_abort = 0;
     fence_mbar_init();
   }
@@ -136,27 +135,24 @@ __global__ void __launch_bounds__(kThreads) decode_cluster_kernel(const CArgs a)
     __syncthreads();
   }
 
-  // Step inputs do not depend on the cache: each step's q (consumers) and
-  // k_t/v_t (warp 0) are loaded one step ahead so their latency hides
-  // behind the current step.
-  uint4 q_next = make_uint4(0u, 0u, 0u, 0u), k_next = q_next, v_next = q_next;
-  if (warp < kConsumers) q_next = ld_nc16((const T *)a.s.q + (size_t)h * D + sub * EPL);
-  if (warp == 0) {
-    k_next = ld_nc16((const T *)a.s.kn + (size_t)h * D + sub * EPL);
-    v_next = ld_nc16((const T *)a.s.vn + (size_t)h * D + sub * EPL);
-  }
+  // Step inputs do not depend on the cache: the producer lane copies each
+  // step's q, k_t and v_t rows into shared memory one step ahead.
+  auto fetch_inputs = [&](int st_i) {
+    const size_t off = (size_t)st_i * step_elems + (size_t)h * D;
+    uint64_t *bar = &s_inbar[st_i & 1];
+    mbar_expect_tx(bar, 3 * D * (int)sizeof(T));
+    bulk_load(s_in[st_i & 1][0], (const T *)a.s.q + off, D * sizeof(T), bar);
+    bulk_load(s_in[st_i & 1][1], (const T *)a.s.kn + off, D * sizeof(T), bar);
+    bulk_load(s_in[st_i & 1][2], (const T *)a.s.vn + off, D * sizeof(T), bar);
+  };
+  if (tid == kConsumerThreads) fetch_inputs(0);
 
   int g = 0;  // slabs streamed (ring position)
   for (int step = 0; step < a.nsteps; ++step) {
-    const uint4 q_cur = q_next, k_cur = k_next, v_cur = v_next;
-    if (step + 1 < a.nsteps) {
-      const size_t nxt = (size_t)(step + 1) * step_elems + (size_t)h * D + sub * EPL;
-      if (warp < kConsumers) q_next = ld_nc16((const T *)a.s.q + nxt);
-      if (warp == 0) {
-        k_next = ld_nc16((const T *)a.s.kn + nxt);
-        v_next = ld_nc16((const T *)a.s.vn + nxt);
-      }
-    }
+    // inputs of this step (buffer step&1) and, ahead, of the next one
+    if (tid == kConsumerThreads && step + 1 < a.nsteps) fetch_inputs(step + 1);
+    if (!__all_sync(0xffffffffu, mbar_wait(&s_inbar[step & 1], (step >> 1) & 1)) && lane == 0) s_abort = 1;
+    const T *in_q = s_in[step & 1][0], *in_k = s_in[step & 1][1], *in_v = s_in[step & 1][2];
     const int n = min(a.s.n_valid + step, c.k);
     const int p = a.s.p + step;
     const int nrows = max(0, min(own, n - s0));  // owned slots already filled
@@ -187,7 +183,7 @@ __global__ void __launch_bounds__(kThreads) decode_cluster_kernel(const CArgs a)
     } else if (!aborted) {
       // ---- consumers: logits and per-warp online softmax over the owned rows
       float qv[EPL];
-      Unpack<T>::run(q_cur, qv);
+      Unpack<T>::run(*(const uint4 *)(in_q + sub * EPL), qv);
 #pragma unroll
       for (int e = 0; e < EPL; ++e) qv[e] *= a.qscale;
       float m = -INFINITY, l = 0.f, acc[EPL];
@@ -258,7 +254,7 @@ __global__ void __launch_bounds__(kThreads) decode_cluster_kernel(const CArgs a)
       }
       if (rank == 0 && warp == 0) {  // the new token, from the step inputs
         float kx[EPL];
-        Unpack<T>::run(k_cur, kx);
+        Unpack<T>::run(*(const uint4 *)(in_k + sub * EPL), kx);
         float dot = 0.f;
 #pragma unroll
         for (int e = 0; e < EPL; ++e) dot = fmaf(qv[e], kx[e], dot);
@@ -275,7 +271,7 @@ __global__ void __launch_bounds__(kThreads) decode_cluster_kernel(const CArgs a)
           const float pr = exp2f(dot - m);
           l += pr;
           float vx[EPL];
-          Unpack<T>::run(v_cur, vx);
+          Unpack<T>::run(*(const uint4 *)(in_v + sub * EPL), vx);
 #pragma unroll
           for (int e = 0; e < EPL; ++e) acc[e] = fmaf(pr, vx[e], acc[e]);
         }
@@ -306,25 +302,25 @@ __global__ void __launch_bounds__(kThreads) decode_cluster_kernel(const CArgs a)
         float t = 0.f;
 #pragma unroll
         for (int w = 0; w < kConsumers; ++w) t = fmaf(f[w], s_wacc[w][col], t);
-        s_acc[col] = t;
+        *cluster.map_shared_rank(&s_accx[rank][col], 0) = t;  // to rank 0
       }
-      if (tid == 0) {
+      if (tid < P) {  // (m, l) to every rank
         float ls = 0.f;
 #pragma unroll
         for (int w = 0; w < kConsumers; ++w) ls = fmaf(f[w], s_wl[w], ls);
-        s_x.m = M;
-        s_x.l = ls;
+        float *dst = cluster.map_shared_rank(&s_mlx[rank][0], tid);
+        dst[0] = M;
+        dst[1] = ls;
       }
     }
     cluster.sync();  // #1: every CTA's (m, l, acc) published
 
-    // ---- global softmax statistics (identical in every CTA); lane r reads rank r
+    // ---- global softmax statistics (identical in every CTA), from local copies
     if (warp == 0) {
       float mr = -INFINITY, lr = 0.f;
       if (lane < P) {
-        const Xchg *x = cluster.map_shared_rank(&s_x, lane);
-        mr = x->m;
-        lr = x->l;
+        mr = s_mlx[lane][0];
+        lr = s_mlx[lane][1];
       }
       const float Mg = warp_max(mr);
       const float fr = (mr == -INFINITY) ? 0.f : exp2f(mr - Mg);
@@ -341,9 +337,8 @@ __global__ void __launch_bounds__(kThreads) decode_cluster_kernel(const CArgs a)
       T *out = (T *)a.s.out + step * step_elems + (size_t)h * D;
       for (int col = tid; col < D; col += kThreads) {
         float o = 0.f;
-#pragma unroll
-        for (int r = 0; r < kMaxCluster; ++r)
-          if (r < P && s_f[r] != 0.f) o = fmaf(s_f[r], cluster.map_shared_rank(s_acc, r)[col], o);
+        for (int r = 0; r < P; ++r)
+          if (s_f[r] != 0.f) o = fmaf(s_f[r], s_accx[r][col], o);
         out[col] = from_f32<T>(o * invL);
       }
     }
@@ -376,50 +371,44 @@ __global__ void __launch_bounds__(kThreads) decode_cluster_kernel(const CArgs a)
       ArgMin b = s_am[0];
       for (int w = 1; w < kConsumers; ++w)
         if (am_less(s_am[w], b)) b = s_am[w];
-      s_x.cand_s = b.s;
-      s_x.cand_p = b.p;
-      s_x.cand_slot = b.slot;
+      *cluster.map_shared_rank(&s_candx[rank], 0) = b;  // to rank 0
     }
     cluster.sync();  // #2: candidates published
 
-    if (rank == 0 && warp == 0) {  // lane r reads rank r's candidate
+    if (rank == 0 && warp == 0) {  // lane r holds rank r's candidate
       ArgMin b{INFINITY, INT_MAX, -2};
-      if (lane < P) {
-        const Xchg *x = cluster.map_shared_rank(&s_x, lane);
-        b = ArgMin{x->cand_s, x->cand_p, x->cand_slot};
-      }
+      if (lane < P) b = s_candx[lane];
       b = warp_argmin(b);
-      if (lane == 0) {
-        int e = -1, ev = -1;
-        if (n < c.k) {
-          e = n;  // |S| < k: admit into the next free slot
-        } else if (b.slot == -2) {
-          atomicOr(c.err, 1);  // no eviction candidate: inconsistent state
-        } else if (b.slot == -1) {
-          ev = p;  // the new token itself scores lowest (k_local = 0)
-        } else {
-          e = b.slot;
-          ev = b.p;
-        }
-        if (a.s.evicted) a.s.evicted[(size_t)step * c.nh + h] = ev;
-        s_x.dec_e = e;
-        s_x.dec_w = w_new;
+      int e = -1, ev = -1;
+      if (n < c.k) {
+        e = n;  // |S| < k: admit into the next free slot
+      } else if (b.slot == -2) {
+        if (lane == 0) atomicOr(c.err, 1);  // no eviction candidate: inconsistent state
+      } else if (b.slot == -1) {
+        ev = p;  // the new token itself scores lowest (k_local = 0)
+      } else {
+        e = b.slot;
+        ev = b.p;
+      }
+      if (lane == 0 && a.s.evicted) a.s.evicted[(size_t)step * c.nh + h] = ev;
+      if (lane < P) {  // decision to every rank
+        *cluster.map_shared_rank(&s_dec_e, lane) = e;
+        *cluster.map_shared_rank(&s_dec_w, lane) = w_new;
       }
     }
     cluster.sync();  // #3: decision published
 
     {
-      const Xchg *d0 = cluster.map_shared_rank(&s_x, 0);
-      const int e = d0->dec_e;
+      const int e = s_dec_e;
       if (e >= s0 && e < s0 + own) {  // this CTA owns the slot that takes the new token
         const int j = e - s0;
         if (tid == 0) {
           ps[j] = p;
-          sc[j] = d0->dec_w;
+          sc[j] = s_dec_w;
         }
-        if (warp == 0 && grp == 0) {  // lanes 0..LPR-1 hold the whole k_t / v_t row
+        if (warp == 0 && grp == 0) {  // lanes 0..LPR-1 copy the k_t / v_t row
           const int i = sub;
-          const uint4 kq = k_cur, vq = v_cur;
+          const uint4 kq = *(const uint4 *)(in_k + i * EPL), vq = *(const uint4 *)(in_v + i * EPL);
           ((uint4 *)((T *)c.K + (hk + e) * D))[i] = kq;
           ((uint4 *)((T *)c.V + (hk + e) * D))[i] = vq;
           if (kResident) {
@@ -433,8 +422,8 @@ __global__ void __launch_bounds__(kThreads) decode_cluster_kernel(const CArgs a)
     }
     __syncthreads();
   }
-  // write back the owned scores and tags; the cluster stays alive until every
-  // CTA is done reading rank 0's shared memory
+  // write back the owned scores and tags; no CTA leaves while a peer could
+  // still store into its shared memory
   for (int j = tid; j < own; j += kThreads) {
     c.score[hk + s0 + j] = sc[j];
     c.pos[hk + s0 + j] = ps[j];
@@ -481,25 +470,39 @@ cudaError_t launch_cluster_t(const CacheView &c, const DecodeStep &s, int nsteps
   return cudaLaunchKernelEx(&cfg, decode_cluster_kernel<T, D, R, S>, a);
 }
 
-// Resident K/V when a CTA's rows fit.  Otherwise a 3-stage ring, unless two
-// stages are what lets every CTA of the grid be resident at once (a partial
-// last wave of whole-run CTAs would stream at a fraction of the bandwidth).
+template <typename T, int D, bool R, int S>
+bool all_resident(const CacheView &c, int chunk) {
+  int dev = 0, sms = 0, per_sm = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
+  const int smem = smem_bytes<T, D, R, S>(chunk);
+  if (smem > 200 * 1024) return false;
+  if (cudaFuncSetAttribute(decode_cluster_kernel<T, D, R, S>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           200 * 1024) != cudaSuccess)
+    return false;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_cluster_kernel<T, D, R, S>, kThreads, smem) !=
+      cudaSuccess)
+    return false;
+  return (long long)c.nh * c.nsplit <= (long long)per_sm * sms;
+}
+
+// K/V resident in shared memory when a CTA's rows fit AND every CTA of the
+// grid is resident at once (each CTA runs all steps of its head, so a second
+// wave would start only when the first finished).
+template <typename T, int D>
+bool resident_t(const CacheView &c) {
+  const int chunk = (c.k + c.nsplit - 1) / c.nsplit;
+  return resident_rows_ok<T, D>(chunk) && all_resident<T, D, true, 1>(c, chunk);
+}
+
+// Streaming: a 3-stage ring, unless two stages are what lets every CTA be
+// resident at once (a partial last wave of whole-run CTAs streams at a
+// fraction of the bandwidth).
 template <typename T, int D>
 cudaError_t dispatch_t(const CacheView &c, const DecodeStep &s, int nsteps, cudaStream_t st) {
   const int chunk = (c.k + c.nsplit - 1) / c.nsplit;
-  if (resident_rows_ok<T, D>(chunk)) return launch_cluster_t<T, D, true, 1>(c, s, nsteps, st);
-  int dev = 0, sms = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const long long ctas = (long long)c.nh * c.nsplit;
-  auto fits = [&](auto kernel, int smem) {
-    int per_sm = 0;
-    cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, smem) != cudaSuccess) return false;
-    return ctas <= (long long)per_sm * sms;
-  };
-  if (!fits(decode_cluster_kernel<T, D, false, 3>, smem_bytes<T, D, false, 3>(chunk)) &&
-      fits(decode_cluster_kernel<T, D, false, 2>, smem_bytes<T, D, false, 2>(chunk)))
+  if (resident_t<T, D>(c)) return launch_cluster_t<T, D, true, 1>(c, s, nsteps, st);
+  if (!all_resident<T, D, false, 3>(c, chunk) && all_resident<T, D, false, 2>(c, chunk))
     return launch_cluster_t<T, D, false, 2>(c, s, nsteps, st);
   return launch_cluster_t<T, D, false, 3>(c, s, nsteps, st);
 }
@@ -508,8 +511,40 @@ cudaError_t dispatch_t(const CacheView &c, const DecodeStep &s, int nsteps, cuda
 
 bool decode_cluster_resident(const CacheView &c) {
   if (c.nsplit < 1 || c.nsplit > kMaxCluster) return false;
+  if (c.dtype == 1) {
+    if (c.d == 128) return resident_t<__nv_bfloat16, 128>(c);
+    if (c.d == 64) return resident_t<__nv_bfloat16, 64>(c);
+  } else {
+    if (c.d == 128) return resident_t<float, 128>(c);
+    if (c.d == 64) return resident_t<float, 64>(c);
+  }
+  return false;
+}
+
+template <typename T, int D>
+bool cluster_waves_ok_t(const CacheView &c) {
   const int chunk = (c.k + c.nsplit - 1) / c.nsplit;
-  return 2 * chunk * c.d * (c.dtype == 1 ? 2 : 4) <= kResidentMaxBytes;
+  if (resident_t<T, D>(c) || all_resident<T, D, false, 3>(c, chunk) || all_resident<T, D, false, 2>(c, chunk))
+    return true;
+  int dev = 0, sms = 0, per_sm = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_cluster_kernel<T, D, false, 3>, kThreads,
+                                                    smem_bytes<T, D, false, 3>(chunk)) != cudaSuccess)
+    return false;
+  return (long long)c.nh * c.nsplit >= 3LL * per_sm * sms;
+}
+
+bool decode_cluster_preferred(const CacheView &c) {
+  if (c.nsplit < 1 || c.nsplit > kMaxCluster) return false;
+  if (c.dtype == 1) {
+    if (c.d == 128) return cluster_waves_ok_t<__nv_bfloat16, 128>(c);
+    if (c.d == 64) return cluster_waves_ok_t<__nv_bfloat16, 64>(c);
+  } else {
+    if (c.d == 128) return cluster_waves_ok_t<float, 128>(c);
+    if (c.d == 64) return cluster_waves_ok_t<float, 64>(c);
+  }
+  return false;
 }
 
 bool decode_cluster_supported(const CacheView &c) {

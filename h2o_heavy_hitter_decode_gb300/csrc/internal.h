@@ -45,6 +45,9 @@ cudaError_t launch_decode_persistent(const CacheView &c, const DecodeStep &s, in
 // cluster barriers; no global scratch.
 bool decode_cluster_supported(const CacheView &c);
 bool decode_cluster_resident(const CacheView &c);  // each CTA's K/V rows stay in shared memory
+// The cluster grid runs in one wave, or in enough waves that a partial last
+// wave still streams at full bandwidth.
+bool decode_cluster_preferred(const CacheView &c);
 cudaError_t launch_decode_cluster(const CacheView &c, const DecodeStep &s, int nsteps, cudaStream_t st);
 // Split count of the decode launch for nh heads of k slots on `sms` SMs
 // (fixes the size of the split-partial scratch).

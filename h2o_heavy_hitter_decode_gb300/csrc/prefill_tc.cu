@@ -36,7 +36,7 @@ using namespace sm100;
 constexpr int kRows = 128;            // tile rows (TMEM lanes / MMA M and N)
 constexpr int kBox = kRows * 128;     // bytes of one 64-column bf16 box
 constexpr int kStages = 2;            // streamed-tile ring depth
-constexpr int kThreads = 128;
+constexpr int kThreads = 256;  // 8 epilogue warps: 2 per TMEM lane quarter, 64 columns each
 
 template <int D> struct TileGeo {
   static constexpr int kBoxes = D / 64;
@@ -53,6 +53,13 @@ struct __align__(8) SmallState {
   uint32_t tmem_base;
   int abort;
 };
+
+// This warp's 32 TMEM lanes x 64 columns: two loads in flight, one wait.
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
+  tmem_ld32(taddr, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+  tmem_ld32(taddr + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+  tmem_ld_wait();
+}
 
 // Bounded wait whose outcome is the same for the whole warp (so the warp's
 // collective TMEM loads after it stay uniform even on a timeout).
@@ -84,7 +91,8 @@ __device__ __forceinline__ void load_tile(uint8_t *dst, const CUtensorMap *map, 
 
 // Shared skeleton: the resident tile (A) at row r0 of `mapA`, streamed tiles
 // j = 0..n-1 of `mapB` at rows s0 + 128 j.  `Epi` is called by all threads with
-// (j, TMEM address of this warp's lanes for tile j) and must read the tile.
+// (j, TMEM address of this warp's 32 lanes and 64-column half of tile j) and
+// must read it.
 template <int D, class Prep, class Epi>
 __device__ __forceinline__ bool tile_pipeline(uint8_t *smem, SmallState &st, const CUtensorMap *mapA,
                                               const CUtensorMap *mapB, int r0, int s0, int n, int h,
@@ -147,7 +155,7 @@ __device__ __forceinline__ bool tile_pipeline(uint8_t *smem, SmallState &st, con
         load_tile<D>(sB + (j % kStages) * G::kTileBytes, mapB, &st.ld_bar[j % kStages], s0 + kRows * loads, h);
         ++loads;
       }
-      epi(j, tbase + ((uint32_t)(warp * 32) << 16) + (uint32_t)(j & 1) * 128);
+      epi(j, tbase + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)(j & 1) * 128 + (uint32_t)(warp >> 2) * 64);
     }
     if (j + 1 < n) prep(j + 1);
     tc_fence_before();
@@ -173,46 +181,50 @@ __device__ __forceinline__ bool tile_pipeline(uint8_t *smem, SmallState &st, con
 template <int D>
 __global__ void __launch_bounds__(kThreads, 2)
     colsum_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-              const float *__restrict__ lse, float *__restrict__ colsum, int L, int nh, float qscale, int *err) {
+              const float *__restrict__ lse, float *__restrict__ colsum, int L, int nkt, float qscale, int *err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = align1024(smem_raw);
   using G = TileGeo<D>;
   float *nl2 = (float *)(smem + G::kTileBytes * (1 + kStages));  // [2][128]: -LSE*log2(e) per query
   SmallState &st = *(SmallState *)(nl2 + 2 * kRows);
   if (*(volatile int *)err) return;
-  // Heaviest CTAs (first key tiles: most query tiles) get the lowest indices.
-  const int kt = blockIdx.x / nh, h = blockIdx.x % nh;
+  // Head-major (a head's CTAs share its Q tiles in L2), heaviest key tile first.
+  const int h = blockIdx.x / nkt, kt = blockIdx.x % nkt;
   const int k0 = kt * kRows;
   const int nq = (L - k0 + kRows - 1) / kRows;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int row = (warp & 3) * 32 + lane;  // key within the tile (TMEM lane)
+  const int c_off = (warp >> 2) * 64;      // this warp's query columns
   const float *lse_h = lse + (size_t)h * L;
   auto prep = [&](int j) {
-    const int q = k0 + kRows * j + tid;
-    nl2[(j & 1) * kRows + tid] = q < L ? -__ldg(lse_h + q) * kLog2e : -INFINITY;
+    if (tid < kRows) {
+      const int q = k0 + kRows * j + tid;
+      nl2[(j & 1) * kRows + tid] = q < L ? -__ldg(lse_h + q) * kLog2e : -INFINITY;
+    }
   };
   float acc = 0.f;
   auto epi = [&](int j, uint32_t taddr) {
-    const float *nl = nl2 + (j & 1) * kRows;
-#pragma unroll 1
-    for (int c0 = 0; c0 < kRows; c0 += 32) {
-      uint32_t r[32];
-      tmem_ld32(taddr + c0, r);
-      tmem_ld_wait();
-      if (j == 0) {  // diagonal tile: query column c contributes iff c >= key row
+    const float *nl = nl2 + (j & 1) * kRows + c_off;
+    uint32_t r[64];
+    tmem_ld64(taddr, r);
+    if (j == 0) {  // diagonal tile: query column c contributes iff c >= key row
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float e = ex2(fmaf(__uint_as_float(r[i]), qscale, nl[c0 + i]));
-          acc += (c0 + i >= tid) ? e : 0.f;
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) acc += ex2(fmaf(__uint_as_float(r[i]), qscale, nl[c0 + i]));
+      for (int i = 0; i < 64; ++i) {
+        const float e = ex2(fmaf(__uint_as_float(r[i]), qscale, nl[i]));
+        acc += (c_off + i >= row) ? e : 0.f;
       }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 64; ++i) acc += ex2(fmaf(__uint_as_float(r[i]), qscale, nl[i]));
     }
   };
   const bool ok = tile_pipeline<D>(smem, st, &tmK, &tmQ, k0, k0, nq, h, prep, epi);
+  // the two column halves of each key row: the second half hands its sum over
+  float *half = nl2;  // free after the pipeline
+  if (ok && warp >= 4) half[row] = acc;
+  __syncthreads();
   if (ok) {
-    if (k0 + tid < L) colsum[(size_t)h * L + k0 + tid] = acc;
+    if (warp < 4 && k0 + row < L) colsum[(size_t)h * L + k0 + row] = acc + half[row];
   } else if (tid == 0) {
     atomicOr(err, 4);
   }
@@ -222,45 +234,55 @@ __global__ void __launch_bounds__(kThreads, 2)
 template <int D>
 __global__ void __launch_bounds__(kThreads, 2)
     lse_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-           float *__restrict__ lse, int L, int nh, int nqt, float qscale, int *err) {
+           float *__restrict__ lse, int L, int nqt, float qscale, int *err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = align1024(smem_raw);
   using G = TileGeo<D>;
-  SmallState &st = *(SmallState *)(smem + G::kTileBytes * (1 + kStages) + 2 * kRows * 4);
+  float *xch = (float *)(smem + G::kTileBytes * (1 + kStages));  // [2][128] hand-over of the second halves
+  SmallState &st = *(SmallState *)(xch + 2 * kRows);
   if (*(volatile int *)err) return;
-  // Heaviest CTAs (last query tiles: most key tiles) first.
-  const int qt = nqt - 1 - blockIdx.x / nh, h = blockIdx.x % nh;
+  // Head-major (a head's CTAs share its K tiles in L2), heaviest query tile first.
+  const int h = blockIdx.x / nqt, qt = nqt - 1 - blockIdx.x % nqt;
   const int q0 = qt * kRows;
   const int nk = qt + 1;  // key tiles 0 .. diagonal
-  const int tid = threadIdx.x;
-  float m = -INFINITY, l = 0.f;  // base-2 running max and sum of this query row
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int row = (warp & 3) * 32 + lane;  // query within the tile (TMEM lane)
+  const int c_off = (warp >> 2) * 64;      // this warp's key columns
+  float m = -INFINITY, l = 0.f;  // base-2 running max and sum over this thread's columns
   auto prep = [](int) {};
   auto epi = [&](int j, uint32_t taddr) {
     const bool diag = (j == nk - 1);
-#pragma unroll 1
-    for (int c0 = 0; c0 < kRows; c0 += 32) {
-      uint32_t r[32];
-      tmem_ld32(taddr + c0, r);
-      tmem_ld_wait();
-      float x[32];
-      float cm = -INFINITY;
+    uint32_t r[64];
+    tmem_ld64(taddr, r);
+    float cm = -INFINITY;
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        x[i] = __uint_as_float(r[i]) * qscale;
-        if (diag && c0 + i > tid) x[i] = -INFINITY;  // key after the query
-        cm = fmaxf(cm, x[i]);
-      }
-      const float mn = fmaxf(m, cm);
-      float s = 0.f;
-#pragma unroll
-      for (int i = 0; i < 32; ++i) s += ex2(x[i] - mn);
-      l = l * ex2(m - mn) + s;
-      m = mn;
+    for (int i = 0; i < 64; ++i) {
+      float x = __uint_as_float(r[i]) * qscale;
+      if (diag && c_off + i > row) x = -INFINITY;  // key after the query
+      r[i] = __float_as_uint(x);
+      cm = fmaxf(cm, x);
     }
+    if (cm == -INFINITY) return;  // every column masked (second half of the diagonal)
+    const float mn = fmaxf(m, cm);
+    float sum = 0.f;
+#pragma unroll
+    for (int i = 0; i < 64; ++i) sum += ex2(__uint_as_float(r[i]) - mn);
+    l = l * ex2(m - mn) + sum;
+    m = mn;
   };
   const bool ok = tile_pipeline<D>(smem, st, &tmQ, &tmK, q0, 0, nk, h, prep, epi);
+  if (ok && warp >= 4) {
+    xch[row] = m;
+    xch[kRows + row] = l;
+  }
+  __syncthreads();
   if (ok) {
-    if (q0 + tid < L) lse[(size_t)h * L + q0 + tid] = (m + __log2f(l)) * kLn2;
+    if (warp < 4 && q0 + row < L) {
+      const float m2 = xch[row], l2 = xch[kRows + row];
+      const float mm = fmaxf(m, m2);
+      const float ll = (m == -INFINITY ? 0.f : l * ex2(m - mm)) + (m2 == -INFINITY ? 0.f : l2 * ex2(m2 - mm));
+      lse[(size_t)h * L + q0 + row] = (mm + __log2f(ll)) * kLn2;
+    }
   } else if (tid == 0) {
     atomicOr(err, 8);
   }
@@ -289,8 +311,11 @@ struct __align__(8) OutState {
   int abort;
 };
 
+constexpr int kOutSoftmaxWarps = 8;  // 2 per TMEM lane quarter, 64 key columns each
+constexpr int kOutThreads = 32 * (kOutSoftmaxWarps + 1);
+
 template <int D>
-__global__ void __launch_bounds__(160, 1)
+__global__ void __launch_bounds__(kOutThreads, 1)
     attn_out_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const float *__restrict__ lse, __nv_bfloat16 *__restrict__ O,
                 int L, int nh, int nqt, float qscale, int *err) {
@@ -304,7 +329,8 @@ __global__ void __launch_bounds__(160, 1)
   uint8_t *sP = smem + 5 * kT;     // 2 buffers of kP
   OutState &st = *(OutState *)(sP + 2 * G::kP);
   if (*(volatile int *)err) return;
-  const int qt = nqt - 1 - blockIdx.x / nh, h = blockIdx.x % nh;
+  // Head-major (a head's CTAs share its K/V tiles in L2), heaviest query tile first.
+  const int h = blockIdx.x / nqt, qt = nqt - 1 - blockIdx.x % nqt;
   const int q0 = qt * kRows;
   const int n = qt + 1;  // key tiles 0 .. diagonal
   const int tid = threadIdx.x, warp = tid >> 5;
@@ -315,8 +341,8 @@ __global__ void __launch_bounds__(160, 1)
       mbar_init(&st.kfull[b], 1);
       mbar_init(&st.vfull[b], 1);
       mbar_init(&st.sfull[b], 1);
-      mbar_init(&st.sfree[b], 128);
-      mbar_init(&st.pfull[b], 128);
+      mbar_init(&st.sfree[b], 32 * kOutSoftmaxWarps);
+      mbar_init(&st.pfull[b], 32 * kOutSoftmaxWarps);
       mbar_init(&st.pvdone[b], 1);
     }
     mbar_init(&st.drain, 1);
@@ -333,7 +359,7 @@ __global__ void __launch_bounds__(160, 1)
   const uint32_t tbase = st.tmem_base;  // S buffers at columns 0 and 128, O at 256
   const uint32_t tO = tbase + 256;
 
-  if (warp == 4) {
+  if (warp == kOutSoftmaxWarps) {
     if ((tid & 31) == 0) {
       constexpr uint32_t idO = idesc_bf16_f32(128, D, true);
       int kl = 0, vl = 0, mS = 0, mPV = 0;  // TMA loads and MMAs issued
@@ -392,42 +418,39 @@ __global__ void __launch_bounds__(160, 1)
       (void)mPV;
     }
   } else {
-    // Softmax warps: thread tid owns query row q0 + tid (TMEM lane tid).
-    const int q = q0 + tid;
+    // Softmax warps: query row `row` (TMEM lane), key columns c_off .. c_off+63.
+    const int lane = tid & 31;
+    const int row = (warp & 3) * 32 + lane;
+    const int half = warp >> 2;
+    const int c_off = half * 64;
+    const int q = q0 + row;
     const float nl2 = q < L ? -__ldg(lse + (size_t)h * L + q) * kLog2e : 0.f;
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-    const int sw = tid & 7;
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const int sw = row & 7;
     bool ok = true;
     for (int j = 0; j < n; ++j) {
       if (j >= 2 && !(ok = wait_warp(&st.pvdone[j & 1], ((j - 2) >> 1) & 1))) break;
       if (!(ok = wait_warp(&st.sfull[j & 1], (j >> 1) & 1))) break;
       tc_fence_after();
       const bool diag = (j == n - 1);
-      uint8_t *prow = sP + (j & 1) * G::kP + tid * 128;
-#pragma unroll 1
-      for (int c0 = 0; c0 < 128; c0 += 32) {
-        uint32_t r[32];
-        tmem_ld32(tbase + lane_off + (uint32_t)(j & 1) * 128 + c0, r);
-        tmem_ld_wait();
-        uint32_t pk[16];
+      uint32_t r[64];
+      tmem_ld64(tbase + lane_off + (uint32_t)(j & 1) * 128 + (uint32_t)c_off, r);
+      uint32_t pk[32];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          float a = ex2(fmaf(__uint_as_float(r[2 * i]), qscale, nl2));
-          float b = ex2(fmaf(__uint_as_float(r[2 * i + 1]), qscale, nl2));
-          if (diag && c0 + 2 * i > tid) a = 0.f;
-          if (diag && c0 + 2 * i + 1 > tid) b = 0.f;
-          __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
-          pk[i] = *reinterpret_cast<uint32_t *>(&v);
-        }
-        // 32 keys = four 16-byte chunks of box c0/64, swizzled by row.
-        uint8_t *box = prow + (c0 >> 6) * kBox;
-#pragma unroll
-        for (int cch = 0; cch < 4; ++cch) {
-          const int logical = ((c0 & 63) >> 3) + cch;
-          *reinterpret_cast<uint4 *>(box + ((logical ^ sw) << 4)) =
-              make_uint4(pk[4 * cch], pk[4 * cch + 1], pk[4 * cch + 2], pk[4 * cch + 3]);
-        }
+      for (int i = 0; i < 32; ++i) {
+        float a = ex2(fmaf(__uint_as_float(r[2 * i]), qscale, nl2));
+        float b = ex2(fmaf(__uint_as_float(r[2 * i + 1]), qscale, nl2));
+        if (diag && c_off + 2 * i > row) a = 0.f;
+        if (diag && c_off + 2 * i + 1 > row) b = 0.f;
+        __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+        pk[i] = *reinterpret_cast<uint32_t *>(&v);
       }
+      // 64 keys = one 128-byte row of box `half`: eight 16-byte chunks, swizzled by row.
+      uint8_t *prow = sP + (j & 1) * G::kP + half * kBox + row * 128;
+#pragma unroll
+      for (int cch = 0; cch < 8; ++cch)
+        *reinterpret_cast<uint4 *>(prow + ((cch ^ sw) << 4)) =
+            make_uint4(pk[4 * cch], pk[4 * cch + 1], pk[4 * cch + 2], pk[4 * cch + 3]);
       tc_fence_before();
       mbar_arrive(&st.sfree[j & 1]);
       fence_proxy_async_smem();
@@ -436,11 +459,12 @@ __global__ void __launch_bounds__(160, 1)
     if (ok) ok = wait_warp(&st.pvdone[(n - 1) & 1], ((n - 1) >> 1) & 1);
     if (ok) {
       tc_fence_after();
-      __nv_bfloat16 *orow = O + ((size_t)h * L + (q < L ? q : 0)) * D;
+      constexpr int kCols = D / 2;  // output columns of this warp
+      __nv_bfloat16 *orow = O + ((size_t)h * L + (q < L ? q : 0)) * D + half * kCols;
 #pragma unroll 1
-      for (int c0 = 0; c0 < D; c0 += 32) {  // collective loads: every lane, every chunk
+      for (int c0 = 0; c0 < kCols; c0 += 32) {  // collective loads: every lane, every chunk
         uint32_t r[32];
-        tmem_ld32(tO + lane_off + c0, r);
+        tmem_ld32(tO + lane_off + (uint32_t)(half * kCols + c0), r);
         tmem_ld_wait();
         if (q < L) {
           uint32_t pk[16];
@@ -505,7 +529,7 @@ cudaError_t colsum_t(const CacheView &c, const void *Q, const void *K, const flo
   if (e != cudaSuccess) return e;
   const int nkt = (L + kRows - 1) / kRows;
   const long long grid = (long long)nkt * c.nh;
-  colsum_tc<D><<<(unsigned)grid, kThreads, smem, st>>>(mq, mk, lse, colsum, L, c.nh, kLog2e / sqrtf((float)D),
+  colsum_tc<D><<<(unsigned)grid, kThreads, smem, st>>>(mq, mk, lse, colsum, L, nkt, kLog2e / sqrtf((float)D),
                                                       c.err);
   return cudaGetLastError();
 }
@@ -521,7 +545,7 @@ cudaError_t attn_out_t(const CacheView &c, const void *Q, const void *K, const v
   if (e != cudaSuccess) return e;
   const int nqt = (L + kRows - 1) / kRows;
   const long long grid = (long long)nqt * c.nh;
-  attn_out_tc<D><<<(unsigned)grid, 160, smem, st>>>(mq, mk, mv, lse, (__nv_bfloat16 *)O, L, c.nh, nqt,
+  attn_out_tc<D><<<(unsigned)grid, kOutThreads, smem, st>>>(mq, mk, mv, lse, (__nv_bfloat16 *)O, L, c.nh, nqt,
                                                      kLog2e / sqrtf((float)D), c.err);
   return cudaGetLastError();
 }
@@ -535,7 +559,7 @@ cudaError_t lse_t(const CacheView &c, const void *Q, const void *K, float *lse, 
   if (e != cudaSuccess) return e;
   const int nqt = (L + kRows - 1) / kRows;
   const long long grid = (long long)nqt * c.nh;
-  lse_tc<D><<<(unsigned)grid, kThreads, smem, st>>>(mq, mk, lse, L, c.nh, nqt, kLog2e / sqrtf((float)D), c.err);
+  lse_tc<D><<<(unsigned)grid, kThreads, smem, st>>>(mq, mk, lse, L, nqt, kLog2e / sqrtf((float)D), c.err);
   return cudaGetLastError();
 }
 

@@ -36,7 +36,8 @@ using namespace sm100;
 constexpr int kRows = 128;            // tile rows (TMEM lanes / MMA M and N)
 constexpr int kBox = kRows * 128;     // bytes of one 64-column bf16 box
 constexpr int kStages = 2;            // streamed-tile ring depth
-constexpr int kThreads = 256;  // 8 epilogue warps: 2 per TMEM lane quarter, 64 columns each
+constexpr int kEpiWarps = 8;   // epilogue warps: 2 per TMEM lane quarter, 64 columns each
+constexpr int kThreads = 32 * (kEpiWarps + 1);  // + one producer warp (TMA, MMA, column vector)
 
 template <int D> struct TileGeo {
   static constexpr int kBoxes = D / 64;
@@ -48,8 +49,11 @@ template <int D> struct TileGeo {
 
 struct __align__(8) SmallState {
   uint64_t res_bar;
-  uint64_t ld_bar[kStages];
-  uint64_t mma_bar[2];
+  uint64_t ld_bar[kStages];   // streamed tile landed
+  uint64_t ld_free[kStages];  // the MMA that read the stage is done
+  uint64_t mma_full[2];       // accumulator (and its column vector) ready
+  uint64_t acc_empty[2];      // epilogue warps done with the accumulator
+  uint64_t drain;
   uint32_t tmem_base;
   int abort;
 };
@@ -89,22 +93,32 @@ __device__ __forceinline__ void load_tile(uint8_t *dst, const CUtensorMap *map, 
   for (int b = 0; b < TileGeo<D>::kBoxes; ++b) tma_load_3d(dst + b * kBox, map, bar, b * 64, row, h);
 }
 
-// Shared skeleton: the resident tile (A) at row r0 of `mapA`, streamed tiles
-// j = 0..n-1 of `mapB` at rows s0 + 128 j.  `Epi` is called by all threads with
-// (j, TMEM address of this warp's 32 lanes and 64-column half of tile j) and
-// must read it.
-template <int D, class Prep, class Epi>
+// Shared skeleton, warp-specialised.  The resident tile (A) comes from row r0
+// of `mapA`; streamed tiles j = 0..n-1 of `mapB` from rows s0 + 128 j.  Warp 8
+// (the producer) issues the TMA loads and the MMAs into two TMEM accumulators
+// and, per tile, fills that tile's column vector with `prep(j, lane)` before
+// marking the accumulator full; warps 0-7 wait for it, call `epi(j, taddr)`
+// with the TMEM address of their 32 lanes and 64-column half, and release
+// the accumulator.  No CTA-wide barrier inside the loop.
+template <int D, bool kPrep, class Prep, class Epi>
 __device__ __forceinline__ bool tile_pipeline(uint8_t *smem, SmallState &st, const CUtensorMap *mapA,
                                               const CUtensorMap *mapB, int r0, int s0, int n, int h,
                                               Prep &&prep, Epi &&epi) {
   using G = TileGeo<D>;
-  const int tid = threadIdx.x, warp = tid >> 5;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   uint8_t *sA = smem;
   uint8_t *sB = smem + G::kTileBytes;
   if (tid == 0) {
     mbar_init(&st.res_bar, 1);
-    for (int s = 0; s < kStages; ++s) mbar_init(&st.ld_bar[s], 1);
-    for (int b = 0; b < 2; ++b) mbar_init(&st.mma_bar[b], 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&st.ld_bar[s], 1);
+      mbar_init(&st.ld_free[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&st.mma_full[b], kPrep ? 2 : 1);
+      mbar_init(&st.acc_empty[b], kEpiWarps);
+    }
+    mbar_init(&st.drain, 1);
     st.abort = 0;
     fence_mbar_init();
   }
@@ -112,67 +126,82 @@ __device__ __forceinline__ bool tile_pipeline(uint8_t *smem, SmallState &st, con
     tmem_alloc(&st.tmem_base, 256);
     tmem_relinquish();
   }
-  prep(0);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = st.tmem_base;
 
-  int loads = 0, mmas = 0;  // issued by thread 0
-  if (tid == 0) {
-    load_tile<D>(sA, mapA, &st.res_bar, r0, h);
-    for (; loads < n && loads < kStages; ++loads)
-      load_tile<D>(sB + loads * G::kTileBytes, mapB, &st.ld_bar[loads], s0 + kRows * loads, h);
-  }
-  auto issue = [&](int j) -> bool {  // thread 0
-    if (!mbar_wait(&st.ld_bar[j % kStages], (j / kStages) & 1)) return false;
-    tc_fence_after();
-    mma_tile<D>(tbase + (uint32_t)(j & 1) * 128, smem_u32(sA), smem_u32(sB + (j % kStages) * G::kTileBytes));
-    umma_commit(&st.mma_bar[j & 1]);
-    return true;
-  };
-  if (tid == 0) {
-    if (mbar_wait(&st.res_bar, 0) && issue(0))
-      mmas = 1;
-    else
-      st.abort = 1;
-  }
-  int done = 0;  // tiles whose MMA this thread saw complete
-  for (int j = 0; j < n; ++j) {
-    if (tid == 0 && !st.abort && j + 1 < n) {
-      if (issue(j + 1))
-        mmas = j + 2;
-      else
-        st.abort = 1;
+  if (warp == kEpiWarps) {
+    // ------------------------------------------------------------ producer
+    int loads = 0, mmas = 0;
+    bool ok = true;
+    if (lane == 0) {
+      load_tile<D>(sA, mapA, &st.res_bar, r0, h);
+      for (; loads < n && loads < kStages; ++loads)
+        load_tile<D>(sB + loads * G::kTileBytes, mapB, &st.ld_bar[loads], s0 + kRows * loads, h);
+      ok = mbar_wait(&st.res_bar, 0);
     }
-    // Warp-uniform: the epilogue's TMEM loads are warp-collective.
-    const bool ready = __all_sync(0xffffffffu, (j < mmas || tid != 0) && mbar_wait(&st.mma_bar[j & 1], (j >> 1) & 1));
-    if (!ready) st.abort = 1;
-    tc_fence_after();
-    if (ready) {
-      done = j + 1;
-      if (tid == 0 && loads < n && loads == j + kStages) {
-        load_tile<D>(sB + (j % kStages) * G::kTileBytes, mapB, &st.ld_bar[j % kStages], s0 + kRows * loads, h);
-        ++loads;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (kPrep) prep.load(0, lane);
+    for (int j = 0; ok && j < n; ++j) {
+      // the whole warp observes the accumulator (and its column vector) free
+      if (j >= 2 && !(ok = wait_warp(&st.acc_empty[j & 1], ((j - 2) >> 1) & 1))) break;
+      if (lane == 0) {
+        ok = mbar_wait(&st.ld_bar[j % kStages], (j / kStages) & 1);
+        if (ok) {
+          tc_fence_after();
+          mma_tile<D>(tbase + (uint32_t)(j & 1) * 128, smem_u32(sA), smem_u32(sB + (j % kStages) * G::kTileBytes));
+          umma_commit(&st.mma_full[j & 1]);
+          umma_commit(&st.ld_free[j % kStages]);
+          mmas = j + 1;
+        }
       }
-      epi(j, tbase + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)(j & 1) * 128 + (uint32_t)(warp >> 2) * 64);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      if (kPrep) {  // the accumulator buffer's column vector (free: its epilogue is done)
+        prep.store(j, lane);
+        if (j + 1 < n) prep.load(j + 1, lane);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&st.mma_full[j & 1]);
+      }
+      // refill the stage of tile j-1 (its MMA is done or nearly) with tile j-1+kStages
+      if (lane == 0 && j >= 1 && loads < n && loads == j - 1 + kStages) {
+        const int sj = (j - 1) % kStages;
+        ok = mbar_wait(&st.ld_free[sj], ((j - 1) / kStages) & 1);
+        if (ok) {
+          load_tile<D>(sB + sj * G::kTileBytes, mapB, &st.ld_bar[sj], s0 + kRows * loads, h);
+          ++loads;
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
     }
-    if (j + 1 < n) prep(j + 1);
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (st.abort) break;
-  }
-  const bool ok = !st.abort;
-  if (!ok && tid == 0) {
-    // Drain: tensor-core work and TMA copies this CTA started must land
-    // before its shared memory and TMEM are released.
-    for (int j = done; j < mmas; ++j) mbar_wait(&st.mma_bar[j & 1], (j >> 1) & 1);
-    for (int j = mmas; j < loads; ++j) mbar_wait(&st.ld_bar[j % kStages], (j / kStages) & 1);
+    if (!ok && lane == 0) {
+      st.abort = 1;
+      // Drain: tensor-core work and TMA copies this CTA started must land
+      // before its shared memory and TMEM are released.
+      umma_commit(&st.drain);
+      mbar_wait(&st.drain, 0);
+      for (int j = mmas; j < loads; ++j) mbar_wait(&st.ld_bar[j % kStages], (j / kStages) & 1);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const uint32_t lane_off = ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)(warp >> 2) * 64;
+    for (int j = 0; j < n; ++j) {
+      if (!wait_warp(&st.mma_full[j & 1], (j >> 1) & 1)) {
+        if (lane == 0) st.abort = 1;
+        break;
+      }
+      tc_fence_after();
+      epi(j, tbase + lane_off + (uint32_t)(j & 1) * 128);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&st.acc_empty[j & 1]);
+    }
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  const bool ok = !*(volatile int *)&st.abort;
   if (warp == 0) tmem_dealloc(tbase, 256);
   return ok;
 }
@@ -196,12 +225,26 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int row = (warp & 3) * 32 + lane;  // key within the tile (TMEM lane)
   const int c_off = (warp >> 2) * 64;      // this warp's query columns
   const float *lse_h = lse + (size_t)h * L;
-  auto prep = [&](int j) {
-    if (tid < kRows) {
-      const int q = k0 + kRows * j + tid;
-      nl2[(j & 1) * kRows + tid] = q < L ? -__ldg(lse_h + q) * kLog2e : -INFINITY;
+  // Column vector of query tile j: -LSE * log2(e) (-inf past L, so those
+  // zero-filled query rows add nothing), four queries per producer lane,
+  // loaded one tile ahead.
+  struct Prep {
+    const float *lse_h;
+    float *nl2;
+    int k0, L;
+    float v[4];
+    __device__ void load(int j, int ln) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int q = k0 + kRows * j + ln + 32 * i;
+        v[i] = q < L ? -__ldg(lse_h + q) * kLog2e : -INFINITY;
+      }
     }
-  };
+    __device__ void store(int j, int ln) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) nl2[(j & 1) * kRows + ln + 32 * i] = v[i];
+    }
+  } prep{lse_h, nl2, k0, L, {0.f, 0.f, 0.f, 0.f}};
   float acc = 0.f;
   auto epi = [&](int j, uint32_t taddr) {
     const float *nl = nl2 + (j & 1) * kRows + c_off;
@@ -218,10 +261,10 @@ __global__ void __launch_bounds__(kThreads, 2)
       for (int i = 0; i < 64; ++i) acc += ex2(fmaf(__uint_as_float(r[i]), qscale, nl[i]));
     }
   };
-  const bool ok = tile_pipeline<D>(smem, st, &tmK, &tmQ, k0, k0, nq, h, prep, epi);
+  const bool ok = tile_pipeline<D, true>(smem, st, &tmK, &tmQ, k0, k0, nq, h, prep, epi);
   // the two column halves of each key row: the second half hands its sum over
   float *half = nl2;  // free after the pipeline
-  if (ok && warp >= 4) half[row] = acc;
+  if (ok && warp >= 4 && warp < kEpiWarps) half[row] = acc;
   __syncthreads();
   if (ok) {
     if (warp < 4 && k0 + row < L) colsum[(size_t)h * L + k0 + row] = acc + half[row];
@@ -249,7 +292,10 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int row = (warp & 3) * 32 + lane;  // query within the tile (TMEM lane)
   const int c_off = (warp >> 2) * 64;      // this warp's key columns
   float m = -INFINITY, l = 0.f;  // base-2 running max and sum over this thread's columns
-  auto prep = [](int) {};
+  struct NoPrep {
+    __device__ void load(int, int) {}
+    __device__ void store(int, int) {}
+  } prep;
   auto epi = [&](int j, uint32_t taddr) {
     const bool diag = (j == nk - 1);
     uint32_t r[64];
@@ -270,8 +316,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     l = l * ex2(m - mn) + sum;
     m = mn;
   };
-  const bool ok = tile_pipeline<D>(smem, st, &tmQ, &tmK, q0, 0, nk, h, prep, epi);
-  if (ok && warp >= 4) {
+  const bool ok = tile_pipeline<D, false>(smem, st, &tmQ, &tmK, q0, 0, nk, h, prep, epi);
+  if (ok && warp >= 4 && warp < kEpiWarps) {
     xch[row] = m;
     xch[kRows + row] = l;
   }

@@ -239,7 +239,10 @@ def run_ours(args, w, rank, world, local_rank):
     value = tokens / (ms_per_step / 1e3)
 
     dec_ms = phases["decode"][0] / K
-    dec_launch_ms = phases["decode"][0] / max(1, phases["decode"][1])
+    dec_launch_ms = dec_ms / w.T  # per decode step (a multi-step form runs many steps per launch)
+    form = caches[-1].decode_form_used()
+    dec_kernel = {"cluster": "decode_cluster_kernel", "cooperative": "decode_kernel",
+                  "per_step": "decode_kernel"}.get(form, "decode_kernel")
     kv_gbs = kv_read_bytes(w) / (dec_launch_ms / 1e3) / 1e9
     dec_alg_gbs = decode_alg_bytes(w) / (dec_launch_ms / 1e3) / 1e9
     cs_ms = phases["prefill_colsum"][0] / K
@@ -251,17 +254,18 @@ def run_ours(args, w, rank, world, local_rank):
     shares = {"decode": dec_ms, "prefill_colsum": cs_ms, "prefill_attn": at_ms, "prefill_select": sel_ms}
     top = max(shares, key=shares.get)
     if top == "decode":
-        roof = {"kernel": "decode_step_kernel", "bound": "hbm", "achieved": dec_alg_gbs, "peak": pk["hbm_gbs"],
-                "unit": "GB/s", "traffic": traffic_for("decode_step_kernel", w),
+        roof = {"kernel": dec_kernel, "decode_form": form, "bound": "hbm", "achieved": dec_alg_gbs,
+                "peak": pk["hbm_gbs"], "unit": "GB/s", "traffic": traffic_for(dec_kernel, w),
+                "per": "decode step (algorithmic bytes and DRAM traffic per step)",
                 "algorithmic_bytes_per_launch": decode_alg_bytes(w), "avg_launch_ms": dec_launch_ms}
     elif top == "prefill_colsum":
         roof = {"kernel": "prefill_colsum", "bound": "tensor", "achieved": cs_tf, "peak": pk["bf16_tflops"],
                 "unit": "TFLOP/s", "traffic": traffic_for("prefill_colsum", w),
-                "algorithmic_flops_per_launch": score_pass_flops(w), "avg_launch_ms": cs_ms}
+                "per": "launch", "algorithmic_flops_per_launch": score_pass_flops(w), "avg_launch_ms": cs_ms}
     else:
         roof = {"kernel": top, "bound": "tensor", "achieved": at_tf if top == "prefill_attn" else None,
                 "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "traffic": traffic_for(top, w),
-                "algorithmic_flops_per_launch": attn_pass_flops(w), "avg_launch_ms": shares[top]}
+                "per": "launch", "algorithmic_flops_per_launch": attn_pass_flops(w), "avg_launch_ms": shares[top]}
     roof["frac"] = (roof["achieved"] / roof["peak"]) if roof.get("achieved") else None
     roof["peak_source"] = pk_src
     roof["share_of_step"] = shares[top] / ms_per_step
@@ -272,7 +276,7 @@ def run_ours(args, w, rank, world, local_rank):
         "vs_baseline": None, "dtype": w.dtype, "impl": "ours",
         "data": "synthetic: seeded per-head generator (Pareto-shifted keys along a hidden direction)",
         "config": workload_config(w, {"decode_form": args.decode_form}),
-        "decode": {"tokens_per_s": w.B * world / (dec_launch_ms / 1e3), "us_per_step": dec_launch_ms * 1e3,
+        "decode": {"form": form, "tokens_per_s": w.B * world / (dec_launch_ms / 1e3), "us_per_step": dec_launch_ms * 1e3,
                    "kv_read_gbs": kv_gbs, "alg_gbs": dec_alg_gbs,
                    "kv_read_frac_measured_hbm": kv_gbs / pk["hbm_gbs"],
                    "kv_read_frac_nominal_8tbs": kv_gbs / NOMINAL_HBM_GBS,

@@ -70,6 +70,7 @@ def lib():
         L.h2o_get_error.argtypes = [vp]
         L.h2o_profile_enable.argtypes = [vp, i32]
         L.h2o_set_decode_form.argtypes = [vp, i32]
+        L.h2o_decode_form_used.argtypes = [vp, C.POINTER(i32)]
         L.h2o_profile_read.argtypes = [vp, C.POINTER(C.c_double), C.POINTER(i64)]
         L.h2o_status_str.argtypes = [i32]
         L.h2o_status_str.restype = C.c_char_p
@@ -77,7 +78,7 @@ def lib():
         L.h2o_build_arch.restype = i32
         for f in ("h2o_cache_create", "h2o_cache_destroy", "h2o_set_stream", "h2o_prefill", "h2o_decode_step",
                   "h2o_decode_steps", "h2o_cache_export", "h2o_cache_import", "h2o_cache_info",
-                  "h2o_get_error", "h2o_profile_enable", "h2o_profile_read", "h2o_set_decode_form"):
+                  "h2o_get_error", "h2o_profile_enable", "h2o_profile_read", "h2o_set_decode_form", "h2o_decode_form_used"):
             getattr(L, f).restype = i32
         _lib = L
     return _lib
@@ -234,6 +235,12 @@ class H2OCache:
         "cluster" (see h2o_set_decode_form)."""
         f = self.DECODE_FORMS[form] if isinstance(form, str) else int(form)
         _check(lib().h2o_set_decode_form(self._h, f), "h2o_set_decode_form")
+
+    def decode_form_used(self) -> str:
+        """Form of the last decode call: "per_step", "cooperative", "cluster" or "" (none yet)."""
+        f = C.c_int32()
+        _check(lib().h2o_decode_form_used(self._h, C.byref(f)), "h2o_decode_form_used")
+        return {0: "", 1: "per_step", 2: "cooperative", 3: "cluster"}[f.value]
 
     def profile(self, on: bool = True):
         """Bracket each phase with CUDA events on the cache's stream."""

@@ -38,6 +38,7 @@ struct h2o_cache {
   int device;
   CacheView view;
   int decode_form = 0;  // h2o_set_decode_form
+  int form_used = 0;    // form of the last decode call
   // phase timing (h2o_profile_enable / h2o_profile_read)
   bool profiling = false;
   struct Mark {
@@ -248,7 +249,7 @@ h2o_status h2o_prefill(h2o_cache_t c, const void *Q, const void *K, const void *
   cudaError_t e;
   const bool tc = prefill_tc_supported(v, L);
   {
-    PhaseTimer pt(c, 0, 1);
+    PhaseTimer pt(c, 0, (tc && O) ? 2 : 1);  // tensor-core pass 1 = LSE kernel + output kernel
     e = tc ? launch_prefill_attn_tc(v, Q, K, V, O, lse, L, c->stream)
            : launch_prefill_attn_simt(v, Q, K, V, O, lse, L, c->stream);
     if (e != cudaSuccess) return cuda_fail(e);
@@ -306,7 +307,8 @@ h2o_status h2o_decode_steps(h2o_cache_t c, int n, const void *q, const void *k, 
       use_cluster = cluster_ok;
   }
   if (n >= 2 && ((form == 3 && !use_cluster) || (form == 2 && !use_coop))) return H2O_EUNSUPPORTED;
-  PhaseTimer pt(c, 3, n);
+  PhaseTimer pt(c, 3, use_cluster ? 1 : use_coop ? (n + 16383) / 16384 : n);
+  c->form_used = use_cluster ? 3 : use_coop ? 2 : 1;
   if (use_cluster) {
     DecodeStep s;
     s.q = q;
@@ -369,6 +371,12 @@ h2o_status h2o_decode_step(h2o_cache_t c, const void *q, const void *k, const vo
 h2o_status h2o_set_decode_form(h2o_cache_t c, int form) {
   if (!c || form < 0 || form > 3) return H2O_EINVAL;
   c->decode_form = form;
+  return H2O_OK;
+}
+
+h2o_status h2o_decode_form_used(h2o_cache_t c, int *form) {
+  if (!c || !form) return H2O_EINVAL;
+  *form = c->form_used;
   return H2O_OK;
 }
 

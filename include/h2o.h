@@ -120,6 +120,10 @@ h2o_status h2o_decode_steps(h2o_cache_t cache, int n, const void *q, const void 
  * H2O_EUNSUPPORTED (nothing launched). */
 h2o_status h2o_set_decode_form(h2o_cache_t cache, int form);
 
+/* The form (1, 2 or 3 as above) the last decode call of this cache ran with;
+ * 0 before any decode call. */
+h2o_status h2o_decode_form_used(h2o_cache_t cache, int *form);
+
 /* Copy the cache state out to device buffers: pos [B][H][k] int32,
  * score [B][H][k] fp32, K, V [B][H][k][d] (any may be NULL); next_pos and
  * n_valid (host, may be NULL) receive the position the next decode token
@@ -144,7 +148,8 @@ h2o_status h2o_cache_info(h2o_cache_t cache, int *B, int *H, int *d, int *k_heav
  * 2 = prefill select + gather, 3 = decode steps.  h2o_profile_read
  * synchronises on the recorded events and returns, per phase, the summed
  * elapsed milliseconds (ms[4]) and the number of kernel launches covered
- * (launches[4]); it then clears the record.  Either output may be NULL. */
+ * (launches[4]: a multi-step decode form counts one launch per grid, not one
+ * per step); it then clears the record.  Either output may be NULL. */
 h2o_status h2o_profile_enable(h2o_cache_t cache, int on);
 h2o_status h2o_profile_read(h2o_cache_t cache, double *ms, int64_t *launches);
 

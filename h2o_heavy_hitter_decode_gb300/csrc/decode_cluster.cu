@@ -82,11 +82,12 @@ __global__ void __launch_bounds__(kThreads, 7) decode_cluster_kernel(const CArgs
   __shared__ float s_wacc[kConsumers][D];
   // Exchange buffers, filled by the peers' DSMEM stores (pushes) before a
   // cluster barrier and read locally after it.
-  __shared__ float s_mlx[kMaxCluster][2];                  // every rank's (m, l), in every CTA
-  __shared__ __align__(16) float s_accx[kMaxCluster][D];   // every rank's acc row (used on rank 0)
-  __shared__ ArgMin s_candx[kMaxCluster];                  // every rank's candidate (used on rank 0)
-  __shared__ int s_dec_e;                                  // rank 0's decision, in every CTA
-  __shared__ float s_dec_w;
+  // Each completes one phase per step when its bytes have arrived.
+  __shared__ __align__(8) uint64_t s_bml, s_bacc, s_bcand, s_bdec;
+  __shared__ __align__(16) uint64_t s_mlx[kMaxCluster];    // every rank's (m, l), in every CTA
+  __shared__ __align__(16) float s_accx[kMaxCluster][D];   // every rank's acc row (rank 0)
+  __shared__ __align__(16) uint4 s_candx[kMaxCluster];     // every rank's candidate (rank 0)
+  __shared__ __align__(16) uint64_t s_dec;                 // rank 0's decision (slot, weight), in every CTA
   __shared__ float s_ML[2], s_lgnew, s_f[kMaxCluster];
   __shared__ ArgMin s_am[kConsumers];
   __shared__ int s_abort;
@@ -117,6 +118,10 @@ __global__ void __launch_bounds__(kThreads, 7) decode_cluster_kernel(const CArgs
     }
     mbar_init(&s_inbar[0], 1);
     mbar_init(&s_inbar[1], 1);
+    mbar_init(&s_bml, 1);
+    mbar_init(&s_bacc, 1);
+    mbar_init(&s_bcand, 1);
+    mbar_init(&s_bdec, 1);
     s_abort = 0;
     fence_mbar_init();
   }
@@ -147,8 +152,21 @@ __global__ void __launch_bounds__(kThreads, 7) decode_cluster_kernel(const CArgs
   };
   if (tid == kConsumerThreads) fetch_inputs(0);
 
+  // The exchange barriers must be initialised in every CTA before any peer
+  // pushes into them.
+  cluster.sync();
+
   int g = 0;  // slabs streamed (ring position)
   for (int step = 0; step < a.nsteps; ++step) {
+    if (*(volatile int *)&s_abort) break;  // uniform: read after the previous step's CTA barrier
+    if (tid == 0) {  // bytes this CTA receives during the step
+      mbar_expect_tx(&s_bml, P * 8);
+      mbar_expect_tx(&s_bdec, 8);
+      if (rank == 0) {
+        mbar_expect_tx(&s_bacc, P * D * 4);
+        mbar_expect_tx(&s_bcand, P * 16);
+      }
+    }
     // inputs of this step (buffer step&1) and, ahead, of the next one
     if (tid == kConsumerThreads && step + 1 < a.nsteps) fetch_inputs(step + 1);
     if (!__all_sync(0xffffffffu, mbar_wait(&s_inbar[step & 1], (step >> 1) & 1)) && lane == 0) s_abort = 1;
@@ -302,25 +320,27 @@ __global__ void __launch_bounds__(kThreads, 7) decode_cluster_kernel(const CArgs
         float t = 0.f;
 #pragma unroll
         for (int w = 0; w < kConsumers; ++w) t = fmaf(f[w], s_wacc[w][col], t);
-        *cluster.map_shared_rank(&s_accx[rank][col], 0) = t;  // to rank 0
+        st_async_b32(mapa(&s_accx[rank][col], 0), __float_as_uint(t), mapa(&s_bacc, 0));  // to rank 0
       }
       if (tid < P) {  // (m, l) to every rank
         float ls = 0.f;
 #pragma unroll
         for (int w = 0; w < kConsumers; ++w) ls = fmaf(f[w], s_wl[w], ls);
-        float *dst = cluster.map_shared_rank(&s_mlx[rank][0], tid);
-        dst[0] = M;
-        dst[1] = ls;
+        const uint64_t v = (uint64_t)__float_as_uint(M) | ((uint64_t)__float_as_uint(ls) << 32);
+        st_async_b64(mapa(&s_mlx[rank], tid), v, mapa(&s_bml, tid));
       }
     }
-    cluster.sync();  // #1: every CTA's (m, l, acc) published
 
-    // ---- global softmax statistics (identical in every CTA), from local copies
+    // ---- global softmax statistics (identical in every CTA), once every
+    // rank's (m, l) has landed here (and, on rank 0, every acc row)
     if (warp == 0) {
+      bool got = mbar_wait(&s_bml, step & 1);
+      if (rank == 0) got = got && mbar_wait(&s_bacc, step & 1);
+      if (!__all_sync(0xffffffffu, got) && lane == 0) s_abort = 1;
       float mr = -INFINITY, lr = 0.f;
       if (lane < P) {
-        mr = s_mlx[lane][0];
-        lr = s_mlx[lane][1];
+        mr = __uint_as_float((uint32_t)s_mlx[lane]);
+        lr = __uint_as_float((uint32_t)(s_mlx[lane] >> 32));
       }
       const float Mg = warp_max(mr);
       const float fr = (mr == -INFINITY) ? 0.f : exp2f(mr - Mg);
@@ -371,13 +391,17 @@ __global__ void __launch_bounds__(kThreads, 7) decode_cluster_kernel(const CArgs
       ArgMin b = s_am[0];
       for (int w = 1; w < kConsumers; ++w)
         if (am_less(s_am[w], b)) b = s_am[w];
-      *cluster.map_shared_rank(&s_candx[rank], 0) = b;  // to rank 0
+      st_async_v4(mapa(&s_candx[rank], 0), make_uint4(__float_as_uint(b.s), (uint32_t)b.p, (uint32_t)b.slot, 0u),
+                  mapa(&s_bcand, 0));  // to rank 0
     }
-    cluster.sync();  // #2: candidates published
 
     if (rank == 0 && warp == 0) {  // lane r holds rank r's candidate
+      if (!__all_sync(0xffffffffu, mbar_wait(&s_bcand, step & 1)) && lane == 0) s_abort = 1;
       ArgMin b{INFINITY, INT_MAX, -2};
-      if (lane < P) b = s_candx[lane];
+      if (lane < P) {
+        const uint4 cv = s_candx[lane];
+        b = ArgMin{__uint_as_float(cv.x), (int)cv.y, (int)cv.z};
+      }
       b = warp_argmin(b);
       int e = -1, ev = -1;
       if (n < c.k) {
@@ -392,19 +416,20 @@ __global__ void __launch_bounds__(kThreads, 7) decode_cluster_kernel(const CArgs
       }
       if (lane == 0 && a.s.evicted) a.s.evicted[(size_t)step * c.nh + h] = ev;
       if (lane < P) {  // decision to every rank
-        *cluster.map_shared_rank(&s_dec_e, lane) = e;
-        *cluster.map_shared_rank(&s_dec_w, lane) = w_new;
+        const uint64_t v = (uint64_t)(uint32_t)e | ((uint64_t)__float_as_uint(w_new) << 32);
+        st_async_b64(mapa(&s_dec, lane), v, mapa(&s_bdec, lane));
       }
     }
-    cluster.sync();  // #3: decision published
 
-    {
-      const int e = s_dec_e;
+    if (warp == 0) {  // the owner's update: warp 0 only
+      if (!__all_sync(0xffffffffu, mbar_wait(&s_bdec, step & 1)) && lane == 0) s_abort = 1;
+      const int e = (int)(uint32_t)s_dec;
+      const float dec_w = __uint_as_float((uint32_t)(s_dec >> 32));
       if (e >= s0 && e < s0 + own) {  // this CTA owns the slot that takes the new token
         const int j = e - s0;
         if (tid == 0) {
           ps[j] = p;
-          sc[j] = s_dec_w;
+          sc[j] = dec_w;
         }
         if (warp == 0 && grp == 0) {  // lanes 0..LPR-1 copy the k_t / v_t row
           const int i = sub;
@@ -422,8 +447,9 @@ __global__ void __launch_bounds__(kThreads, 7) decode_cluster_kernel(const CArgs
     }
     __syncthreads();
   }
+  if (*(volatile int *)&s_abort && tid == 0) atomicOr(c.err, 1);
   // write back the owned scores and tags; no CTA leaves while a peer could
-  // still store into its shared memory
+  // still push into its shared memory
   for (int j = tid; j < own; j += kThreads) {
     c.score[hk + s0 + j] = sc[j];
     c.pos[hk + s0 + j] = ps[j];

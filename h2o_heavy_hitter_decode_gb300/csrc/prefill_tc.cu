@@ -44,7 +44,7 @@ template <int D> struct TileGeo {
   static constexpr int kTileBytes = kBox * kBoxes;
   static constexpr int kKSteps = D / 16;  // UMMA K = 16 for bf16
   // resident tile + ring, each 1024-aligned, then the small state
-  static constexpr int kSmem = kTileBytes * (1 + kStages) + 2 * kRows * 4 + 256 + 1024;
+  static constexpr int kSmem = kTileBytes * (1 + kStages) + 2 * kRows * 4 + 3 * kRows * 4 + 256 + 1024;
 };
 
 struct __align__(8) SmallState {
@@ -215,7 +215,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   uint8_t *smem = align1024(smem_raw);
   using G = TileGeo<D>;
   float *nl2 = (float *)(smem + G::kTileBytes * (1 + kStages));  // [2][128]: -LSE*log2(e) per query
-  SmallState &st = *(SmallState *)(nl2 + 2 * kRows);
+  float *raw = nl2 + 2 * kRows;                                   // [3][128]: LSE slices in flight
+  SmallState &st = *(SmallState *)(raw + 3 * kRows);
   if (*(volatile int *)err) return;
   // Head-major (a head's CTAs share its Q tiles in L2), heaviest key tile first.
   const int h = blockIdx.x / nkt, kt = blockIdx.x % nkt;
@@ -226,25 +227,45 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int c_off = (warp >> 2) * 64;      // this warp's query columns
   const float *lse_h = lse + (size_t)h * L;
   // Column vector of query tile j: -LSE * log2(e) (-inf past L, so those
-  // zero-filled query rows add nothing), four queries per producer lane,
-  // loaded one tile ahead.
+  // zero-filled query rows add nothing).  The producer lanes fetch each
+  // tile's LSE slice with asynchronous 4-byte copies two tiles ahead (a
+  // three-slot staging ring), so no global load latency sits on the path
+  // that issues the MMAs.
   struct Prep {
     const float *lse_h;
-    float *nl2;
-    int k0, L;
-    float v[4];
+    float *nl2, *raw;
+    int k0, L, n;
+    __device__ void fetch(int j, int ln) {  // copies of tile j, one commit group
+      if (j < n) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int q = k0 + kRows * j + ln + 32 * i;
+          if (q < L) {
+            asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(
+                             sm100::smem_u32(raw + (j % 3) * kRows + ln + 32 * i)),
+                         "l"(lse_h + q)
+                         : "memory");
+          }
+        }
+      }
+      asm volatile("cp.async.commit_group;" ::: "memory");
+    }
     __device__ void load(int j, int ln) {
+      if (j == 0) {
+        fetch(0, ln);
+        fetch(1, ln);
+      }
+    }
+    __device__ void store(int j, int ln) {  // tile j landed (at most one newer group pending)
+      asm volatile("cp.async.wait_group 1;" ::: "memory");
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int q = k0 + kRows * j + ln + 32 * i;
-        v[i] = q < L ? -__ldg(lse_h + q) * kLog2e : -INFINITY;
+        nl2[(j & 1) * kRows + ln + 32 * i] = q < L ? -raw[(j % 3) * kRows + ln + 32 * i] * kLog2e : -INFINITY;
       }
+      fetch(j + 2, ln);
     }
-    __device__ void store(int j, int ln) {
-#pragma unroll
-      for (int i = 0; i < 4; ++i) nl2[(j & 1) * kRows + ln + 32 * i] = v[i];
-    }
-  } prep{lse_h, nl2, k0, L, {0.f, 0.f, 0.f, 0.f}};
+  } prep{lse_h, nl2, raw, k0, L, nq};
   float acc = 0.f;
   auto epi = [&](int j, uint32_t taddr) {
     const float *nl = nl2 + (j & 1) * kRows + c_off;
@@ -565,12 +586,18 @@ bool make_map(CUtensorMap *m, const void *base, int d, int L, int nh) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Each CTA of the LSE and column-sum passes holds 256 TMEM columns, so at most
+// two may share an SM's 512: the d = 64 kernels request the d = 128 shared
+// memory footprint to keep a third CTA off the SM instead of blocking in
+// tcgen05.alloc.
+constexpr int kTwoPerSmSmem = TileGeo<128>::kSmem;
+
 template <int D>
 cudaError_t colsum_t(const CacheView &c, const void *Q, const void *K, const float *lse, float *colsum, int L,
                      cudaStream_t st) {
   CUtensorMap mq, mk;
   if (!make_map(&mq, Q, D, L, c.nh) || !make_map(&mk, K, D, L, c.nh)) return cudaErrorInvalidValue;
-  const int smem = TileGeo<D>::kSmem;
+  const int smem = kTwoPerSmSmem;
   cudaError_t e = cudaFuncSetAttribute(colsum_tc<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int nkt = (L + kRows - 1) / kRows;
@@ -600,7 +627,7 @@ template <int D>
 cudaError_t lse_t(const CacheView &c, const void *Q, const void *K, float *lse, int L, cudaStream_t st) {
   CUtensorMap mq, mk;
   if (!make_map(&mq, Q, D, L, c.nh) || !make_map(&mk, K, D, L, c.nh)) return cudaErrorInvalidValue;
-  const int smem = TileGeo<D>::kSmem;
+  const int smem = kTwoPerSmSmem;
   cudaError_t e = cudaFuncSetAttribute(lse_tc<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int nqt = (L + kRows - 1) / kRows;

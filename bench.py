@@ -154,6 +154,21 @@ class Clocks:
                 "samples": len(rows), "power_w_max": float(max(r[2] for r in rows))}
 
 
+# ------------------------------------------------------------ multi-rank
+
+def aggregate_over_ranks(total_ms, steps, tokens_per_job, world, dist=None, device="cpu"):
+    """Whole-job figures of a weak-scaling run: every rank times its own job;
+    the slowest rank's total time counts, and the value is the tokens of all
+    ranks' jobs over that time.  Returns (ms_per_step, tokens_per_s)."""
+    if dist is not None and world > 1:
+        import torch
+        t = torch.tensor([float(total_ms)], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / steps
+    return ms_per_step, tokens_per_job * world / (ms_per_step / 1e3)
+
+
 # --------------------------------------------------------------- our arm
 
 def run_ours(args, w, rank, world, local_rank):
@@ -228,15 +243,8 @@ def run_ours(args, w, rank, world, local_rank):
             phases[p][0] += ms
             phases[p][1] += n
     caches[-1].check_device_error()
-    tot_ms = float(np.sum(step_ms))
-    if dist:
-        t = torch.tensor([tot_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        tot_ms = float(t.item())
-    ms_per_step = tot_ms / args.steps
     K = args.steps
-    tokens = w.B * w.T * world
-    value = tokens / (ms_per_step / 1e3)
+    ms_per_step, value = aggregate_over_ranks(float(np.sum(step_ms)), K, w.B * w.T, world, dist, dev)
 
     dec_ms = phases["decode"][0] / K
     dec_launch_ms = dec_ms / w.T  # per decode step (a multi-step form runs many steps per launch)
@@ -339,15 +347,12 @@ def e2e(args, w, dev, hQ, hK, hV, hq, hk, hv, tdt, stream, world, dist):
         job()
         ev[i][1].record(stream)
     torch.cuda.synchronize()
-    ms = float(np.sum([a.elapsed_time(b) for a, b in ev]))
-    if dist:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms_step, value = aggregate_over_ranks(float(np.sum([a.elapsed_time(b) for a, b in ev])), n, w.B * w.T,
+                                          world, dist, dev)
     h2d = sum(x.numel() * x.element_size() for x in pin)
     d2h = hout.numel() * hout.element_size()
-    return {"value": w.B * w.T * world / (ms / n / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": ms / n}
+    return {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": ms_step}
 
 
 # ------------------------------------------------------------ oracle timing

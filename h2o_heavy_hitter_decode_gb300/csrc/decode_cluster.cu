@@ -91,6 +91,7 @@ __global__ void __launch_bounds__(kThreads, 7) decode_cluster_kernel(const CArgs
   __shared__ float s_ML[2], s_lgnew, s_f[kMaxCluster];
   __shared__ ArgMin s_am[kConsumers];
   __shared__ int s_abort;
+  __shared__ int s_spec;  // slabs of the next step the producer issued ahead
 
   const CacheView &c = a.c;
   const int P = (int)cluster.num_blocks();
@@ -123,6 +124,7 @@ __global__ void __launch_bounds__(kThreads, 7) decode_cluster_kernel(const CArgs
     mbar_init(&s_bcand, 1);
     mbar_init(&s_bdec, 1);
     s_abort = 0;
+    s_spec = 0;
     fence_mbar_init();
   }
   for (int j = tid; j < own; j += kThreads) {
@@ -156,7 +158,8 @@ __global__ void __launch_bounds__(kThreads, 7) decode_cluster_kernel(const CArgs
   // pushes into them.
   cluster.sync();
 
-  int g = 0;  // slabs streamed (ring position)
+  int g = 0;   // slabs consumed (ring position), consumers
+  int gp = 0;  // slabs issued (ring position), producer lane
   for (int step = 0; step < a.nsteps; ++step) {
     if (*(volatile int *)&s_abort) break;  // uniform: read after the previous step's CTA barrier
     if (tid == 0) {  // bytes this CTA receives during the step
@@ -177,24 +180,37 @@ __global__ void __launch_bounds__(kThreads, 7) decode_cluster_kernel(const CArgs
     const int nst = kResident ? 0 : (nrows + TR - 1) / TR;
     const bool aborted = *(volatile int *)&s_abort;
     if (warp == kConsumers) {
-      // ---- producer (streaming form only)
+      // ---- producer (streaming form only).  Slabs [spec, nst) of this step,
+      // then the first slabs of the next step ahead of its decision: they land
+      // while the cluster exchanges partials; the owner of the slot that
+      // changes patches that row in the landed slab (below).
       if (!kResident && lane == 0 && !aborted) {
-        int issued = 0;
         bool ok = true;
-        for (; issued < nst; ++issued) {
-          const int gi = g + issued, st = gi % kStages;
-          if (gi >= kStages && !(ok = mbar_wait(&s_empty[st], ((gi / kStages) - 1) & 1))) break;
-          const uint32_t bytes = (uint32_t)(min(TR, nrows - issued * TR) * ROWB);
-          const size_t off = (hk + s0 + (size_t)issued * TR) * ROWB;
+        auto issue = [&](int i, int step_rows) -> bool {  // slab i of a step with `step_rows` owned rows
+          const int st = gp % kStages;
+          if (gp >= kStages && !mbar_wait(&s_empty[st], ((gp / kStages) - 1) & 1)) return false;
+          const uint32_t bytes = (uint32_t)(min(TR, step_rows - i * TR) * ROWB);
+          const size_t off = (hk + s0 + (size_t)i * TR) * ROWB;
           mbar_expect_tx(&s_full[st], 2 * bytes);
           bulk_load(kv + st * 2 * kStageBytes, (const uint8_t *)c.K + off, bytes, &s_full[st]);
           bulk_load(kv + st * 2 * kStageBytes + kStageBytes, (const uint8_t *)c.V + off, bytes, &s_full[st]);
+          ++gp;
+          return true;
+        };
+        for (int i = s_spec; ok && i < nst; ++i) ok = issue(i, nrows);
+        int spec = 0;
+        if (ok && step + 1 < a.nsteps) {
+          const int n1 = min(a.s.n_valid + step + 1, c.k);
+          const int nrows1 = max(0, min(own, n1 - s0));
+          const int nst1 = (nrows1 + TR - 1) / TR;
+          for (; ok && spec < kStages && spec < nst1; ++spec) ok = issue(spec, nrows1);
+          if (!ok) --spec;
         }
+        s_spec = spec;
         if (!ok) {
           s_abort = 1;
           atomicOr(c.err, 1);
-          for (int j = max(0, issued - kStages); j < issued; ++j)
-            mbar_wait(&s_full[(g + j) % kStages], ((g + j) / kStages) & 1);
+          for (int j = max(0, gp - kStages); j < gp; ++j) mbar_wait(&s_full[j % kStages], (j / kStages) & 1);
         }
       }
       g += nst;
@@ -443,6 +459,18 @@ __global__ void __launch_bounds__(kThreads, 7) decode_cluster_kernel(const CArgs
         }
         fence_proxy_async_smem();
         asm volatile("fence.proxy.async.global;" ::: "memory");  // before our next bulk reads of row e
+        if (!kResident && step + 1 < a.nsteps && j / TR < s_spec) {
+          // The producer already loaded the slab holding row j for the next
+          // step: let that copy land, then overwrite the stale row in it.
+          const int gpos = g + j / TR;  // ring position of that slab (g = next step's first)
+          const int st = gpos % kStages;
+          if (!__all_sync(0xffffffffu, mbar_wait(&s_full[st], (gpos / kStages) & 1)) && lane == 0) s_abort = 1;
+          if (grp == 0) {
+            uint8_t *slab = kv + st * 2 * kStageBytes;
+            ((uint4 *)(slab + (j % TR) * ROWB))[sub] = *(const uint4 *)(in_k + sub * EPL);
+            ((uint4 *)(slab + kStageBytes + (j % TR) * ROWB))[sub] = *(const uint4 *)(in_v + sub * EPL);
+          }
+        }
       }
     }
     __syncthreads();

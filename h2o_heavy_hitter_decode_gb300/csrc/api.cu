@@ -249,7 +249,7 @@ h2o_status h2o_prefill(h2o_cache_t c, const void *Q, const void *K, const void *
   cudaError_t e;
   const bool tc = prefill_tc_supported(v, L);
   {
-    PhaseTimer pt(c, 0, (tc && O) ? 2 : 1);  // tensor-core pass 1 = LSE kernel + output kernel
+    PhaseTimer pt(c, 0, 1);
     e = tc ? launch_prefill_attn_tc(v, Q, K, V, O, lse, L, c->stream)
            : launch_prefill_attn_simt(v, Q, K, V, O, lse, L, c->stream);
     if (e != cudaSuccess) return cuda_fail(e);

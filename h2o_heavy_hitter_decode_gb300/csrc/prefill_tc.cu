@@ -355,17 +355,21 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
 }
 
-// ------------------------------------------------------- attention output
-// O_i = sum_j P_ij V_j with the exact probabilities P_ij = exp2(s_ij*c -
-// LSE_i*log2(e)) (LSE from the pass above), so no online rescaling is needed.
-// One CTA per 128 queries; warps 0-3 turn S = Q K^T (TMEM) into bf16 P in
-// shared memory (128-byte swizzled K-major layout, the A operand of the next
-// MMA); warp 4 is the producer: TMA for Q (resident) and the K and V rings,
-// the S MMAs and the O += P V MMAs (V is the MN-major B operand).  S is
-// double-buffered in TMEM, O accumulates in TMEM and is written out at the
+// ------------------------------------------------------- attention pass
+// Causal attention over the prompt in one pass: O and the row log-sum-exp.
+// One CTA per 128 queries.  Warp 8 is the producer: TMA for Q (resident) and
+// the K and V rings, the S = Q K^T MMAs into two TMEM buffers and the
+// O += P V MMAs (V is the MN-major B operand) into a TMEM accumulator.  Warps
+// 0-7 (two per TMEM lane quarter, 64 key columns each) turn S into bf16
+// P = exp2(s*c - m) in shared memory (128-byte swizzled K-major layout, the A
+// operand of the PV MMA) with an online row max m and an fp32 row sum l.  The
+// two warps of a row exchange their half-row maxima through each other's P
+// rows.  O is rescaled (tcgen05.ld/st) only when a row's max grows by more
+// than 2^8 over the max its P values were taken against, so P stays <= 256
+// and rescales are rare; O / l and LSE = (m + log2 l) ln 2 are written at the
 // end.  Barriers: kfull/vfull (TMA landed), sfull (S_j computed), sfree (S_j
 // read), pfull (P_j written), pvdone (O += P_j V_j done: P buffer and V stage
-// free).
+// free), pair (half-row exchange between the two warps of a row).
 template <int D> struct OutGeo {
   static constexpr int kTile = TileGeo<D>::kTileBytes;  // 128 rows x D bf16
   static constexpr int kP = 128 * 128 * 2;               // P tile: 128 queries x 128 keys
@@ -374,6 +378,8 @@ template <int D> struct OutGeo {
 
 struct __align__(8) OutState {
   uint64_t res, kfull[2], vfull[2], sfull[2], sfree[2], pfull[2], pvdone[2], drain;
+  uint64_t pair[2][4];  // [tile parity][lane quarter]: both warps of a row wrote their half-row max
+  uint64_t pair_l[4];   // [lane quarter]: both warps wrote their half-row sum
   uint32_t tmem_base;
   int abort;
 };
@@ -384,7 +390,7 @@ constexpr int kOutThreads = 32 * (kOutSoftmaxWarps + 1);
 template <int D>
 __global__ void __launch_bounds__(kOutThreads, 1)
     attn_out_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                const __grid_constant__ CUtensorMap tmV, const float *__restrict__ lse, __nv_bfloat16 *__restrict__ O,
+                const __grid_constant__ CUtensorMap tmV, float *__restrict__ lse, __nv_bfloat16 *__restrict__ O,
                 int L, int nh, int nqt, float qscale, int *err) {
   using G = OutGeo<D>;
   constexpr int kT = G::kTile;
@@ -413,6 +419,11 @@ __global__ void __launch_bounds__(kOutThreads, 1)
       mbar_init(&st.pvdone[b], 1);
     }
     mbar_init(&st.drain, 1);
+    for (int qq = 0; qq < 4; ++qq) {
+      mbar_init(&st.pair[0][qq], 64);
+      mbar_init(&st.pair[1][qq], 64);
+      mbar_init(&st.pair_l[qq], 64);
+    }
     st.abort = 0;
     fence_mbar_init();
   }
@@ -487,13 +498,15 @@ __global__ void __launch_bounds__(kOutThreads, 1)
   } else {
     // Softmax warps: query row `row` (TMEM lane), key columns c_off .. c_off+63.
     const int lane = tid & 31;
-    const int row = (warp & 3) * 32 + lane;
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
     const int half = warp >> 2;
     const int c_off = half * 64;
     const int q = q0 + row;
-    const float nl2 = q < L ? -__ldg(lse + (size_t)h * L + q) * kLog2e : 0.f;
-    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const int sw = row & 7;
+    constexpr int kHalfD = D / 2;  // output columns of this warp
+    float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
     for (int j = 0; j < n; ++j) {
       if (j >= 2 && !(ok = wait_warp(&st.pvdone[j & 1], ((j - 2) >> 1) & 1))) break;
@@ -502,42 +515,95 @@ __global__ void __launch_bounds__(kOutThreads, 1)
       const bool diag = (j == n - 1);
       uint32_t r[64];
       tmem_ld64(tbase + lane_off + (uint32_t)(j & 1) * 128 + (uint32_t)c_off, r);
+      float hm = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < 64; ++i) {
+        float x = __uint_as_float(r[i]) * qscale;
+        if (diag && c_off + i > row) x = -INFINITY;  // key after the query
+        r[i] = __float_as_uint(x);
+        hm = fmaxf(hm, x);
+      }
+      tc_fence_before();
+      mbar_arrive(&st.sfree[j & 1]);  // the logits are in registers: S buffer free
+      // Half-row maxima: each warp writes into the partner's rows of this P
+      // buffer (free: its last PV is done), which the partner reads before it
+      // overwrites them with its own P.
+      uint8_t *pbuf = sP + (j & 1) * G::kP;
+      *reinterpret_cast<float *>(pbuf + (1 - half) * kBox + row * 128) = hm;
+      mbar_arrive(&st.pair[j & 1][quarter]);
+      if (!(ok = wait_warp(&st.pair[j & 1][quarter], (j >> 1) & 1))) break;
+      const float m_tile = fmaxf(hm, *reinterpret_cast<const float *>(pbuf + half * kBox + row * 128));
+      float m_new = m_run;
+      bool resc = false;
+      if (m_run == -INFINITY) {
+        m_new = m_tile;  // the row's first logits: nothing accumulated yet
+      } else if (m_tile > m_run + 8.f) {
+        m_new = m_tile;
+        resc = true;
+      }
+      if (__any_sync(0xffffffffu, resc)) {
+        // O must hold every earlier P V before it is rescaled
+        if (!(ok = wait_warp(&st.pvdone[(j - 1) & 1], ((j - 1) >> 1) & 1))) break;
+        tc_fence_after();
+        const float f = resc ? ex2(m_run - m_new) : 1.f;
+#pragma unroll 1
+        for (int cc = 0; cc < kHalfD; cc += 32) {
+          uint32_t o[32];
+          const uint32_t ta = tO + lane_off + (uint32_t)(half * kHalfD + cc);
+          tmem_ld32(ta, o);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * f);
+          tmem_st32(ta, o);
+        }
+        tmem_st_wait();
+        l_run *= f;
+      }
+      m_run = m_new;
       uint32_t pk[32];
+      float ls = 0.f;
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
-        float a = ex2(fmaf(__uint_as_float(r[2 * i]), qscale, nl2));
-        float b = ex2(fmaf(__uint_as_float(r[2 * i + 1]), qscale, nl2));
-        if (diag && c_off + 2 * i > row) a = 0.f;
-        if (diag && c_off + 2 * i + 1 > row) b = 0.f;
+        const float a = ex2(__uint_as_float(r[2 * i]) - m_run);  // masked: exp2(-inf) = 0
+        const float b = ex2(__uint_as_float(r[2 * i + 1]) - m_run);
+        ls += a + b;
         __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
         pk[i] = *reinterpret_cast<uint32_t *>(&v);
       }
+      l_run += ls;
       // 64 keys = one 128-byte row of box `half`: eight 16-byte chunks, swizzled by row.
-      uint8_t *prow = sP + (j & 1) * G::kP + half * kBox + row * 128;
+      uint8_t *prow = pbuf + half * kBox + row * 128;
 #pragma unroll
       for (int cch = 0; cch < 8; ++cch)
         *reinterpret_cast<uint4 *>(prow + ((cch ^ sw) << 4)) =
             make_uint4(pk[4 * cch], pk[4 * cch + 1], pk[4 * cch + 2], pk[4 * cch + 3]);
-      tc_fence_before();
-      mbar_arrive(&st.sfree[j & 1]);
       fence_proxy_async_smem();
+      tc_fence_before();
       mbar_arrive(&st.pfull[j & 1]);
     }
     if (ok) ok = wait_warp(&st.pvdone[(n - 1) & 1], ((n - 1) >> 1) & 1);
     if (ok) {
       tc_fence_after();
-      constexpr int kCols = D / 2;  // output columns of this warp
-      __nv_bfloat16 *orow = O + ((size_t)h * L + (q < L ? q : 0)) * D + half * kCols;
+      // Row sum: the halves hand each other l through P buffer 0 (free now).
+      *reinterpret_cast<float *>(sP + (1 - half) * kBox + row * 128 + 4) = l_run;
+      mbar_arrive(&st.pair_l[quarter]);
+      ok = wait_warp(&st.pair_l[quarter], 0);
+    }
+    if (ok) {
+      const float l_row = l_run + *reinterpret_cast<const float *>(sP + half * kBox + row * 128 + 4);
+      const float inv = 1.f / l_row;
+      __nv_bfloat16 *orow = O + ((size_t)h * L + (q < L ? q : 0)) * D + half * kHalfD;
 #pragma unroll 1
-      for (int c0 = 0; c0 < kCols; c0 += 32) {  // collective loads: every lane, every chunk
-        uint32_t r[32];
-        tmem_ld32(tO + lane_off + (uint32_t)(half * kCols + c0), r);
+      for (int c0 = 0; c0 < kHalfD; c0 += 32) {  // collective loads: every lane, every chunk
+        uint32_t o[32];
+        tmem_ld32(tO + lane_off + (uint32_t)(half * kHalfD + c0), o);
         tmem_ld_wait();
         if (q < L) {
           uint32_t pk[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            __nv_bfloat162 v = __floats2bfloat162_rn(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+            __nv_bfloat162 v =
+                __floats2bfloat162_rn(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv);
             pk[i] = *reinterpret_cast<uint32_t *>(&v);
           }
           uint4 *dst = reinterpret_cast<uint4 *>(orow + c0);
@@ -545,6 +611,7 @@ __global__ void __launch_bounds__(kOutThreads, 1)
           for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
         }
       }
+      if (half == 0 && q < L) lse[(size_t)h * L + q] = (m_run + __log2f(l_row)) * kLn2;
     } else {
       st.abort = 1;
     }
@@ -608,7 +675,7 @@ cudaError_t colsum_t(const CacheView &c, const void *Q, const void *K, const flo
 }
 
 template <int D>
-cudaError_t attn_out_t(const CacheView &c, const void *Q, const void *K, const void *V, const float *lse, void *O,
+cudaError_t attn_out_t(const CacheView &c, const void *Q, const void *K, const void *V, float *lse, void *O,
                        int L, cudaStream_t st) {
   CUtensorMap mq, mk, mv;
   if (!make_map(&mq, Q, D, L, c.nh) || !make_map(&mk, K, D, L, c.nh) || !make_map(&mv, V, D, L, c.nh))
@@ -643,12 +710,11 @@ bool prefill_tc_supported(const CacheView &c, int L) {
          encode_fn() != nullptr;
 }
 
-// Pass 1: the row log-sum-exp, then (if O is wanted) the attention output
-// from the exact probabilities; both on the tensor cores.
+// Pass 1 on the tensor cores: with an O output, one attention pass writes O
+// and the row log-sum-exp; without it, the LSE-only pass (no PV work).
 cudaError_t launch_prefill_attn_tc(const CacheView &c, const void *Q, const void *K, const void *V, void *O,
                                    float *lse, int L, cudaStream_t st) {
-  cudaError_t e = c.d == 128 ? lse_t<128>(c, Q, K, lse, L, st) : lse_t<64>(c, Q, K, lse, L, st);
-  if (e != cudaSuccess || !O) return e;
+  if (!O) return c.d == 128 ? lse_t<128>(c, Q, K, lse, L, st) : lse_t<64>(c, Q, K, lse, L, st);
   return c.d == 128 ? attn_out_t<128>(c, Q, K, V, lse, O, L, st) : attn_out_t<64>(c, Q, K, V, lse, O, L, st);
 }
 

@@ -10,10 +10,11 @@
  * definition, in double precision, one query at a time.
  *
  * Parity pins (what ties this file to something other than itself) live in
- * tests/test_oracle_pins.py: closed-form harmonic scores for identical keys,
- * a library attention routine for the Full (k >= length) and Local
- * (k_heavy = 0) special cases, Definition 4.3's invariants, conservation of
- * score mass, and brute-force enumeration on tiny inputs.
+ * tests/test_oracle_pins.py: hand-derived rational worked examples (plain
+ * H2O, a pinned sink, the mean-weight ranking), a library attention routine
+ * for the Full (k >= length), Local (k_heavy = 0) and sinks-plus-window
+ * (n_sink = k_heavy) special cases, Definition 4.3's invariants, conservation
+ * of score mass, and brute-force enumeration on tiny inputs.
  */
 #include "h2o_oracle.h"
 
@@ -51,13 +52,26 @@ static int int_cmp(const void *pa, const void *pb) {
   return (a > b) - (a < b);
 }
 
-/* Step 1 of the walkthrough ("prefill the prompt ... begin scoring if the
- * prompt already exceeds k"), read as: every prompt query attends causally to
+/* Step 1 of the walkthrough (fill the cache from the prompt, scoring it at
+ * once when the prompt is longer than k), read as: every prompt query attends causally to
  * the prompt (no eviction inside the prompt), each key's F_score is the sum
  * of the softmax weights it received (its causal column sum), and if L > k the
  * cache keeps the k_local most recent positions (the protected local block)
- * plus the k_heavy largest F_scores among the older ones. */
-static void prefill_head(int d, int L, int kh, int kl, const double *Q, const double *K,
+ * plus the k_heavy largest F_scores among the older ones.
+ *
+ * Policy variants (the page's "Limitations" contrasts H2O with attention-sink
+ * streaming and notes the bias of the running sum towards old tokens):
+ *   - n_sink > 0 pins positions 0 .. n_sink-1 (they take n_sink of the
+ *     k_heavy slots; the other k_heavy - n_sink go to the largest keys among
+ *     positions n_sink .. L-k_local-1);
+ *   - score_mode 1 ranks by the mean weight instead of the sum: F_score
+ *     divided by the number of queries that attended to the position, which
+ *     for prompt position j is L - j. */
+static double rank_key(double F, int64_t attended, int score_mode) {
+  return score_mode ? F / (double)attended : F;
+}
+
+static void prefill_head(int d, int L, int kh, int kl, int ns, int mode, const double *Q, const double *K,
                          const double *V, double *O, double *lse, double *colsum,
                          int32_t *pos, double *score, double *Ks, double *Vs,
                          int32_t *n_valid, double *margin, double *dropped_mass) {
@@ -100,15 +114,19 @@ static void prefill_head(int d, int L, int kh, int kl, const double *Q, const do
     for (int j = 0; j < L; ++j) keep[n++] = j;
   } else {
     const int nc = L - kl; /* candidates for the heavy-hitter slots: 0 .. L-kl-1 */
+    const int nfree = kh - ns; /* heavy slots left after the pinned sinks */
     cand_t *c = (cand_t *)malloc(sizeof(cand_t) * (size_t)nc);
-    for (int j = 0; j < nc; ++j) {
-      c[j].colsum = F[j];
-      c[j].j = j;
+    for (int j = 0; j < ns; ++j) keep[n++] = j;
+    int m = 0;
+    for (int j = ns; j < nc; ++j) {
+      c[m].colsum = rank_key(F[j], L - j, mode);
+      c[m].j = j;
+      ++m;
     }
-    qsort(c, (size_t)nc, sizeof(cand_t), cand_cmp);
-    for (int r = 0; r < kh; ++r) keep[n++] = c[r].j;
-    for (int r = kh; r < nc; ++r) dropped += c[r].colsum;
-    if (kh > 0 && nc > kh) mg = c[kh - 1].colsum - c[kh].colsum;
+    qsort(c, (size_t)m, sizeof(cand_t), cand_cmp);
+    for (int r = 0; r < nfree; ++r) keep[n++] = c[r].j;
+    for (int r = nfree; r < m; ++r) dropped += F[c[r].j];
+    if (nfree > 0 && m > nfree) mg = c[nfree - 1].colsum - c[nfree].colsum;
     for (int j = L - kl; j < L; ++j) keep[n++] = j;
     free(c);
     qsort(keep, (size_t)n, sizeof(int), int_cmp);
@@ -136,19 +154,20 @@ static void prefill_head(int d, int L, int kh, int kl, const double *Q, const do
   free(F);
 }
 
-int h2o_oracle_prefill(int nh, int d, int L, int k_heavy, int k_local,
+int h2o_oracle_prefill(int nh, int d, int L, int k_heavy, int k_local, int n_sink, int score_mode,
                        const double *Q, const double *K, const double *V,
                        double *O, double *lse, double *colsum,
                        int32_t *pos, double *score, double *Ks, double *Vs,
                        int32_t *n_valid, double *margin, double *dropped_mass) {
   if (nh < 0 || d < 1 || L < 1 || k_heavy < 0 || k_local < 0 || k_heavy + k_local < 1)
     return -1;
+  if (n_sink < 0 || n_sink > k_heavy || (score_mode != 0 && score_mode != 1)) return -1;
   if (!Q || !K || !V || !pos || !score || !Ks || !Vs || !n_valid) return -1;
   const int k = k_heavy + k_local;
 #pragma omp parallel for schedule(dynamic, 1)
   for (int h = 0; h < nh; ++h) {
     const size_t hl = (size_t)h * L;
-    prefill_head(d, L, k_heavy, k_local, Q + hl * d, K + hl * d, V + hl * d,
+    prefill_head(d, L, k_heavy, k_local, n_sink, score_mode, Q + hl * d, K + hl * d, V + hl * d,
                  O ? O + hl * d : NULL, lse ? lse + hl : NULL, colsum ? colsum + hl : NULL,
                  pos + (size_t)h * k, score + (size_t)h * k, Ks + (size_t)h * k * d,
                  Vs + (size_t)h * k * d, n_valid + h, margin ? margin + h : NULL,
@@ -163,8 +182,11 @@ int h2o_oracle_prefill(int nh, int d, int L, int k_heavy, int k_local,
  * over C = S ∪ {p}; each member of C adds its softmax weight to its F_score
  * (the new entry starts at its own weight).  If |C| <= k the new entry is
  * admitted; otherwise the entry with the lowest (F_score, position) among
- * those not in the local block (positions <= p - k_local) leaves the cache. */
-static void decode_head(int d, int kh, int kl, int64_t p0, int T, int nh, int h,
+ * those not in the local block (positions <= p - k_local) leaves the cache.
+ * Variants: positions below n_sink are never candidates; score_mode 1 ranks
+ * by F_score over the number of queries that attended to the entry, which at
+ * step p is p - position + 1 (an entry, once cached, saw every later query). */
+static void decode_head(int d, int kh, int kl, int ns, int mode, int64_t p0, int T, int nh, int h,
                         int32_t *pos, double *score, double *Ks, double *Vs, int32_t *n_valid,
                         const double *q, const double *kn, const double *vn, double *out,
                         int32_t *evicted, double *margin, double *evicted_mass) {
@@ -223,7 +245,8 @@ static void decode_head(int d, int kh, int kl, int64_t p0, int T, int nh, int h,
       for (int j = -1; j < n; ++j) {
         const int64_t pj = (j < 0) ? p : (int64_t)pos[j];
         if (pj > p - kl) continue; /* protected: one of the k_local newest */
-        const double sj = (j < 0) ? w_new : score[j];
+        if (pj < ns) continue;     /* protected: an attention sink */
+        const double sj = rank_key((j < 0) ? w_new : score[j], p - pj + 1, mode);
         if (best == -2 || sj < best_s || (sj == best_s && pj < best_p)) {
           if (best != -2) second_s = best_s;
           best = j;
@@ -233,8 +256,9 @@ static void decode_head(int d, int kh, int kl, int64_t p0, int T, int nh, int h,
           second_s = sj;
         }
       }
-      /* best == -2 cannot happen: with k_heavy + k_local = k and k+1 entries,
-       * at least k_heavy + 1 >= 1 lie outside the local block. */
+      /* best == -2 cannot happen: of the k+1 entries, k_local are in the
+       * local block and at most n_sink <= k_heavy are sinks, so at least
+       * k_heavy + 1 - n_sink >= 1 are candidates. */
       if (best >= 0) {
         ev = pos[best];
         if (evicted_mass) *evicted_mass += score[best];
@@ -254,18 +278,20 @@ static void decode_head(int d, int kh, int kl, int64_t p0, int T, int nh, int h,
   free(w);
 }
 
-int h2o_oracle_decode(int nh, int d, int k_heavy, int k_local, int64_t p0, int T,
+int h2o_oracle_decode(int nh, int d, int k_heavy, int k_local, int n_sink, int score_mode,
+                      int64_t p0, int T,
                       int32_t *pos, double *score, double *Ks, double *Vs, int32_t *n_valid,
                       const double *q, const double *kn, const double *vn,
                       double *out, int32_t *evicted, double *margin, double *evicted_mass) {
   if (nh < 0 || d < 1 || T < 0 || k_heavy < 0 || k_local < 0 || k_heavy + k_local < 1 || p0 < 0)
     return -1;
+  if (n_sink < 0 || n_sink > k_heavy || (score_mode != 0 && score_mode != 1)) return -1;
   if (p0 + (int64_t)T > (int64_t)0x7fffffff) return -1;
   if (!pos || !score || !Ks || !Vs || !n_valid || (T > 0 && (!q || !kn || !vn))) return -1;
   const int k = k_heavy + k_local;
 #pragma omp parallel for schedule(dynamic, 1)
   for (int h = 0; h < nh; ++h) {
-    decode_head(d, k_heavy, k_local, p0, T, nh, h, pos + (size_t)h * k, score + (size_t)h * k,
+    decode_head(d, k_heavy, k_local, n_sink, score_mode, p0, T, nh, h, pos + (size_t)h * k, score + (size_t)h * k,
                 Ks + (size_t)h * k * d, Vs + (size_t)h * k * d, n_valid + h, q, kn, vn, out,
                 evicted, margin, evicted_mass ? evicted_mass + h : NULL);
   }

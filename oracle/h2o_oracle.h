@@ -22,6 +22,14 @@
  *     k_heavy largest column sums of the rest;
  *   - ties: eviction takes the lowest (score, position) pair; prefill keeps the
  *     largest (colsum, position) pairs, i.e. the higher position survives.
+ * Policy variants (both parameters 0 give plain H2O):
+ *   - n_sink (0 <= n_sink <= k_heavy): positions 0 .. n_sink-1 are pinned
+ *     attention sinks, never evicted, taking n_sink of the heavy slots; with
+ *     n_sink = k_heavy the cache is exactly sinks + a recent window;
+ *   - score_mode 1: eviction and selection rank entries by their mean weight,
+ *     F_score / (number of queries that attended to the entry) — L - j for
+ *     prompt position j after the prefill, p - j + 1 after the step at p.
+ *     The stored F_score stays the plain sum.
  *
  * All arrays are row-major doubles (int32 for positions).  A "head" is one
  * (batch, head) pair; heads are independent.
@@ -41,10 +49,11 @@ extern "C" {
  *   softmax, and the initial cache of each head in k slots:
  *   pos [nh][k] (ascending positions, -1 past n_valid), score [nh][k],
  *   Ks, Vs [nh][k][d]; n_valid [nh]; margin [nh] = smallest kept minus largest
- *   dropped heavy-candidate colsum (+inf when nothing is dropped by score);
+ *   dropped heavy-candidate ranking key (the colsum, or the mean weight in
+ *   score_mode 1; +inf when nothing is dropped by score);
  *   dropped_mass [nh] = sum of dropped colsums.
  * Returns 0, or -1 on bad arguments. */
-int h2o_oracle_prefill(int nh, int d, int L, int k_heavy, int k_local,
+int h2o_oracle_prefill(int nh, int d, int L, int k_heavy, int k_local, int n_sink, int score_mode,
                        const double *Q, const double *K, const double *V,
                        double *O, double *lse, double *colsum,
                        int32_t *pos, double *score, double *Ks, double *Vs,
@@ -57,11 +66,12 @@ int h2o_oracle_prefill(int nh, int d, int L, int k_heavy, int k_local,
  *   out [T][nh][d] attention output of each step;
  *   evicted [T][nh] position evicted at that step (-1 = admitted without
  *   eviction; the new position itself if it was the one evicted);
- *   margin [T][nh] gap between the two smallest F_scores among the eviction
- *   candidates (+inf when there was no choice);
+ *   margin [T][nh] gap between the two smallest ranking keys among the
+ *   eviction candidates (+inf when there was no choice);
  *   evicted_mass [nh] (accumulated: sum of F_scores of evicted entries).
  * Returns 0, or -1 on bad arguments. */
-int h2o_oracle_decode(int nh, int d, int k_heavy, int k_local, int64_t p0, int T,
+int h2o_oracle_decode(int nh, int d, int k_heavy, int k_local, int n_sink, int score_mode,
+                      int64_t p0, int T,
                       int32_t *pos, double *score, double *Ks, double *Vs, int32_t *n_valid,
                       const double *q, const double *kn, const double *vn,
                       double *out, int32_t *evicted, double *margin, double *evicted_mass);

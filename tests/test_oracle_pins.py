@@ -10,6 +10,9 @@
   (live + dropped + evicted = number of attending queries);
 * brute force on tiny inputs: enumeration of every heavy-hitter subset for the
   prefill choice, and a history-based replay of the decode loop;
+* the policy variants (pinned attention sinks, mean-weight ranking): worked
+  examples, the sinks-plus-window case against the library routine with a
+  sink+band mask, and a brute-force replay that counts attending queries;
 * a planted-mistake check: mutated builds of the oracle source must each fail
   at least one of the pins above.
 
@@ -39,7 +42,7 @@ GOLDEN_FILES = sorted(glob.glob(os.path.join(GOLDEN, "*.json")))
 
 
 def _fr(s) -> float:
-    return float(Fraction(s))
+    return math.inf if s == "inf" else float(Fraction(s))
 
 
 # --------------------------------------------------------------- golden inputs
@@ -76,10 +79,17 @@ def pin_golden(path, L=None):
     rng = np.random.default_rng(7)
     Q, K, V, qd, kd, vd = _golden_inputs(g, rng)
     kh, kl = g["k_heavy"], g["k_local"]
-    r = oracle.prefill(Q, K, V, kh, kl, _L=L)
+    pol = dict(n_sink=g.get("n_sink", 0), score_mode=g.get("score_mode", 0))
+    r = oracle.prefill(Q, K, V, kh, kl, _L=L, **pol)
     np.testing.assert_allclose(r["colsum"][0], [_fr(x) for x in g["colsum"]], rtol=0, atol=1e-12)
     st = r["state"]
     assert list(st.sets()[0]) == g["prefill_set"]
+    if "prefill_set_plain" in g:  # the same prompt under plain summed scores
+        plain = oracle.prefill(Q, K, V, kh, kl, _L=L)["state"]
+        assert list(plain.sets()[0]) == g["prefill_set_plain"]
+    if "evicted_plain" in g:  # the same stream without pinned sinks
+        plain = oracle.prefill(Q, K, V, kh, kl, _L=L)["state"]
+        assert list(oracle.decode(plain, g["L"], qd, kd, vd, kh, kl, _L=L)["evicted"][:, 0]) == g["evicted_plain"]
     if "prefill_margin" in g:
         assert abs(r["margin"][0] - _fr(g["prefill_margin"])) < 1e-12
     if "prefill_dropped" in g:
@@ -90,7 +100,7 @@ def pin_golden(path, L=None):
         np.testing.assert_allclose(r["O"][0, :, 0], [_fr(x) for x in g["O"]], rtol=0, atol=1e-12)
     if g["T"] == 0:
         return
-    o = oracle.decode(st, g["L"], qd, kd, vd, kh, kl, _L=L)
+    o = oracle.decode(st, g["L"], qd, kd, vd, kh, kl, _L=L, **pol)
     assert list(o["evicted"][:, 0]) == g["evicted"]
     np.testing.assert_allclose(o["margin"][:, 0], [_fr(x) for x in g["margin"]], rtol=0, atol=1e-12)
     assert list(st.sets()[0]) == g["final_set"]
@@ -269,8 +279,120 @@ def pin_decode_bruteforce(L=None):
             assert abs(sc - math.fsum(history[int(pos)])) < 1e-12
 
 
+# ------------------------------------------------------- policy variants
+
+def pin_streaming_equals_library(L=None):
+    """n_sink = k_heavy: every heavy slot is a pinned sink, so the cache is the
+    first n_sink positions plus a window of the k_local newest, each decode
+    query at p attends to j < n_sink and p-k_local <= j <= p, and the entry
+    evicted at p is p-k_local."""
+    nh, Lp, T, d, ns, kl = 2, 12, 15, 8, 3, 4
+    Q, K, V, qd, kd, vd = _rand(nh, Lp, T, d, 31)
+    r = oracle.prefill(Q, K, V, ns, kl, _L=L, n_sink=ns)
+    st = r["state"]
+    for h in range(nh):
+        assert list(st.sets()[h]) == list(range(ns)) + list(range(Lp - kl, Lp))
+    o = oracle.decode(st, Lp, qd, kd, vd, ns, kl, _L=L, n_sink=ns)
+    for t in range(T):
+        assert (o["evicted"][t] == Lp + t - kl).all()
+    for h in range(nh):
+        assert list(st.sets()[h]) == list(range(ns)) + list(range(Lp + T - kl, Lp + T))
+        q = np.concatenate([Q[h], qd[:, h]]); k = np.concatenate([K[h], kd[:, h]])
+        v = np.concatenate([V[h], vd[:, h]])
+        n = Lp + T
+        i, j = np.meshgrid(np.arange(n), np.arange(n), indexing="ij")
+        mask = (j <= i) & ((i < Lp) | (j < ns) | (j >= i - kl))
+        np.testing.assert_allclose(o["out"][:, h], _sdpa(q, k, v, mask)[Lp:], rtol=0, atol=1e-12)
+
+
+def pin_policy_bruteforce(L=None):
+    """Replay of the loop for the variants from the full weight history: the
+    number of queries that attended to each position is counted, not derived;
+    the prefill heavy set is found by enumerating subsets of the non-sink
+    candidates; the evicted entry by comparing every candidate with every
+    other."""
+    nh, Lp, T, d, kh, kl = 2, 9, 14, 4, 3, 2
+    Q, K, V, qd, kd, vd = _rand(nh, Lp, T, d, 41)
+    for ns, mode in [(1, 0), (0, 1), (2, 1), (3, 1)]:
+        r = oracle.prefill(Q, K, V, kh, kl, _L=L, n_sink=ns, score_mode=mode)
+        st = r["state"]
+        o = oracle.decode(st, Lp, qd, kd, vd, kh, kl, _L=L, n_sink=ns, score_mode=mode)
+        causal = np.tril(np.ones((Lp, Lp), bool))
+        for h in range(nh):
+            keys = {j: K[h, j] for j in range(Lp)}
+            history = {j: [r["colsum"][h, j]] for j in range(Lp)}
+            seen = {j: int(causal[:, j].sum()) for j in range(Lp)}  # prompt queries that attended to j
+
+            def rank(j):
+                return math.fsum(history[j]) / seen[j] if mode else math.fsum(history[j])
+
+            nc = Lp - kl
+            free = [j for j in range(nc) if j >= ns]
+            heavy = max(itertools.combinations(free, kh - ns),
+                        key=lambda s: (sum(rank(j) for j in s), sorted(s, reverse=True)))
+            S = set(range(ns)) | set(heavy) | set(range(Lp - kl, Lp))
+            assert set(r["state"].sets()[h].tolist()) >= set(range(ns))
+            for t in range(T):
+                p = Lp + t
+                keys[p] = kd[t, h]
+                C = sorted(S | {p})
+                logits = [float(np.dot(qd[t, h], keys[j])) / math.sqrt(d) for j in C]
+                mx = max(logits)
+                ex = [math.exp(x - mx) for x in logits]
+                z = sum(ex)
+                for e, j in zip(ex, C):
+                    history.setdefault(j, []).append(e / z)
+                    seen[j] = seen.get(j, 0) + 1
+                if len(C) <= kh + kl:
+                    assert o["evicted"][t, h] == -1
+                    S = set(C)
+                    continue
+                E = [j for j in C if ns <= j <= p - kl]
+                loser = [j for j in E if all((rank(j), j) <= (rank(i), i) for i in E)]
+                assert len(loser) == 1
+                assert o["evicted"][t, h] == loser[0], (ns, mode, t, h)
+                S = set(C) - {loser[0]}
+            assert set(st.sets()[h].tolist()) == S
+            live = st.pos[h] >= 0
+            for pos, sc in zip(st.pos[h][live], st.score[h][live]):
+                assert abs(sc - math.fsum(history[int(pos)])) < 1e-12
+
+
+def pin_policy_invariants(L=None):
+    """Definition 4.3 and score-mass conservation hold for the variants too,
+    and the first n_sink positions never leave the cache."""
+    nh, Lp, T, d, kh, kl = 3, 30, 50, 8, 6, 5
+    Q, K, V, qd, kd, vd = _rand(nh, Lp, T, d, 51)
+    for ns, mode in [(2, 0), (0, 1), (4, 1)]:
+        r = oracle.prefill(Q, K, V, kh, kl, _L=L, n_sink=ns, score_mode=mode)
+        st = r["state"]
+        total = r["dropped_mass"].copy()
+        prev = st.sets()
+        for t in range(T):
+            p = Lp + t
+            o = oracle.decode(st, p, qd[t:t + 1], kd[t:t + 1], vd[t:t + 1], kh, kl, _L=L, n_sink=ns,
+                              score_mode=mode)
+            total += o["evicted_mass"]
+            cur = st.sets()
+            for h in range(nh):
+                c, pr = set(cur[h].tolist()), set(prev[h].tolist())
+                assert len(c) == kh + kl and len(c - pr) <= 1 and len(pr - c) <= 1
+                assert set(range(ns)) <= c and set(range(p - kl + 1, p + 1)) <= c
+                live = st.score[h][st.pos[h] >= 0].sum()
+                assert abs(live + total[h] - (p + 1)) < 1e-9 * (p + 1)
+            prev = cur
+
+
+def test_policy_arguments_checked():
+    Q, K, V, *_ = _rand(1, 8, 0, 4, 3)
+    with pytest.raises(ValueError):
+        oracle.prefill(Q, K, V, 2, 2, n_sink=3)
+    with pytest.raises(ValueError):
+        oracle.prefill(Q, K, V, 2, 2, score_mode=2)
+
+
 PINS = [pin_full_equals_library, pin_local_equals_library, pin_def43_and_mass, pin_select_bruteforce,
-        pin_decode_bruteforce] + [
+        pin_decode_bruteforce, pin_streaming_equals_library, pin_policy_bruteforce, pin_policy_invariants] + [
     (lambda path: (lambda L=None: pin_golden(path, L)))(p) for p in GOLDEN_FILES]
 
 
@@ -303,6 +425,18 @@ def test_select_bruteforce():
 
 def test_decode_bruteforce():
     pin_decode_bruteforce()
+
+
+def test_streaming_equals_library():
+    pin_streaming_equals_library()
+
+
+def test_policy_bruteforce():
+    pin_policy_bruteforce()
+
+
+def test_policy_invariants():
+    pin_policy_invariants()
 
 
 def test_naive_topk_is_not_h2o():
@@ -345,6 +479,12 @@ MUTANTS = {
     "base-2 log-sum-exp": ("if (lse) lse[i] = m + log(l);", "if (lse) lse[i] = m + log2(l);"),
     "heavy candidates include the local block": ("const int nc = L - kl;", "const int nc = L;"),
     "scores not accumulated": ("for (int j = 0; j < n; ++j) score[j] += w[j];", ";"),
+    "sinks not protected in decode": ("if (pj < ns) continue;", ";"),
+    "sinks not kept by the prefill": ("for (int j = 0; j < ns; ++j) keep[n++] = j;", ";"),
+    "decode age counts one query too few": ("p - pj + 1, mode)", "p - pj, mode)"),
+    "prefill age counts one query too many": ("rank_key(F[j], L - j, mode)", "rank_key(F[j], L - j + 1, mode)"),
+    "decode ignores the mean ranking": ("p - pj + 1, mode)", "p - pj + 1, 0)"),
+    "prefill ignores the mean ranking": ("rank_key(F[j], L - j, mode)", "rank_key(F[j], L - j, 0)"),
 }
 
 

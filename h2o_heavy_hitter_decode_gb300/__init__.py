@@ -71,6 +71,8 @@ def lib():
         L.h2o_profile_enable.argtypes = [vp, i32]
         L.h2o_set_decode_form.argtypes = [vp, i32]
         L.h2o_decode_form_used.argtypes = [vp, C.POINTER(i32)]
+        L.h2o_cache_set_policy.argtypes = [vp, i32, i32]
+        L.h2o_cache_get_policy.argtypes = [vp, C.POINTER(i32), C.POINTER(i32)]
         L.h2o_profile_read.argtypes = [vp, C.POINTER(C.c_double), C.POINTER(i64)]
         L.h2o_status_str.argtypes = [i32]
         L.h2o_status_str.restype = C.c_char_p
@@ -78,7 +80,8 @@ def lib():
         L.h2o_build_arch.restype = i32
         for f in ("h2o_cache_create", "h2o_cache_destroy", "h2o_set_stream", "h2o_prefill", "h2o_decode_step",
                   "h2o_decode_steps", "h2o_cache_export", "h2o_cache_import", "h2o_cache_info",
-                  "h2o_get_error", "h2o_profile_enable", "h2o_profile_read", "h2o_set_decode_form", "h2o_decode_form_used"):
+                  "h2o_get_error", "h2o_profile_enable", "h2o_profile_read", "h2o_set_decode_form",
+                  "h2o_decode_form_used", "h2o_cache_set_policy", "h2o_cache_get_policy"):
             getattr(L, f).restype = i32
         _lib = L
     return _lib
@@ -241,6 +244,18 @@ class H2OCache:
         f = C.c_int32()
         _check(lib().h2o_decode_form_used(self._h, C.byref(f)), "h2o_decode_form_used")
         return {0: "", 1: "per_step", 2: "cooperative", 3: "cluster"}[f.value]
+
+    def set_policy(self, n_sink: int = 0, score_mode: int = 0):
+        """Eviction variant for later calls: ``n_sink`` pinned first positions
+        (0 <= n_sink <= k_heavy) and ``score_mode`` 1 to rank by mean weight
+        instead of summed weight (see h2o_cache_set_policy)."""
+        _check(lib().h2o_cache_set_policy(self._h, int(n_sink), int(score_mode)), "h2o_cache_set_policy")
+
+    def policy(self):
+        """(n_sink, score_mode) of this cache."""
+        ns, sm = C.c_int32(), C.c_int32()
+        _check(lib().h2o_cache_get_policy(self._h, C.byref(ns), C.byref(sm)), "h2o_cache_get_policy")
+        return ns.value, sm.value
 
     def profile(self, on: bool = True):
         """Bracket each phase with CUDA events on the cache's stream."""

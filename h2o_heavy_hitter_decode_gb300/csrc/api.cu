@@ -374,6 +374,20 @@ h2o_status h2o_set_decode_form(h2o_cache_t c, int form) {
   return H2O_OK;
 }
 
+h2o_status h2o_cache_set_policy(h2o_cache_t c, int n_sink, int score_mode) {
+  if (!c || n_sink < 0 || n_sink > c->kh || (score_mode != 0 && score_mode != 1)) return H2O_EINVAL;
+  c->view.n_sink = n_sink;
+  c->view.score_mode = score_mode;
+  return H2O_OK;
+}
+
+h2o_status h2o_cache_get_policy(h2o_cache_t c, int *n_sink, int *score_mode) {
+  if (!c) return H2O_EINVAL;
+  if (n_sink) *n_sink = c->view.n_sink;
+  if (score_mode) *score_mode = c->view.score_mode;
+  return H2O_OK;
+}
+
 h2o_status h2o_decode_form_used(h2o_cache_t c, int *form) {
   if (!c || !form) return H2O_EINVAL;
   *form = c->form_used;

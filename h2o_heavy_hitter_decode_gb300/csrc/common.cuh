@@ -73,6 +73,14 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
+// Ranking key of the cache entry at position `pos` once the query at position
+// p has attended: its accumulated score, or (score_mode 1) that score over
+// the number of queries that attended to it, p - pos + 1 (an entry, once
+// cached, has seen every later query).
+__device__ __forceinline__ float rank_key(float score, long long p, int pos, int score_mode) {
+  return score_mode ? __fdiv_rn(score, (float)(p - pos + 1)) : score;
+}
+
 // Lexicographic (score, position) minimum carried with the slot index.
 struct ArgMin {
   float s;

@@ -350,21 +350,22 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const Args a) {
       }
 
       // exact weights into the scores; argmin over entries outside the local block
-      const long long lim = (long long)p - c.kl;  // eligible iff pos <= p - k_local
+      // (eligible iff n_sink <= pos <= p - k_local)
+      const long long lim = (long long)p - c.kl;
       ArgMin best{INFINITY, INT_MAX, -2};
       for (int j = tid; j < n; j += kConsumerThreads) {
         const float w = exp2f(__ldcg(lg + j) - Mg) * invL;
         const float sc = sch[j] + w;
         sch[j] = sc;
         const int pj = posh[j];
-        if ((long long)pj <= lim) {
-          const ArgMin cand{sc, pj, j};
+        if ((long long)pj <= lim && pj >= c.n_sink) {
+          const ArgMin cand{rank_key(sc, p, pj, c.score_mode), pj, j};
           if (am_less(cand, best)) best = cand;
         }
       }
       const float w_new = exp2f(__ldcg(lg + n) - Mg) * invL;
-      if (tid == 0 && c.kl == 0) {
-        const ArgMin cand{w_new, p, -1};
+      if (tid == 0 && c.kl == 0 && p >= c.n_sink) {
+        const ArgMin cand{w_new, p, -1};  // attended by one query: its mean is its weight
         if (am_less(cand, best)) best = cand;
       }
       best = warp_argmin(best);

@@ -380,22 +380,23 @@ __global__ void __launch_bounds__(kThreads, 7) decode_cluster_kernel(const CArgs
     }
 
     // ---- exact weights into the owned scores; local argmin
-    const long long lim = (long long)p - c.kl;  // eligible iff pos <= p - k_local
+    const long long lim = (long long)p - c.kl;  // eligible iff n_sink <= pos <= p - k_local
     ArgMin best{INFINITY, INT_MAX, -2};
     if (warp < kConsumers) {
       for (int j = tid; j < nrows; j += kConsumerThreads) {
         const float w = exp2f(lg[j] - Mg) * invL;
         const float s_new = sc[j] + w;
         sc[j] = s_new;
-        if ((long long)ps[j] <= lim) {
-          const ArgMin cand{s_new, ps[j], s0 + j};
+        const int pj = ps[j];
+        if ((long long)pj <= lim && pj >= c.n_sink) {
+          const ArgMin cand{rank_key(s_new, p, pj, c.score_mode), pj, s0 + j};
           if (am_less(cand, best)) best = cand;
         }
       }
     }
     const float w_new = (rank == 0) ? exp2f(s_lgnew - Mg) * invL : 0.f;
-    if (rank == 0 && tid == 0 && c.kl == 0) {
-      const ArgMin cand{w_new, p, -1};
+    if (rank == 0 && tid == 0 && c.kl == 0 && p >= c.n_sink) {
+      const ArgMin cand{w_new, p, -1};  // attended by one query: its mean is its weight
       if (am_less(cand, best)) best = cand;
     }
     if (warp < kConsumers) {

@@ -20,6 +20,8 @@ struct CacheView {
   int *err;          // [1]                   sticky device error flag
   int *done;         // [nh]                  per-head step flags of a persistent decode launch
   int nsplit;
+  int n_sink = 0;      // positions 0 .. n_sink-1 are never evicted (pinned attention sinks)
+  int score_mode = 0;  // 0: rank by accumulated score; 1: by score / queries that attended
 };
 
 struct DecodeStep {

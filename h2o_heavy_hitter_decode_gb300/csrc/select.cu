@@ -5,9 +5,13 @@
 // local/heavy split of "The mechanism": if the prompt fits (L <= k) every
 // position is kept; otherwise the k_local newest positions are kept plus the
 // k_heavy largest column sums among positions 0 .. L-k_local-1, equal sums
-// resolved in favour of the higher position.
+// resolved in favour of the higher position.  Policy variants ("Limitations":
+// attention-sink streaming, the old-token bias of summed scores): positions
+// below n_sink are always kept and take n_sink of the heavy slots; score_mode
+// 1 ranks position j by colsum_j / (L - j), its mean weight over the prompt
+// queries that attended to it.
 //
-// Column sums are non-negative floats, so their bit patterns order like the
+// Ranking keys are non-negative floats, so their bit patterns order like the
 // values.  A 4-pass radix select (8-bit digits, per-warp shared histograms)
 // finds the threshold pattern and how many of the equal-to-threshold
 // positions to keep; a block-wide ballot scan then assigns slots in ascending
@@ -37,19 +41,24 @@ __global__ void __launch_bounds__(kThreads) select_gather(const CacheView c, con
   int32_t *posh = c.pos + (size_t)h * k;
   float *sch = c.score + (size_t)h * k;
   const bool keep_all = L <= k;
-  const int nc = keep_all ? L : L - kl;  // heavy-hitter candidates 0 .. nc-1
-  const bool by_score = !keep_all && kh > 0;
+  const int nc = keep_all ? L : L - kl;  // heavy-hitter candidates n_sink .. nc-1
+  const int ns = c.n_sink, mode = c.score_mode;
+  const bool by_score = !keep_all && kh > ns;
+  auto rank_of = [&](int j) -> uint32_t {
+    const float v = cs[j];
+    return __float_as_uint(mode ? __fdiv_rn(v, (float)(L - j)) : v);
+  };
 
   uint32_t thr = 0;
   int need = 0, eq_total = 0;
   if (by_score) {
     uint32_t prefix = 0, pmask = 0;
-    unsigned want = (unsigned)kh;
+    unsigned want = (unsigned)(kh - ns);
     for (int shift = 24; shift >= 0; shift -= 8) {
       for (int b = tid; b < kWarps * 256; b += kThreads) (&hist[0][0])[b] = 0u;
       __syncthreads();
-      for (int j = tid; j < nc; j += kThreads) {
-        const uint32_t key = __float_as_uint(cs[j]);
+      for (int j = ns + tid; j < nc; j += kThreads) {
+        const uint32_t key = rank_of(j);
         if ((key & pmask) == prefix) atomicAdd(&hist[warp][(key >> shift) & 255u], 1u);
       }
       __syncthreads();
@@ -88,10 +97,10 @@ __global__ void __launch_bounds__(kThreads) select_gather(const CacheView c, con
     const int j = base + tid;
     const bool in = j < L;
     const float v = in ? cs[j] : 0.f;
-    const uint32_t key = __float_as_uint(v);
+    const uint32_t key = in ? rank_of(j) : 0u;
     bool keep = false, eq = false;
     if (in) {
-      if (keep_all || j >= nc) keep = true;
+      if (keep_all || j >= nc || j < ns) keep = true;
       else if (by_score) {
         if (key > thr) keep = true;
         else if (key == thr) eq = true;

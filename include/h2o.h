@@ -124,6 +124,26 @@ h2o_status h2o_set_decode_form(h2o_cache_t cache, int form);
  * 0 before any decode call. */
 h2o_status h2o_decode_form_used(h2o_cache_t cache, int *form);
 
+/* Eviction policy variants of one cache (explainer page "Limitations":
+ * attention-sink streaming as the contrasting policy, and the bias of summed
+ * scores towards older tokens).  Both 0 (the default) is plain H2O.
+ *   n_sink      0 <= n_sink <= k_heavy: positions 0 .. n_sink-1 are pinned
+ *               attention sinks, never evicted; they take n_sink of the
+ *               k_heavy slots, so the prefill keeps them, the k_heavy - n_sink
+ *               best-ranked positions of n_sink .. L-k_local-1 and the
+ *               k_local newest.  n_sink = k_heavy is a sinks-plus-window
+ *               cache.
+ *   score_mode  0: rank entries by accumulated score; 1: by accumulated score
+ *               divided by the number of queries that attended to the entry
+ *               (L - j after the prefill for prompt position j, p - j + 1
+ *               after the decode step at p).  The stored scores stay plain
+ *               sums either way.
+ * Applies to every later prefill and decode call; host-only, no device
+ * work.  H2O_EINVAL for out-of-range values (nothing changes). */
+h2o_status h2o_cache_set_policy(h2o_cache_t cache, int n_sink, int score_mode);
+/* Current policy (either pointer may be NULL). */
+h2o_status h2o_cache_get_policy(h2o_cache_t cache, int *n_sink, int *score_mode);
+
 /* Copy the cache state out to device buffers: pos [B][H][k] int32,
  * score [B][H][k] fp32, K, V [B][H][k][d] (any may be NULL); next_pos and
  * n_valid (host, may be NULL) receive the position the next decode token

@@ -3,8 +3,9 @@ the bench's parity leg.
 
 Tolerances (fixed by the method's acceptance rules):
   * cache sets: bit-exact; a mismatch is permitted only where the oracle's
-    eviction margin (gap between the two lowest candidate scores; for prefill
-    the gap between the smallest kept and largest dropped column sum) is at or
+    eviction margin (gap between the two lowest candidate ranking keys; for
+    prefill the gap between the smallest kept and largest dropped key; the
+    key is the score, or the mean weight under score_mode 1) is at or
     below 1e-5, and it is then counted, the GPU is resynchronised from the
     oracle's state through h2o_cache_import, and the run continues;
   * attention outputs: max abs error <= 1e-4 (fp32 cache) or 2e-2 (bf16);
@@ -97,9 +98,10 @@ def compare_scores(rep: Report, g_pos, g_score, o_st: oracle.State, heads):
 
 
 def run_parity(w, T=None, heads=None, resync=True, check=True, prompt=None, dec=None, want_O=True,
-               decode_form="auto"):
+               decode_form="auto", policy=(0, 0)):
     """Prefill + T decode steps on the GPU through the C ABI, against the
-    oracle on `heads` (all heads when None; resynchronisation needs all)."""
+    oracle on `heads` (all heads when None; resynchronisation needs all).
+    `policy` = (n_sink, score_mode) of both sides."""
     T = w.T if T is None else T
     nh = w.nh
     hs = list(range(nh)) if heads is None else list(heads)
@@ -110,12 +112,14 @@ def run_parity(w, T=None, heads=None, resync=True, check=True, prompt=None, dec=
 
     cache = H2OCache(w.B, w.H, w.d, w.k_heavy, w.k_local, tdtype(w))
     cache.set_decode_form(decode_form)
+    pol = dict(n_sink=policy[0], score_mode=policy[1])
+    cache.set_policy(**pol)
     shp = (w.B, w.H, w.L, w.d)
     O, lse, colsum = cache.prefill(to_dev(Qs, w, shp), to_dev(Ks, w, shp), to_dev(Vs, w, shp), want_O=want_O)
     torch.cuda.synchronize()
 
     cv = lambda x: synth.as_f64(x, w.dtype)
-    r = oracle.prefill(cv(Qs[hs]), cv(Ks[hs]), cv(Vs[hs]), w.k_heavy, w.k_local)
+    r = oracle.prefill(cv(Qs[hs]), cv(Ks[hs]), cv(Vs[hs]), w.k_heavy, w.k_local, **pol)
     if O is not None:
         rep.max_O_err = float(np.max(np.abs(f64(O).reshape(nh, w.L, w.d)[hs] - r["O"])))
     rep.max_lse_err = float(np.max(np.abs(f64(lse).reshape(nh, w.L)[hs] - r["lse"])))
@@ -163,7 +167,7 @@ def run_parity(w, T=None, heads=None, resync=True, check=True, prompt=None, dec=
             qs, ks, vs = synth.decode(w, t0, n)
         q64, k64, v64 = cv(qs[:, hs]), cv(ks[:, hs]), cv(vs[:, hs])
         st_start = o_st.copy()
-        od = oracle.decode(o_st, w.L + t0, q64, k64, v64, w.k_heavy, w.k_local)
+        od = oracle.decode(o_st, w.L + t0, q64, k64, v64, w.k_heavy, w.k_local, **pol)
         o_ev, o_mg, o_out = od["evicted"], od["margin"], od["out"]
         finite = o_mg[:, alive][np.isfinite(o_mg[:, alive])]
         if finite.size:
@@ -206,7 +210,7 @@ def run_parity(w, T=None, heads=None, resync=True, check=True, prompt=None, dec=
                 assert np.all(mg <= MARGIN_TOL), (t0 + t + first, [hs[c] for c in cols], mg)
             st = st_start.copy()
             oracle.decode(st, w.L + t0, q64[:t + first + 1], k64[:t + first + 1], v64[:t + first + 1],
-                          w.k_heavy, w.k_local, want_out=False)
+                          w.k_heavy, w.k_local, want_out=False, **pol)
             import_oracle_state(cache, st, w, w.L + t0 + t + first + 1)
             rep.resyncs += 1
             t = t + first + 1

@@ -45,9 +45,9 @@ def load(path: str):
     source for the tests' planted-mistake checks)."""
     L = C.CDLL(path)
     dp, ip = C.POINTER(C.c_double), C.POINTER(C.c_int32)
-    L.h2o_oracle_prefill.argtypes = [C.c_int] * 7 + [dp] * 6 + [ip, dp, dp, dp, ip, dp, dp]
+    L.h2o_oracle_prefill.argtypes = [C.c_int] * 8 + [dp] * 6 + [ip, dp, dp, dp, dp, dp, ip, dp, dp]
     L.h2o_oracle_prefill.restype = C.c_int
-    L.h2o_oracle_decode.argtypes = [C.c_int] * 6 + [C.c_int64, C.c_int] + [ip, dp, dp, dp, ip] + \
+    L.h2o_oracle_decode.argtypes = [C.c_int] * 7 + [C.c_int64, C.c_int] + [ip, dp, dp, dp, dp, dp, ip] + \
         [dp] * 3 + [dp, ip, dp, dp]
     L.h2o_oracle_decode.restype = C.c_int
     L.h2o_oracle_set_threads.argtypes = [C.c_int]
@@ -83,12 +83,15 @@ class State:
         self.score = np.zeros((nh, k), np.float64)
         self.K = np.zeros((nh, k, d), np.float64)
         self.V = np.zeros((nh, k, d), np.float64)
+        self.Ksc = np.ones((nh, k), np.float64)  # per-row scales of an fp8 cache
+        self.Vsc = np.ones((nh, k), np.float64)
         self.n_valid = np.zeros(nh, np.int32)
 
     def copy(self) -> "State":
         s = State.__new__(State)
-        s.pos, s.score, s.K, s.V, s.n_valid = (self.pos.copy(), self.score.copy(), self.K.copy(),
-                                               self.V.copy(), self.n_valid.copy())
+        s.pos, s.score, s.K, s.V, s.Ksc, s.Vsc, s.n_valid = (
+            self.pos.copy(), self.score.copy(), self.K.copy(), self.V.copy(), self.Ksc.copy(),
+            self.Vsc.copy(), self.n_valid.copy())
         return s
 
     def sets(self):
@@ -96,10 +99,12 @@ class State:
         return [np.sort(p[p >= 0]) for p in self.pos]
 
 
-def prefill(Q, K, V, k_heavy: int, k_local: int, _L=None, n_sink: int = 0, score_mode: int = 0):
+def prefill(Q, K, V, k_heavy: int, k_local: int, _L=None, n_sink: int = 0, score_mode: int = 0,
+            kv_fp8: bool = False):
     """Q, K, V: float64 [nh, L, d].  Returns dict with O, lse, colsum, state,
-    margin, dropped_mass.  ``n_sink`` pins the first positions and
-    ``score_mode`` 1 ranks by mean weight (see ``h2o_oracle.h``)."""
+    margin, dropped_mass.  ``n_sink`` pins the first positions,
+    ``score_mode`` 1 ranks by mean weight and ``kv_fp8`` stores cached rows
+    as e4m3 with per-row scales (see ``h2o_oracle.h``)."""
     Q, K, V = (np.ascontiguousarray(x, np.float64) for x in (Q, K, V))
     nh, L, d = Q.shape
     k = k_heavy + k_local
@@ -109,16 +114,17 @@ def prefill(Q, K, V, k_heavy: int, k_local: int, _L=None, n_sink: int = 0, score
     colsum = np.empty((nh, L))
     margin = np.empty(nh)
     dropped = np.empty(nh)
-    rc = (_L or lib()).h2o_oracle_prefill(nh, d, L, k_heavy, k_local, n_sink, score_mode, _p(Q), _p(K), _p(V),
-                                          _p(O), _p(lse), _p(colsum), _p(st.pos, C.c_int32), _p(st.score), _p(st.K), _p(st.V),
-                                  _p(st.n_valid, C.c_int32), _p(margin), _p(dropped))
+    rc = (_L or lib()).h2o_oracle_prefill(nh, d, L, k_heavy, k_local, n_sink, score_mode, int(kv_fp8), _p(Q),
+                                          _p(K), _p(V), _p(O), _p(lse), _p(colsum), _p(st.pos, C.c_int32),
+                                          _p(st.score), _p(st.K), _p(st.V), _p(st.Ksc), _p(st.Vsc),
+                                          _p(st.n_valid, C.c_int32), _p(margin), _p(dropped))
     if rc != 0:
         raise ValueError("h2o_oracle_prefill: bad arguments")
     return dict(O=O, lse=lse, colsum=colsum, state=st, margin=margin, dropped_mass=dropped)
 
 
 def decode(state: State, p0: int, q, k, v, k_heavy: int, k_local: int, want_out: bool = True,
-           _L=None, n_sink: int = 0, score_mode: int = 0):
+           _L=None, n_sink: int = 0, score_mode: int = 0, kv_fp8: bool = False):
     """Run T decode steps in place on ``state``.  q, k, v: float64 [T, nh, d].
     Returns dict with out [T, nh, d], evicted [T, nh], margin [T, nh],
     evicted_mass [nh]."""
@@ -128,9 +134,10 @@ def decode(state: State, p0: int, q, k, v, k_heavy: int, k_local: int, want_out:
     ev = np.empty((T, nh), np.int32)
     mg = np.empty((T, nh))
     em = np.zeros(nh)
-    rc = (_L or lib()).h2o_oracle_decode(nh, d, k_heavy, k_local, n_sink, score_mode, int(p0), T,
-                                         _p(state.pos, C.c_int32), _p(state.score), _p(state.K), _p(state.V), _p(state.n_valid, C.c_int32),
-                                 _p(q), _p(k), _p(v), _p(out), _p(ev, C.c_int32), _p(mg), _p(em))
+    rc = (_L or lib()).h2o_oracle_decode(nh, d, k_heavy, k_local, n_sink, score_mode, int(kv_fp8), int(p0), T,
+                                         _p(state.pos, C.c_int32), _p(state.score), _p(state.K), _p(state.V),
+                                         _p(state.Ksc), _p(state.Vsc), _p(state.n_valid, C.c_int32),
+                                         _p(q), _p(k), _p(v), _p(out), _p(ev, C.c_int32), _p(mg), _p(em))
     if rc != 0:
         raise ValueError("h2o_oracle_decode: bad arguments")
     return dict(out=out, evicted=ev, margin=mg, evicted_mass=em)

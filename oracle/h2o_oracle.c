@@ -31,6 +31,52 @@ static double dot(const double *a, const double *b, int d) {
   return s;
 }
 
+/* ------------------------------------------------------ fp8 cache rows */
+
+/* Nearest e4m3 value (OCP FP8 "E4M3FN": 1 sign, 4 exponent bits with bias 7,
+ * 3 mantissa bits, no infinities; largest finite 448, smallest subnormal
+ * 2^-9), ties to even, saturating at 448.  Written from the format's
+ * definition: the quantum of a normal value in [2^E, 2^(E+1)) is 2^(E-3),
+ * below 2^-6 it is the subnormal step 2^-9. */
+static double e4m3_round(double x) {
+  const double a = fabs(x);
+  if (a >= 448.0) return copysign(448.0, x);
+  double quantum = ldexp(1.0, -9);
+  if (a >= ldexp(1.0, -6)) {
+    int e;
+    frexp(a, &e); /* a = f * 2^e, f in [0.5, 1): a in [2^(e-1), 2^e) */
+    quantum = ldexp(1.0, e - 1 - 3);
+  }
+  return copysign(nearbyint(a / quantum) * quantum, x); /* default mode: ties to even */
+}
+
+/* Store one row the way an fp8 cache holds it ("H2O-c"-style composition
+ * with quantisation, explainer page "Limitations" and the quantisation
+ * compatibility claim): one fp32 scale per row, scale = amax / 448 in fp32
+ * (0 for an all-zero row), code_c = e4m3(x_c / scale) with the division in
+ * fp32; the row reads back as code_c * scale (exact in double). */
+static void fp8_store_row(const double *x, int d, double *row, double *scale) {
+  float amax = 0.f;
+  for (int c = 0; c < d; ++c) {
+    const float a = fabsf((float)x[c]);
+    if (a > amax) amax = a;
+  }
+  const float sc = amax / 448.0f;
+  for (int c = 0; c < d; ++c)
+    row[c] = (sc > 0.f) ? e4m3_round((double)((float)x[c] / sc)) * (double)sc : 0.0;
+  *scale = (double)sc;
+}
+
+/* Copy a K/V row into a cache slot: verbatim, or as an fp8 row. */
+static void store_row(const double *x, int d, int fp8, double *row, double *scale) {
+  if (fp8) {
+    fp8_store_row(x, d, row, scale);
+  } else {
+    memcpy(row, x, sizeof(double) * (size_t)d);
+    if (scale) *scale = 1.0;
+  }
+}
+
 /* ---------------------------------------------------------------- prefill */
 
 typedef struct {
@@ -71,9 +117,9 @@ static double rank_key(double F, int64_t attended, int score_mode) {
   return score_mode ? F / (double)attended : F;
 }
 
-static void prefill_head(int d, int L, int kh, int kl, int ns, int mode, const double *Q, const double *K,
-                         const double *V, double *O, double *lse, double *colsum,
-                         int32_t *pos, double *score, double *Ks, double *Vs,
+static void prefill_head(int d, int L, int kh, int kl, int ns, int mode, int fp8, const double *Q,
+                         const double *K, const double *V, double *O, double *lse, double *colsum,
+                         int32_t *pos, double *score, double *Ks, double *Vs, double *Ksc, double *Vsc,
                          int32_t *n_valid, double *margin, double *dropped_mass) {
   const int k = kh + kl;
   const double scale = 1.0 / sqrt((double)d);
@@ -137,13 +183,15 @@ static void prefill_head(int d, int L, int kh, int kl, int ns, int mode, const d
       const int j = keep[s];
       pos[s] = j;
       score[s] = F[j];
-      memcpy(ks, K + (size_t)j * d, sizeof(double) * (size_t)d);
-      memcpy(vs, V + (size_t)j * d, sizeof(double) * (size_t)d);
+      store_row(K + (size_t)j * d, d, fp8, ks, Ksc ? Ksc + s : NULL);
+      store_row(V + (size_t)j * d, d, fp8, vs, Vsc ? Vsc + s : NULL);
     } else {
       pos[s] = -1;
       score[s] = 0.0;
       memset(ks, 0, sizeof(double) * (size_t)d);
       memset(vs, 0, sizeof(double) * (size_t)d);
+      if (Ksc) Ksc[s] = fp8 ? 0.0 : 1.0;
+      if (Vsc) Vsc[s] = fp8 ? 0.0 : 1.0;
     }
   }
   *n_valid = n;
@@ -155,22 +203,24 @@ static void prefill_head(int d, int L, int kh, int kl, int ns, int mode, const d
 }
 
 int h2o_oracle_prefill(int nh, int d, int L, int k_heavy, int k_local, int n_sink, int score_mode,
-                       const double *Q, const double *K, const double *V,
+                       int kv_fp8, const double *Q, const double *K, const double *V,
                        double *O, double *lse, double *colsum,
-                       int32_t *pos, double *score, double *Ks, double *Vs,
+                       int32_t *pos, double *score, double *Ks, double *Vs, double *Ksc, double *Vsc,
                        int32_t *n_valid, double *margin, double *dropped_mass) {
   if (nh < 0 || d < 1 || L < 1 || k_heavy < 0 || k_local < 0 || k_heavy + k_local < 1)
     return -1;
   if (n_sink < 0 || n_sink > k_heavy || (score_mode != 0 && score_mode != 1)) return -1;
+  if (kv_fp8 != 0 && kv_fp8 != 1) return -1;
   if (!Q || !K || !V || !pos || !score || !Ks || !Vs || !n_valid) return -1;
   const int k = k_heavy + k_local;
 #pragma omp parallel for schedule(dynamic, 1)
   for (int h = 0; h < nh; ++h) {
     const size_t hl = (size_t)h * L;
-    prefill_head(d, L, k_heavy, k_local, n_sink, score_mode, Q + hl * d, K + hl * d, V + hl * d,
-                 O ? O + hl * d : NULL, lse ? lse + hl : NULL, colsum ? colsum + hl : NULL,
+    prefill_head(d, L, k_heavy, k_local, n_sink, score_mode, kv_fp8, Q + hl * d, K + hl * d,
+                 V + hl * d, O ? O + hl * d : NULL, lse ? lse + hl : NULL, colsum ? colsum + hl : NULL,
                  pos + (size_t)h * k, score + (size_t)h * k, Ks + (size_t)h * k * d,
-                 Vs + (size_t)h * k * d, n_valid + h, margin ? margin + h : NULL,
+                 Vs + (size_t)h * k * d, Ksc ? Ksc + (size_t)h * k : NULL,
+                 Vsc ? Vsc + (size_t)h * k : NULL, n_valid + h, margin ? margin + h : NULL,
                  dropped_mass ? dropped_mass + h : NULL);
   }
   return 0;
@@ -186,8 +236,9 @@ int h2o_oracle_prefill(int nh, int d, int L, int k_heavy, int k_local, int n_sin
  * Variants: positions below n_sink are never candidates; score_mode 1 ranks
  * by F_score over the number of queries that attended to the entry, which at
  * step p is p - position + 1 (an entry, once cached, saw every later query). */
-static void decode_head(int d, int kh, int kl, int ns, int mode, int64_t p0, int T, int nh, int h,
-                        int32_t *pos, double *score, double *Ks, double *Vs, int32_t *n_valid,
+static void decode_head(int d, int kh, int kl, int ns, int mode, int fp8, int64_t p0, int T, int nh,
+                        int h, int32_t *pos, double *score, double *Ks, double *Vs, double *Ksc,
+                        double *Vsc, int32_t *n_valid,
                         const double *q, const double *kn, const double *vn, double *out,
                         int32_t *evicted, double *margin, double *evicted_mass) {
   const int k = kh + kl;
@@ -234,8 +285,8 @@ static void decode_head(int d, int kh, int kl, int ns, int mode, int64_t p0, int
       /* |S| < k: admit. */
       pos[n] = (int32_t)p;
       score[n] = w_new;
-      memcpy(Ks + (size_t)n * d, kt, sizeof(double) * (size_t)d);
-      memcpy(Vs + (size_t)n * d, vt, sizeof(double) * (size_t)d);
+      store_row(kt, d, fp8, Ks + (size_t)n * d, Ksc ? Ksc + n : NULL);
+      store_row(vt, d, fp8, Vs + (size_t)n * d, Vsc ? Vsc + n : NULL);
       *n_valid = n + 1;
     } else {
       /* Full: lowest (F_score, position) outside the local block leaves. */
@@ -264,8 +315,8 @@ static void decode_head(int d, int kh, int kl, int ns, int mode, int64_t p0, int
         if (evicted_mass) *evicted_mass += score[best];
         pos[best] = (int32_t)p;
         score[best] = w_new;
-        memcpy(Ks + (size_t)best * d, kt, sizeof(double) * (size_t)d);
-        memcpy(Vs + (size_t)best * d, vt, sizeof(double) * (size_t)d);
+        store_row(kt, d, fp8, Ks + (size_t)best * d, Ksc ? Ksc + best : NULL);
+        store_row(vt, d, fp8, Vs + (size_t)best * d, Vsc ? Vsc + best : NULL);
       } else {
         ev = (int32_t)p; /* the new entry itself (only when k_local = 0) */
         if (evicted_mass) *evicted_mass += w_new;
@@ -279,20 +330,23 @@ static void decode_head(int d, int kh, int kl, int ns, int mode, int64_t p0, int
 }
 
 int h2o_oracle_decode(int nh, int d, int k_heavy, int k_local, int n_sink, int score_mode,
-                      int64_t p0, int T,
-                      int32_t *pos, double *score, double *Ks, double *Vs, int32_t *n_valid,
+                      int kv_fp8, int64_t p0, int T,
+                      int32_t *pos, double *score, double *Ks, double *Vs, double *Ksc, double *Vsc,
+                      int32_t *n_valid,
                       const double *q, const double *kn, const double *vn,
                       double *out, int32_t *evicted, double *margin, double *evicted_mass) {
   if (nh < 0 || d < 1 || T < 0 || k_heavy < 0 || k_local < 0 || k_heavy + k_local < 1 || p0 < 0)
     return -1;
   if (n_sink < 0 || n_sink > k_heavy || (score_mode != 0 && score_mode != 1)) return -1;
   if (p0 + (int64_t)T > (int64_t)0x7fffffff) return -1;
+  if (kv_fp8 != 0 && kv_fp8 != 1) return -1;
   if (!pos || !score || !Ks || !Vs || !n_valid || (T > 0 && (!q || !kn || !vn))) return -1;
   const int k = k_heavy + k_local;
 #pragma omp parallel for schedule(dynamic, 1)
   for (int h = 0; h < nh; ++h) {
-    decode_head(d, k_heavy, k_local, n_sink, score_mode, p0, T, nh, h, pos + (size_t)h * k, score + (size_t)h * k,
-                Ks + (size_t)h * k * d, Vs + (size_t)h * k * d, n_valid + h, q, kn, vn, out,
+    decode_head(d, k_heavy, k_local, n_sink, score_mode, kv_fp8, p0, T, nh, h, pos + (size_t)h * k,
+                score + (size_t)h * k, Ks + (size_t)h * k * d, Vs + (size_t)h * k * d,
+                Ksc ? Ksc + (size_t)h * k : NULL, Vsc ? Vsc + (size_t)h * k : NULL, n_valid + h, q, kn, vn, out,
                 evicted, margin, evicted_mass ? evicted_mass + h : NULL);
   }
   return 0;

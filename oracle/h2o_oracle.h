@@ -30,6 +30,11 @@
  *     F_score / (number of queries that attended to the entry) — L - j for
  *     prompt position j after the prefill, p - j + 1 after the step at p.
  *     The stored F_score stays the plain sum.
+ * fp8 cache (kv_fp8 = 1): every K/V row written into a slot is stored as
+ *   e4m3 codes with one fp32 scale per row (scale = amax/448 in fp32, 0 for
+ *   an all-zero row; code = nearest-even e4m3 of x/scale, the division in
+ *   fp32, saturating at 448) and read back as code * scale.  The prefill's
+ *   own attention and each decode step's new token use the input values.
  *
  * All arrays are row-major doubles (int32 for positions).  A "head" is one
  * (batch, head) pair; heads are independent.
@@ -48,20 +53,23 @@ extern "C" {
  *   log-sum-exp of each query row, colsum [nh][L] column sums of the causal
  *   softmax, and the initial cache of each head in k slots:
  *   pos [nh][k] (ascending positions, -1 past n_valid), score [nh][k],
- *   Ks, Vs [nh][k][d]; n_valid [nh]; margin [nh] = smallest kept minus largest
+ *   Ks, Vs [nh][k][d] (the values the cache reads back); Ksc, Vsc [nh][k]
+ *   (may be NULL) the per-row scales (1 without kv_fp8; 0 for empty slots
+ *   with it); n_valid [nh]; margin [nh] = smallest kept minus largest
  *   dropped heavy-candidate ranking key (the colsum, or the mean weight in
  *   score_mode 1; +inf when nothing is dropped by score);
  *   dropped_mass [nh] = sum of dropped colsums.
  * Returns 0, or -1 on bad arguments. */
 int h2o_oracle_prefill(int nh, int d, int L, int k_heavy, int k_local, int n_sink, int score_mode,
-                       const double *Q, const double *K, const double *V,
+                       int kv_fp8, const double *Q, const double *K, const double *V,
                        double *O, double *lse, double *colsum,
-                       int32_t *pos, double *score, double *Ks, double *Vs,
+                       int32_t *pos, double *score, double *Ks, double *Vs, double *Ksc, double *Vsc,
                        int32_t *n_valid, double *margin, double *dropped_mass);
 
 /* T decode steps of nh heads starting at absolute position p0 (the first new
  * token's position).  State (k slots per head) is read and updated in place:
- *   pos [nh][k], score [nh][k], Ks, Vs [nh][k][d], n_valid [nh].
+ *   pos [nh][k], score [nh][k], Ks, Vs [nh][k][d], Ksc, Vsc [nh][k] (may be
+ *   NULL), n_valid [nh].
  * Step inputs q, kn, vn: [T][nh][d] (step-major).  Outputs (any may be NULL):
  *   out [T][nh][d] attention output of each step;
  *   evicted [T][nh] position evicted at that step (-1 = admitted without
@@ -71,8 +79,9 @@ int h2o_oracle_prefill(int nh, int d, int L, int k_heavy, int k_local, int n_sin
  *   evicted_mass [nh] (accumulated: sum of F_scores of evicted entries).
  * Returns 0, or -1 on bad arguments. */
 int h2o_oracle_decode(int nh, int d, int k_heavy, int k_local, int n_sink, int score_mode,
-                      int64_t p0, int T,
-                      int32_t *pos, double *score, double *Ks, double *Vs, int32_t *n_valid,
+                      int kv_fp8, int64_t p0, int T,
+                      int32_t *pos, double *score, double *Ks, double *Vs, double *Ksc, double *Vsc,
+                      int32_t *n_valid,
                       const double *q, const double *kn, const double *vn,
                       double *out, int32_t *evicted, double *margin, double *evicted_mass);
 

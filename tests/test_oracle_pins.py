@@ -36,6 +36,7 @@ import torch
 
 import oracle
 import synth
+from test_oracle_fp8 import FP8_PINS
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 GOLDEN_FILES = sorted(glob.glob(os.path.join(GOLDEN, "*.json")))
@@ -392,7 +393,8 @@ def test_policy_arguments_checked():
 
 
 PINS = [pin_full_equals_library, pin_local_equals_library, pin_def43_and_mass, pin_select_bruteforce,
-        pin_decode_bruteforce, pin_streaming_equals_library, pin_policy_bruteforce, pin_policy_invariants] + [
+        pin_decode_bruteforce, pin_streaming_equals_library, pin_policy_bruteforce,
+        pin_policy_invariants] + FP8_PINS + [
     (lambda path: (lambda L=None: pin_golden(path, L)))(p) for p in GOLDEN_FILES]
 
 
@@ -485,6 +487,14 @@ MUTANTS = {
     "prefill age counts one query too many": ("rank_key(F[j], L - j, mode)", "rank_key(F[j], L - j + 1, mode)"),
     "decode ignores the mean ranking": ("p - pj + 1, mode)", "p - pj + 1, 0)"),
     "prefill ignores the mean ranking": ("rank_key(F[j], L - j, mode)", "rank_key(F[j], L - j, 0)"),
+    "fp8 rows not scaled back": ("e4m3_round((double)((float)x[c] / sc)) * (double)sc : 0.0",
+                                 "e4m3_round((double)((float)x[c] / sc)) : 0.0"),
+    "fp8 rounding ties away from zero": ("nearbyint(a / quantum)", "round(a / quantum)"),
+    "fp8 subnormal step too fine": ("double quantum = ldexp(1.0, -9);", "double quantum = ldexp(1.0, -10);"),
+    "fp8 scale for a 240 maximum": ("amax / 448.0f", "amax / 240.0f"),
+    "fp8 decode rows stored unquantised": ("store_row(kt, d, fp8, Ks + (size_t)best * d",
+                                           "store_row(kt, d, 0, Ks + (size_t)best * d"),
+    "fp8 prefill rows stored unquantised": ("store_row(K + (size_t)j * d, d, fp8,", "store_row(K + (size_t)j * d, d, 0,"),
 }
 
 

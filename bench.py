@@ -50,19 +50,32 @@ def peaks():
     return dict(FALLBACK), "fallback"
 
 
+FP8_SUFFIX = "_kvfp8"  # workload name suffix of a run with an fp8 K/V cache (--kv fp8)
+
+
+def is_kvfp8(w):
+    return w.name.endswith(FP8_SUFFIX)
+
+
 def esize(w):
+    """Bytes per input / output element."""
     return 2 if w.dtype == "bf16" else 4
+
+
+def slot_kv_bytes(w):
+    """Stored K+V bytes of one cache slot: two rows, plus two fp32 row scales
+    for an fp8 cache."""
+    return 2 * w.d + 8 if is_kvfp8(w) else 2 * w.d * esize(w)
 
 
 def decode_alg_bytes(w):
     """Algorithmic HBM bytes of one decode step: K and V slots, position tags,
     score read+write, the step's q/k/v inputs and its output."""
-    e = esize(w)
-    return w.nh * (2 * w.k * w.d * e + 12 * w.k) + 4 * w.nh * w.d * e
+    return w.nh * (w.k * slot_kv_bytes(w) + 12 * w.k) + 4 * w.nh * w.d * esize(w)
 
 
 def kv_read_bytes(w):
-    return w.nh * 2 * w.k * w.d * esize(w)
+    return w.nh * w.k * slot_kv_bytes(w)
 
 
 def score_pass_flops(w):
@@ -76,7 +89,8 @@ def attn_pass_flops(w):
 
 def workload_config(w, extra=None):
     c = {"workload": w.name, "B": w.B, "H": w.H, "d": w.d, "prompt_L": w.L, "decode_T": w.T,
-         "k_heavy": w.k_heavy, "k_local": w.k_local, "cache_dtype": w.dtype,
+         "k_heavy": w.k_heavy, "k_local": w.k_local,
+         "cache_dtype": "e4m3 + fp32 row scale" if is_kvfp8(w) else w.dtype,
          "global_batch": w.B, "seq_len": w.L + w.T, "parallelism": "none (heads independent)",
          "l2": "flushed before every step (256 MB write)"}
     if extra:
@@ -208,7 +222,7 @@ def run_ours(args, w, rank, world, local_rank):
     stream = torch.cuda.current_stream(dev)
 
     def job():
-        c = H2OCache(w.B, w.H, w.d, w.k_heavy, w.k_local, tdt, device=dev)
+        c = H2OCache(w.B, w.H, w.d, w.k_heavy, w.k_local, tdt, device=dev, kv_fp8=is_kvfp8(w))
         c.set_decode_form(args.decode_form)
         c.profile(True)
         c.prefill(Qd, Kd, Vd, O=O, lse=lse, colsum=colsum)
@@ -350,7 +364,7 @@ def e2e(args, w, dev, hQ, hK, hV, hq, hk, hv, tdt, stream, world, dist, copy_str
         dec_done = copy_group((3, 4, 5), start_ev)
         for ev in prompt_done:
             stream.wait_event(ev)
-        c = H2OCache(w.B, w.H, w.d, w.k_heavy, w.k_local, tdt, device=dev)
+        c = H2OCache(w.B, w.H, w.d, w.k_heavy, w.k_local, tdt, device=dev, kv_fp8=is_kvfp8(w))
         c.set_decode_form(args.decode_form)
         c.prefill(dbuf[0], dbuf[1], dbuf[2], O=O, lse=lse, colsum=colsum)
         for ev in dec_done:
@@ -397,8 +411,8 @@ def oracle_job(w, data):
     import oracle
     Q, K, V, q, k, v = data
     t = time.perf_counter()
-    r = oracle.prefill(Q, K, V, w.k_heavy, w.k_local)
-    oracle.decode(r["state"], w.L, q, k, v, w.k_heavy, w.k_local)
+    r = oracle.prefill(Q, K, V, w.k_heavy, w.k_local, kv_fp8=is_kvfp8(w))
+    oracle.decode(r["state"], w.L, q, k, v, w.k_heavy, w.k_local, kv_fp8=is_kvfp8(w))
     return time.perf_counter() - t
 
 
@@ -447,6 +461,8 @@ def main():
     ap.add_argument("--prompt-len", type=int, default=None, help="override L (profiling captures)")
     ap.add_argument("--decode-steps", type=int, default=None, help="override T (profiling captures)")
     ap.add_argument("--decode-form", default="auto", choices=["auto", "per_step", "cooperative", "cluster"])
+    ap.add_argument("--kv", choices=["native", "fp8"], default="native",
+                    help="K/V cache storage: the workload's dtype, or e4m3 codes with a row scale (bf16 workloads)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
@@ -457,6 +473,10 @@ def main():
         L = w.L if args.prompt_len is None else args.prompt_len
         T = w.T if args.decode_steps is None else args.decode_steps
         w = w.with_(name=f"{w.name}[L={L},T={T}]", L=L, T=T)
+    if args.kv == "fp8":
+        if w.dtype != "bf16":
+            ap.error("--kv fp8 needs a bf16 workload")
+        w = w.with_(name=w.name + FP8_SUFFIX)
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))

@@ -24,7 +24,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libh2o.so")
 HEADER_PATH = os.path.join(os.path.dirname(_HERE), "include", "h2o.h")
 
-H2O_F32, H2O_BF16 = 0, 1
+H2O_F32, H2O_BF16, H2O_BF16_FP8KV = 0, 1, 2
 _STATUS = {0: "H2O_OK", 1: "H2O_EINVAL", 2: "H2O_ESTATE", 3: "H2O_ECUDA", 4: "H2O_ENOMEM",
            5: "H2O_EDEVICE", 6: "H2O_EUNSUPPORTED"}
 
@@ -72,6 +72,8 @@ def lib():
         L.h2o_set_decode_form.argtypes = [vp, i32]
         L.h2o_decode_form_used.argtypes = [vp, C.POINTER(i32)]
         L.h2o_cache_set_policy.argtypes = [vp, i32, i32]
+        L.h2o_cache_export_scales.argtypes = [vp, vp, vp]
+        L.h2o_cache_import_scales.argtypes = [vp, vp, vp]
         L.h2o_cache_get_policy.argtypes = [vp, C.POINTER(i32), C.POINTER(i32)]
         L.h2o_profile_read.argtypes = [vp, C.POINTER(C.c_double), C.POINTER(i64)]
         L.h2o_status_str.argtypes = [i32]
@@ -81,7 +83,8 @@ def lib():
         for f in ("h2o_cache_create", "h2o_cache_destroy", "h2o_set_stream", "h2o_prefill", "h2o_decode_step",
                   "h2o_decode_steps", "h2o_cache_export", "h2o_cache_import", "h2o_cache_info",
                   "h2o_get_error", "h2o_profile_enable", "h2o_profile_read", "h2o_set_decode_form",
-                  "h2o_decode_form_used", "h2o_cache_set_policy", "h2o_cache_get_policy"):
+                  "h2o_decode_form_used", "h2o_cache_set_policy", "h2o_cache_get_policy",
+                  "h2o_cache_export_scales", "h2o_cache_import_scales"):
             getattr(L, f).restype = i32
         _lib = L
     return _lib
@@ -112,21 +115,29 @@ class H2OCache:
     CUDA stream."""
 
     def __init__(self, B: int, H: int, d: int, k_heavy: int, k_local: int, dtype=torch.bfloat16,
-                 device=None):
+                 device=None, kv_fp8: bool = False):
+        """``dtype`` is the type of every input and output; ``kv_fp8`` (bf16
+        only) stores the K/V slots as e4m3 codes with one fp32 scale per row
+        (H2O_BF16_FP8KV)."""
         L = lib()
         self.B, self.H, self.d, self.k_heavy, self.k_local = B, H, d, k_heavy, k_local
         self.k = k_heavy + k_local
         self.dtype = dtype
+        self.kv_fp8 = bool(kv_fp8)
+        if self.kv_fp8 and dtype != torch.bfloat16:
+            raise TypeError("an fp8 K/V cache takes bf16 inputs")
+        code = H2O_BF16_FP8KV if self.kv_fp8 else _dt(dtype)
+        self.kv_dtype = torch.float8_e4m3fn if self.kv_fp8 else dtype
         self.device = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
         if self.device.type != "cuda":
             raise ValueError("H2OCache lives on a CUDA device")
         with torch.cuda.device(self.device):
-            nbytes = L.h2o_cache_workspace_bytes(B, H, d, k_heavy, k_local, _dt(dtype))
+            nbytes = L.h2o_cache_workspace_bytes(B, H, d, k_heavy, k_local, code)
             if nbytes == 0:
                 raise H2OError(1, f"h2o_cache_workspace_bytes({B},{H},{d},{k_heavy},{k_local})")
             self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=self.device)
             h = C.c_void_p()
-            _check(L.h2o_cache_create(B, H, d, k_heavy, k_local, _dt(dtype), _ptr(self.workspace),
+            _check(L.h2o_cache_create(B, H, d, k_heavy, k_local, code, _ptr(self.workspace),
                                       C.c_void_p(torch.cuda.current_stream(self.device).cuda_stream),
                                       C.byref(h)), "h2o_cache_create")
             self._h = h
@@ -199,26 +210,41 @@ class H2OCache:
         return out
 
     def export(self):
-        """Copy of the cache state: dict(pos, score, K, V, next_pos, n_valid)."""
+        """Copy of the cache state: dict(pos, score, K, V, next_pos, n_valid),
+        plus K_scale, V_scale [B,H,k] for an fp8 cache (K, V then hold the
+        e4m3 codes as torch.float8_e4m3fn)."""
         B, H, k, d = self.B, self.H, self.k, self.d
         pos = torch.empty((B, H, k), dtype=torch.int32, device=self.device)
         score = torch.empty((B, H, k), dtype=torch.float32, device=self.device)
-        K = torch.empty((B, H, k, d), dtype=self.dtype, device=self.device)
+        K = torch.empty((B, H, k, d), dtype=self.kv_dtype, device=self.device)
         V = torch.empty_like(K)
         nxt, nv = C.c_int64(), C.c_int32()
         self._sync_stream()
         _check(lib().h2o_cache_export(self._h, _ptr(pos), _ptr(score), _ptr(K), _ptr(V), C.byref(nxt), C.byref(nv)),
                "h2o_cache_export")
-        return dict(pos=pos, score=score, K=K, V=V, next_pos=nxt.value, n_valid=nv.value)
+        out = dict(pos=pos, score=score, K=K, V=V, next_pos=nxt.value, n_valid=nv.value)
+        if self.kv_fp8:
+            out["K_scale"] = torch.empty((B, H, k), dtype=torch.float32, device=self.device)
+            out["V_scale"] = torch.empty_like(out["K_scale"])
+            _check(lib().h2o_cache_export_scales(self._h, _ptr(out["K_scale"]), _ptr(out["V_scale"])),
+                   "h2o_cache_export_scales")
+        return out
 
-    def import_state(self, pos, score, K, V, next_pos: int, n_valid: int):
+    def import_state(self, pos, score, K, V, next_pos: int, n_valid: int, K_scale=None, V_scale=None):
+        """Replace the state (layouts of export; an fp8 cache also needs the
+        row scales)."""
         B, H, k, d = self.B, self.H, self.k, self.d
         self._arg(pos, (B, H, k), "pos", torch.int32)
         self._arg(score, (B, H, k), "score", torch.float32)
-        self._arg(K, (B, H, k, d), "K"); self._arg(V, (B, H, k, d), "V")
+        self._arg(K, (B, H, k, d), "K", self.kv_dtype); self._arg(V, (B, H, k, d), "V", self.kv_dtype)
+        if self.kv_fp8:
+            self._arg(K_scale, (B, H, k), "K_scale", torch.float32)
+            self._arg(V_scale, (B, H, k), "V_scale", torch.float32)
         self._sync_stream()
         _check(lib().h2o_cache_import(self._h, _ptr(pos), _ptr(score), _ptr(K), _ptr(V), int(next_pos), int(n_valid)),
                "h2o_cache_import")
+        if self.kv_fp8:
+            _check(lib().h2o_cache_import_scales(self._h, _ptr(K_scale), _ptr(V_scale)), "h2o_cache_import_scales")
 
     def info(self):
         vals = [C.c_int32() for _ in range(6)]

@@ -30,7 +30,8 @@ using namespace h2o;
 struct h2o_cache {
   int B, H, d, kh, kl, k, nh;
   h2o_dtype dtype;
-  int esize;
+  int esize;  // bytes per input / output element
+  int ssize;  // bytes per stored K/V element (1 for an fp8 cache)
   int64_t next_pos;
   int n_valid;
   bool prefilled;
@@ -62,7 +63,7 @@ bool shape_ok(int B, int H, int d, int kh, int kl, h2o_dtype dt) {
   if (B < 1 || H < 1 || kh < 0 || kl < 0) return false;
   if ((int64_t)kh + kl < 1 || (int64_t)kh + kl > (1 << 24)) return false;
   if ((int64_t)B * H > (1LL << 24)) return false;
-  if (dt != H2O_F32 && dt != H2O_BF16) return false;
+  if (dt != H2O_F32 && dt != H2O_BF16 && dt != H2O_BF16_FP8KV) return false;
   return d >= 1;
 }
 
@@ -71,16 +72,23 @@ bool d_supported(int d) { return d == 64 || d == 128; }
 int choose_nsplit(int nh, int k, int sms) { return h2o::decode_splits(nh, k, sms); }
 
 struct Layout {
-  size_t K, V, pos, score, part, logits, counter, done, err, total;
+  size_t K, V, pos, score, Ksc, Vsc, part, logits, counter, done, err, total;
 };
 
-Layout layout(int nh, int k, int d, int esize, int nsplit) {
+int input_size(h2o_dtype dt) { return dt == H2O_F32 ? 4 : 2; }
+int stored_size(h2o_dtype dt) { return dt == H2O_F32 ? 4 : dt == H2O_BF16 ? 2 : 1; }
+
+Layout layout(int nh, int k, int d, h2o_dtype dt, int nsplit) {
   Layout l;
+  const int ssize = stored_size(dt);
+  const size_t scales = dt == H2O_BF16_FP8KV ? (size_t)nh * k * sizeof(float) : 0;
   size_t o = 0;
-  l.K = o;       o = align_up(o + (size_t)nh * k * d * esize);
-  l.V = o;       o = align_up(o + (size_t)nh * k * d * esize);
+  l.K = o;       o = align_up(o + (size_t)nh * k * d * ssize);
+  l.V = o;       o = align_up(o + (size_t)nh * k * d * ssize);
   l.pos = o;     o = align_up(o + (size_t)nh * k * sizeof(int32_t));
   l.score = o;   o = align_up(o + (size_t)nh * k * sizeof(float));
+  l.Ksc = o;     o = align_up(o + scales);
+  l.Vsc = o;     o = align_up(o + scales);
   l.part = o;    o = align_up(o + (size_t)nh * nsplit * (2 + d) * sizeof(float));
   l.logits = o;  o = align_up(o + (size_t)nh * (k + 1) * sizeof(float));
   l.counter = o; o = align_up(o + (size_t)nh * sizeof(int));
@@ -145,8 +153,7 @@ size_t h2o_cache_workspace_bytes(int B, int H, int d, int k_heavy, int k_local, 
   const int sms = num_sms_current_device();
   if (sms <= 0) return 0;
   const int nh = B * H, k = k_heavy + k_local;
-  const int esize = dtype == H2O_BF16 ? 2 : 4;
-  return layout(nh, k, d, esize, choose_nsplit(nh, k, sms)).total;
+  return layout(nh, k, d, dtype, choose_nsplit(nh, k, sms)).total;
 }
 
 h2o_status h2o_cache_create(int B, int H, int d, int k_heavy, int k_local, h2o_dtype dtype,
@@ -162,16 +169,22 @@ h2o_status h2o_cache_create(int B, int H, int d, int k_heavy, int k_local, h2o_d
   if (!c) return H2O_ENOMEM;
   c->B = B; c->H = H; c->d = d; c->kh = k_heavy; c->kl = k_local;
   c->k = k_heavy + k_local; c->nh = B * H; c->dtype = dtype;
-  c->esize = dtype == H2O_BF16 ? 2 : 4;
+  c->esize = input_size(dtype);
+  c->ssize = stored_size(dtype);
   c->next_pos = 0; c->n_valid = 0; c->prefilled = false;
   c->stream = (cudaStream_t)cuda_stream;
   cudaGetDevice(&c->device);
   const int ns = choose_nsplit(c->nh, c->k, sms);
-  const Layout l = layout(c->nh, c->k, d, c->esize, ns);
+  const Layout l = layout(c->nh, c->k, d, dtype, ns);
   char *w = (char *)workspace;
   CacheView &v = c->view;
   v.nh = c->nh; v.d = d; v.k = c->k; v.kh = k_heavy; v.kl = k_local;
-  v.dtype = dtype == H2O_BF16 ? 1 : 0;
+  v.dtype = dtype == H2O_F32 ? 0 : 1;  // input type: fp32 or bf16
+  v.kv_fp8 = dtype == H2O_BF16_FP8KV ? 1 : 0;
+  if (v.kv_fp8) {
+    v.Ksc = (float *)(w + l.Ksc);
+    v.Vsc = (float *)(w + l.Vsc);
+  }
   v.K = w + l.K; v.V = w + l.V;
   v.pos = (int32_t *)(w + l.pos); v.score = (float *)(w + l.score);
   v.part = (float *)(w + l.part); v.logits = (float *)(w + l.logits);
@@ -183,6 +196,8 @@ h2o_status h2o_cache_create(int B, int H, int d, int k_heavy, int k_local, h2o_d
   if (e == cudaSuccess) e = cudaMemsetAsync(v.score, 0, (size_t)c->nh * c->k * sizeof(float), c->stream);
   if (e == cudaSuccess) e = cudaMemsetAsync(v.counter, 0, (size_t)c->nh * sizeof(int), c->stream);
   if (e == cudaSuccess) e = cudaMemsetAsync(v.err, 0, sizeof(int), c->stream);
+  if (e == cudaSuccess && v.kv_fp8)
+    e = cudaMemsetAsync(v.Ksc, 0, (l.Vsc - l.Ksc) * 2, c->stream);  // both scale arrays
   if (e != cudaSuccess) {
     delete c;
     return cuda_fail(e);
@@ -403,8 +418,8 @@ h2o_status h2o_cache_export(h2o_cache_t c, int32_t *pos, float *score, void *K, 
   if (pos) e = cudaMemcpyAsync(pos, v.pos, slots * sizeof(int32_t), cudaMemcpyDefault, c->stream);
   if (e == cudaSuccess && score)
     e = cudaMemcpyAsync(score, v.score, slots * sizeof(float), cudaMemcpyDefault, c->stream);
-  if (e == cudaSuccess && K) e = cudaMemcpyAsync(K, v.K, slots * c->d * c->esize, cudaMemcpyDefault, c->stream);
-  if (e == cudaSuccess && V) e = cudaMemcpyAsync(V, v.V, slots * c->d * c->esize, cudaMemcpyDefault, c->stream);
+  if (e == cudaSuccess && K) e = cudaMemcpyAsync(K, v.K, slots * c->d * c->ssize, cudaMemcpyDefault, c->stream);
+  if (e == cudaSuccess && V) e = cudaMemcpyAsync(V, v.V, slots * c->d * c->ssize, cudaMemcpyDefault, c->stream);
   if (e != cudaSuccess) return cuda_fail(e);
   if (next_pos) *next_pos = c->next_pos;
   if (n_valid) *n_valid = c->n_valid;
@@ -419,13 +434,32 @@ h2o_status h2o_cache_import(h2o_cache_t c, const int32_t *pos, const float *scor
   const size_t slots = (size_t)c->nh * c->k;
   cudaError_t e = cudaMemcpyAsync(v.pos, pos, slots * sizeof(int32_t), cudaMemcpyDefault, c->stream);
   if (e == cudaSuccess) e = cudaMemcpyAsync(v.score, score, slots * sizeof(float), cudaMemcpyDefault, c->stream);
-  if (e == cudaSuccess) e = cudaMemcpyAsync(v.K, K, slots * c->d * c->esize, cudaMemcpyDefault, c->stream);
-  if (e == cudaSuccess) e = cudaMemcpyAsync(v.V, V, slots * c->d * c->esize, cudaMemcpyDefault, c->stream);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(v.K, K, slots * c->d * c->ssize, cudaMemcpyDefault, c->stream);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(v.V, V, slots * c->d * c->ssize, cudaMemcpyDefault, c->stream);
   if (e != cudaSuccess) return cuda_fail(e);
   c->next_pos = next_pos;
   c->n_valid = n_valid;
   c->prefilled = true;
   return H2O_OK;
+}
+
+h2o_status h2o_cache_export_scales(h2o_cache_t c, float *Ksc, float *Vsc) {
+  if (!c) return H2O_EINVAL;
+  if (!c->view.kv_fp8) return H2O_EUNSUPPORTED;
+  const size_t bytes = (size_t)c->nh * c->k * sizeof(float);
+  cudaError_t e = cudaSuccess;
+  if (Ksc) e = cudaMemcpyAsync(Ksc, c->view.Ksc, bytes, cudaMemcpyDefault, c->stream);
+  if (e == cudaSuccess && Vsc) e = cudaMemcpyAsync(Vsc, c->view.Vsc, bytes, cudaMemcpyDefault, c->stream);
+  return e == cudaSuccess ? H2O_OK : cuda_fail(e);
+}
+
+h2o_status h2o_cache_import_scales(h2o_cache_t c, const float *Ksc, const float *Vsc) {
+  if (!c || !Ksc || !Vsc) return H2O_EINVAL;
+  if (!c->view.kv_fp8) return H2O_EUNSUPPORTED;
+  const size_t bytes = (size_t)c->nh * c->k * sizeof(float);
+  cudaError_t e = cudaMemcpyAsync(c->view.Ksc, Ksc, bytes, cudaMemcpyDefault, c->stream);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(c->view.Vsc, Vsc, bytes, cudaMemcpyDefault, c->stream);
+  return e == cudaSuccess ? H2O_OK : cuda_fail(e);
 }
 
 h2o_status h2o_cache_info(h2o_cache_t c, int *B, int *H, int *d, int *k_heavy, int *k_local, int *dtype,

@@ -2,8 +2,12 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+
+#include <type_traits>
 
 #include "internal.h"
 
@@ -16,6 +20,26 @@ constexpr float kLn2 = 0.6931471805599453f;
 template <typename T> struct VecN;
 template <> struct VecN<float> { static constexpr int N = 4; };
 template <> struct VecN<__nv_bfloat16> { static constexpr int N = 8; };
+
+// Storage element of an fp8 cache: one e4m3 byte (sign, 4 exponent bits with
+// bias 7, 3 mantissa bits; largest finite 448).  Each cached row carries one
+// fp32 scale and reads back as code * scale.
+struct e4m3 {
+  uint8_t bits;
+};
+template <typename S> constexpr bool is_fp8() { return std::is_same<S, e4m3>::value; }
+
+// How a lane reads a stored row: 16 bytes per load, 8 for an fp8 row (so an
+// fp8 row of d codes maps onto as many lanes, with as few registers, as a
+// bf16 row).
+template <typename S> struct Lane {
+  static constexpr int VB = 16;
+  using V = uint4;
+};
+template <> struct Lane<e4m3> {
+  static constexpr int VB = 8;
+  using V = uint2;
+};
 
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
@@ -51,6 +75,46 @@ template <> struct Unpack<__nv_bfloat16> {
   }
 };
 
+// Four e4m3 codes (byte i of w is element i) as floats, through the hardware
+// e4m3x2 -> f16x2 conversion (exact: every e4m3 value is an f16 value).
+// Measured on GB300 the fastest of the unpack forms tried (integer bit
+// placement and mixed-precision FMAs were slower).
+__device__ __forceinline__ void e4m3x4_to_f32(uint32_t w, float *x) {
+  const __half2_raw a = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w & 0xffffu), __NV_E4M3);
+  const __half2_raw b = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w >> 16), __NV_E4M3);
+  x[0] = __half2float(__ushort_as_half(a.x));
+  x[1] = __half2float(__ushort_as_half(a.y));
+  x[2] = __half2float(__ushort_as_half(b.x));
+  x[3] = __half2float(__ushort_as_half(b.y));
+}
+template <> struct Unpack<e4m3> {
+  // 8 codes (byte i is element i)
+  __device__ __forceinline__ static void run(const uint2 &v, float *x) {
+    e4m3x4_to_f32(v.x, x);
+    e4m3x4_to_f32(v.y, x + 4);
+  }
+};
+// One lane's share of a stored row (Lane<S>::VB bytes at p) as floats.
+template <typename S> __device__ __forceinline__ void unpack_lane(const uint8_t *p, float *x) {
+  Unpack<S>::run(*(const typename Lane<S>::V *)p, x);
+}
+
+// N consecutive elements of T as floats, 16 bytes per load (N a multiple of
+// the elements in 16 bytes): plain loads (shared memory), and read-only
+// global loads.
+template <typename T, int N> __device__ __forceinline__ void load_f32(const T *p, float *x) {
+  constexpr int V = VecN<T>::N;
+  static_assert(N % V == 0, "whole 16-byte vectors");
+#pragma unroll
+  for (int i = 0; i < N / V; ++i) Unpack<T>::run(*(const uint4 *)(p + i * V), x + i * V);
+}
+template <typename T, int N> __device__ __forceinline__ void load_f32_nc(const T *p, float *x) {
+  constexpr int V = VecN<T>::N;
+  static_assert(N % V == 0, "whole 16-byte vectors");
+#pragma unroll
+  for (int i = 0; i < N / V; ++i) Unpack<T>::run(ld_nc16(p + i * V), x + i * V);
+}
+
 template <typename T> __device__ __forceinline__ T from_f32(float x);
 template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
 template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
@@ -71,6 +135,36 @@ __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   return v;
+}
+
+// Warp-collective quantisation of one row of 32 * PER values into an fp8
+// cache row: lane L holds elements L*PER .. L*PER+PER-1 in x.  scale =
+// amax / 448 (fp32 division; 0 for an all-zero row), code = e4m3 of x / scale
+// rounded to nearest even and saturated at 448 (0 when scale is 0).  Returns
+// the lane's PER codes packed little-end first; every lane gets the scale.
+template <int PER>
+__device__ __forceinline__ uint32_t quant_row_e4m3(const float *x, float &scale) {
+  static_assert(PER == 2 || PER == 4, "a lane packs 2 or 4 codes");
+  float amax = 0.f;
+#pragma unroll
+  for (int e = 0; e < PER; ++e) amax = fmaxf(amax, fabsf(x[e]));
+  amax = warp_max(amax);
+  scale = __fdiv_rn(amax, 448.f);
+  uint32_t packed = 0u;
+  if (scale > 0.f) {
+#pragma unroll
+    for (int e = 0; e < PER; ++e)
+      packed |= (uint32_t)__nv_cvt_float_to_fp8(__fdiv_rn(x[e], scale), __NV_SATFINITE, __NV_E4M3) << (8 * e);
+  }
+  return packed;
+}
+// Store a lane's PER packed codes at byte offset lane * PER of a row.
+template <int PER>
+__device__ __forceinline__ void store_codes(uint8_t *row, int lane, uint32_t packed) {
+  if (PER == 4)
+    *(uint32_t *)(row + lane * 4) = packed;
+  else
+    *(uint16_t *)(row + lane * 2) = (uint16_t)packed;
 }
 
 // Ranking key of the cache entry at position `pos` once the query at position

@@ -22,6 +22,10 @@
 // place.  Every other CTA of that head has finished reading K/V before it took
 // its ticket, so the in-place write cannot race.
 //
+// An fp8 cache (S = e4m3) streams 1-byte codes: each K logit is scaled by its
+// row's K scale and each V row enters the accumulator with weight times its V
+// scale; the new token's row is quantised (one scale per row) when written.
+//
 // Two launch forms share this body:
 //  * per step: one grid per step, chained with programmatic dependent launch;
 //  * persistent: one cooperative grid (all CTAs resident) runs many steps.
@@ -49,11 +53,11 @@ constexpr int kStageBytes = 4096;                // per operand (K or V) per sta
 constexpr int kSmemBytes = kStages * 2 * kStageBytes;
 constexpr uint32_t kDoneSpinLimit = 1u << 24;    // polls of a head's step flag
 
-template <typename T, int D> struct Geo {
-  static constexpr int EPL = VecN<T>::N;          // elements per lane per 16-byte load
+template <typename S, int D> struct Geo {
+  static constexpr int EPL = Lane<S>::VB / (int)sizeof(S);  // elements per lane per load
   static constexpr int LPR = D / EPL;             // lanes per row
   static constexpr int RPW = 32 / LPR;            // rows per warp per pass
-  static constexpr int ROWB = D * (int)sizeof(T); // bytes per slot row
+  static constexpr int ROWB = D * (int)sizeof(S); // bytes per slot row
   static constexpr int TR = kStageBytes / ROWB;   // rows per slab
   static constexpr int ITER = TR / (kConsumers * RPW);
   static_assert(LPR >= 1 && LPR <= 32 && 32 % LPR == 0, "row must map onto a warp");
@@ -84,9 +88,11 @@ __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
-template <typename T, int D, bool kPersistent>
+// T: type of the step inputs and outputs; S: type of the stored K/V rows.
+template <typename T, typename S, int D, bool kPersistent>
 __global__ void __launch_bounds__(kThreads) decode_kernel(const Args a) {
-  using G = Geo<T, D>;
+  using G = Geo<S, D>;
+  constexpr bool kFp8 = is_fp8<S>();
   constexpr int EPL = G::EPL, LPR = G::LPR, RPW = G::RPW, ROWB = G::ROWB, TR = G::TR, ITER = G::ITER;
   extern __shared__ __align__(128) uint8_t s_ring[];  // [kStages][K | V][kStageBytes]
   __shared__ uint64_t s_full[kStages], s_empty[kStages];
@@ -189,7 +195,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const Args a) {
 
     // -------------------------------------------------------------- consumers
     float qv[EPL];
-    Unpack<T>::run(ld_nc16((const T *)a.s.q + step * step_elems + (size_t)h * D + sub * EPL), qv);
+    load_f32_nc<T, EPL>((const T *)a.s.q + step * step_elems + (size_t)h * D + sub * EPL, qv);
 #pragma unroll
     for (int e = 0; e < EPL; ++e) qv[e] *= a.qscale;
     float m = -INFINITY, l = 0.f, acc[EPL];
@@ -198,22 +204,33 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const Args a) {
     bool ok = __all_sync(0xffffffffu, mbar_wait(&s_go, step & 1));
     for (int i = 0; ok && i < nst; ++i, ++g) {
       const int st = g % kStages;
+      const int rows = min(TR, nrows - i * TR);
+      float ksc[ITER], vsc[ITER];  // row scales of an fp8 cache (read before the slab wait)
+      if (kFp8) {
+#pragma unroll
+        for (int it = 0; it < ITER; ++it) {
+          const int r = warp * RPW + grp + it * kConsumers * RPW;
+          const size_t slot = hk + r0 + (size_t)i * TR + r;
+          ksc[it] = (r < rows) ? __ldcg(c.Ksc + slot) : 0.f;
+          vsc[it] = (r < rows) ? __ldcg(c.Vsc + slot) : 0.f;
+        }
+      }
       if (!(ok = __all_sync(0xffffffffu, mbar_wait(&s_full[st], (g / kStages) & 1)))) break;
       const uint8_t *ks = s_ring + st * 2 * kStageBytes;
       const uint8_t *vs = ks + kStageBytes;
-      const int rows = min(TR, nrows - i * TR);
       float x[ITER];
       float wmax = -INFINITY;
 #pragma unroll
       for (int it = 0; it < ITER; ++it) {
         const int r = warp * RPW + grp + it * kConsumers * RPW;
         float kx[EPL];
-        Unpack<T>::run(*(const uint4 *)(ks + r * ROWB + sub * 16), kx);
+        unpack_lane<S>(ks + r * ROWB + sub * Lane<S>::VB, kx);
         float dot = 0.f;
 #pragma unroll
         for (int e = 0; e < EPL; ++e) dot = fmaf(qv[e], kx[e], dot);
 #pragma unroll
         for (int o = LPR / 2; o; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+        if (kFp8) dot *= ksc[it];
         x[it] = (r < rows) ? dot : -INFINITY;
         if (r < rows && sub == 0) lg[r0 + i * TR + r] = dot;
         wmax = fmaxf(wmax, x[it]);
@@ -233,10 +250,11 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const Args a) {
           if (r < rows) {
             const float pr = exp2f(x[it] - m);
             l += pr;
+            const float pv = kFp8 ? pr * vsc[it] : pr;
             float vx[EPL];
-            Unpack<T>::run(*(const uint4 *)(vs + r * ROWB + sub * 16), vx);
+            unpack_lane<S>(vs + r * ROWB + sub * Lane<S>::VB, vx);
 #pragma unroll
-            for (int e = 0; e < EPL; ++e) acc[e] = fmaf(pr, vx[e], acc[e]);
+            for (int e = 0; e < EPL; ++e) acc[e] = fmaf(pv, vx[e], acc[e]);
           }
         }
       }
@@ -253,7 +271,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const Args a) {
     if (*(volatile int *)&s_abort) break;
     if (has_new && warp == 0) {  // the new token, straight from the step inputs
       float kx[EPL];
-      Unpack<T>::run(ld_nc16(kn + sub * EPL), kx);
+      load_f32_nc<T, EPL>(kn + sub * EPL, kx);
       float dot = 0.f;
 #pragma unroll
       for (int e = 0; e < EPL; ++e) dot = fmaf(qv[e], kx[e], dot);
@@ -270,7 +288,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const Args a) {
         const float pr = exp2f(dot - m);
         l += pr;
         float vx[EPL];
-        Unpack<T>::run(ld_nc16(vn + sub * EPL), vx);
+        load_f32_nc<T, EPL>(vn + sub * EPL, vx);
 #pragma unroll
         for (int e = 0; e < EPL; ++e) acc[e] = fmaf(pr, vx[e], acc[e]);
       }
@@ -396,9 +414,26 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const Args a) {
       }
       consumers_sync();
       const int e = s_flag;
-      if (e >= 0) {
-        uint4 *Kw = (uint4 *)((T *)c.K + (hk + e) * D);
-        uint4 *Vw = (uint4 *)((T *)c.V + (hk + e) * D);
+      if (e >= 0 && kFp8) {
+        if (warp == 0) {  // quantise the new row: one scale per row, lane L codes elements L*PER..
+          constexpr int PER = D / 32;
+          float xk[PER], xv[PER], sk, sv;
+#pragma unroll
+          for (int j = 0; j < PER; ++j) {
+            xk[j] = to_f32<T>(kn[lane * PER + j]);
+            xv[j] = to_f32<T>(vn[lane * PER + j]);
+          }
+          const uint32_t ck = quant_row_e4m3<PER>(xk, sk), cv = quant_row_e4m3<PER>(xv, sv);
+          store_codes<PER>((uint8_t *)c.K + (hk + e) * ROWB, lane, ck);
+          store_codes<PER>((uint8_t *)c.V + (hk + e) * ROWB, lane, cv);
+          if (lane == 0) {
+            c.Ksc[hk + e] = sk;
+            c.Vsc[hk + e] = sv;
+          }
+        }
+      } else if (e >= 0) {
+        uint4 *Kw = (uint4 *)((S *)c.K + (hk + e) * D);
+        uint4 *Vw = (uint4 *)((S *)c.V + (hk + e) * D);
         for (int i = tid; i < D / EPL; i += kConsumerThreads) {
           Kw[i] = ld_nc16(kn + i * EPL);
           Vw[i] = ld_nc16(vn + i * EPL);
@@ -416,22 +451,22 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const Args a) {
   __syncthreads();
 }
 
-template <typename T, int D, bool P>
+template <typename T, typename S, int D, bool P>
 cudaError_t set_smem_attr() {
   // The shared-memory opt-in is per device; remember it per device ordinal.
   static bool done[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(decode_kernel<T, D, P>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(decode_kernel<T, S, D, P>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        kSmemBytes);
   if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
   return e;
 }
 
-template <typename T, int D>
+template <typename T, typename S, int D>
 cudaError_t launch_step_t(const CacheView &c, const DecodeStep &s, cudaStream_t st) {
   Args a{c, s, 1, kLog2e / sqrtf((float)D), nullptr};
-  cudaError_t e = set_smem_attr<T, D, false>();
+  cudaError_t e = set_smem_attr<T, S, D, false>();
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(c.nsplit * c.nh));
@@ -443,26 +478,26 @@ cudaError_t launch_step_t(const CacheView &c, const DecodeStep &s, cudaStream_t 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_kernel<T, D, false>, a);
+  return cudaLaunchKernelEx(&cfg, decode_kernel<T, S, D, false>, a);
 }
 
-template <typename T, int D>
+template <typename T, typename S, int D>
 bool persistent_fits_t(const CacheView &c) {
   int dev = 0, sms = 0, per_sm = 0, coop = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return false;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
   if (cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess || !coop) return false;
-  if (set_smem_attr<T, D, true>() != cudaSuccess) return false;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel<T, D, true>, kThreads, kSmemBytes) !=
+  if (set_smem_attr<T, S, D, true>() != cudaSuccess) return false;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel<T, S, D, true>, kThreads, kSmemBytes) !=
       cudaSuccess)
     return false;
   return (long long)c.nsplit * c.nh <= (long long)per_sm * sms;
 }
 
-template <typename T, int D>
+template <typename T, typename S, int D>
 cudaError_t launch_persistent_t(const CacheView &c, const DecodeStep &s, int nsteps, int *done, cudaStream_t st) {
   Args a{c, s, nsteps, kLog2e / sqrtf((float)D), done};
-  cudaError_t e = set_smem_attr<T, D, true>();
+  cudaError_t e = set_smem_attr<T, S, D, true>();
   if (e != cudaSuccess) return e;
   e = cudaMemsetAsync(done, 0, (size_t)c.nh * sizeof(int), st);
   if (e != cudaSuccess) return e;
@@ -476,7 +511,7 @@ cudaError_t launch_persistent_t(const CacheView &c, const DecodeStep &s, int nst
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_kernel<T, D, true>, a);
+  return cudaLaunchKernelEx(&cfg, decode_kernel<T, S, D, true>, a);
 }
 
 }  // namespace
@@ -509,15 +544,18 @@ int decode_splits(int nh, int k, int sms) {
   return best;
 }
 
-#define H2O_DISPATCH(FN, ...)                                      \
-  do {                                                            \
-    if (c.dtype == 1) {                                           \
-      if (c.d == 128) return FN<__nv_bfloat16, 128>(__VA_ARGS__); \
-      if (c.d == 64) return FN<__nv_bfloat16, 64>(__VA_ARGS__);   \
-    } else {                                                      \
-      if (c.d == 128) return FN<float, 128>(__VA_ARGS__);         \
-      if (c.d == 64) return FN<float, 64>(__VA_ARGS__);           \
-    }                                                             \
+#define H2O_DISPATCH(FN, ...)                                                      \
+  do {                                                                            \
+    if (c.dtype == 1 && c.kv_fp8) {                                               \
+      if (c.d == 128) return FN<__nv_bfloat16, e4m3, 128>(__VA_ARGS__);           \
+      if (c.d == 64) return FN<__nv_bfloat16, e4m3, 64>(__VA_ARGS__);             \
+    } else if (c.dtype == 1) {                                                    \
+      if (c.d == 128) return FN<__nv_bfloat16, __nv_bfloat16, 128>(__VA_ARGS__);  \
+      if (c.d == 64) return FN<__nv_bfloat16, __nv_bfloat16, 64>(__VA_ARGS__);    \
+    } else if (!c.kv_fp8) {                                                       \
+      if (c.d == 128) return FN<float, float, 128>(__VA_ARGS__);                  \
+      if (c.d == 64) return FN<float, float, 64>(__VA_ARGS__);                    \
+    }                                                                             \
   } while (0)
 
 cudaError_t launch_decode_step(const CacheView &c, const DecodeStep &s, cudaStream_t st) {

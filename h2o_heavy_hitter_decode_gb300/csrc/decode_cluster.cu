@@ -24,6 +24,10 @@
 //      token) and publishes the decision; cluster barrier;
 //   5. the owner of the chosen slot writes the new token's K/V row (HBM, and
 //      its resident copy) and its position tag and score.
+// An fp8 cache (S = e4m3) streams 1-byte codes; the owned rows' K and V
+// scales stay in shared memory beside the scores, each logit is scaled by its
+// K scale and each V row weighted by its V scale, and the owner quantises the
+// new token's row (one scale per row) when it writes it.
 // All synchronisation is the cluster's hardware barrier or a CTA mbarrier
 // (bounded waits); there is no global atomic, fence round trip or spin between
 // CTAs, and clusters never wait on one another.
@@ -49,11 +53,11 @@ constexpr int kStageBytes = 4096;  // per operand per slab
 constexpr int ring_bytes(int stages) { return stages * 2 * kStageBytes; }
 constexpr int kResidentMaxBytes = 96 * 1024;  // K+V rows of one CTA kept in shared memory
 
-template <typename T, int D> struct Geo {
-  static constexpr int EPL = VecN<T>::N;
+template <typename S, int D> struct Geo {
+  static constexpr int EPL = Lane<S>::VB / (int)sizeof(S);  // elements per lane per load
   static constexpr int LPR = D / EPL;
   static constexpr int RPW = 32 / LPR;
-  static constexpr int ROWB = D * (int)sizeof(T);
+  static constexpr int ROWB = D * (int)sizeof(S);
   static constexpr int TR = kStageBytes / ROWB;  // rows per slab
   static constexpr int ITER = TR / (kConsumers * RPW);
   static_assert(ITER >= 1 && TR % (kConsumers * RPW) == 0, "slab must split evenly over warps");
@@ -69,9 +73,11 @@ struct CArgs {
 
 __device__ __forceinline__ void consumers_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
-template <typename T, int D, bool kResident, int kStages>
+// T: type of the step inputs and outputs; S: type of the stored K/V rows.
+template <typename T, typename S, int D, bool kResident, int kStages>
 __global__ void __launch_bounds__(kThreads, 7) decode_cluster_kernel(const CArgs a) {
-  using G = Geo<T, D>;
+  using G = Geo<S, D>;
+  constexpr bool kFp8 = is_fp8<S>();
   constexpr int EPL = G::EPL, LPR = G::LPR, RPW = G::RPW, ROWB = G::ROWB, TR = G::TR, ITER = G::ITER;
   cg::cluster_group cluster = cg::this_cluster();
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -106,11 +112,14 @@ __global__ void __launch_bounds__(kThreads, 7) decode_cluster_kernel(const CArgs
   const size_t step_elems = (size_t)c.nh * D;
 
   // dynamic shared memory: [ring or resident K|V][score][pos][logit]
+  // (+ [K scale][V scale] for an fp8 cache)
   uint8_t *kv = smem;
   const int kv_bytes = kResident ? 2 * chunk * ROWB : ring_bytes(kStages);
   float *sc = (float *)(smem + kv_bytes);
   int *ps = (int *)(sc + chunk);
   float *lg = (float *)(ps + chunk);
+  float *ksc = lg + chunk;
+  float *vsc = ksc + chunk;
 
   if (tid == 0) {
     for (int i = 0; i < kStages; ++i) {
@@ -130,6 +139,10 @@ __global__ void __launch_bounds__(kThreads, 7) decode_cluster_kernel(const CArgs
   for (int j = tid; j < own; j += kThreads) {
     sc[j] = c.score[hk + s0 + j];
     ps[j] = c.pos[hk + s0 + j];
+    if (kFp8) {
+      ksc[j] = c.Ksc[hk + s0 + j];
+      vsc[j] = c.Vsc[hk + s0 + j];
+    }
   }
   __syncthreads();
   if (kResident) {  // all owned rows, once
@@ -217,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, 7) decode_cluster_kernel(const CArgs
     } else if (!aborted) {
       // ---- consumers: logits and per-warp online softmax over the owned rows
       float qv[EPL];
-      Unpack<T>::run(*(const uint4 *)(in_q + sub * EPL), qv);
+      load_f32<T, EPL>(in_q + sub * EPL, qv);
 #pragma unroll
       for (int e = 0; e < EPL; ++e) qv[e] *= a.qscale;
       float m = -INFINITY, l = 0.f, acc[EPL];
@@ -244,12 +257,13 @@ __global__ void __launch_bounds__(kThreads, 7) decode_cluster_kernel(const CArgs
         for (int it = 0; it < ITER; ++it) {
           const int r = warp * RPW + grp + it * kConsumers * RPW;
           float kx[EPL];
-          Unpack<T>::run(*(const uint4 *)(ks + (r < rows ? r : 0) * ROWB + sub * 16), kx);
+          unpack_lane<S>(ks + (r < rows ? r : 0) * ROWB + sub * Lane<S>::VB, kx);
           float dot = 0.f;
 #pragma unroll
           for (int e = 0; e < EPL; ++e) dot = fmaf(qv[e], kx[e], dot);
 #pragma unroll
           for (int o = LPR / 2; o; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+          if (kFp8) dot *= (r < rows) ? ksc[i * TR + r] : 0.f;
           x[it] = (r < rows) ? dot : -INFINITY;
           if (r < rows && sub == 0) lg[i * TR + r] = dot;
           wmax = fmaxf(wmax, x[it]);
@@ -269,10 +283,11 @@ __global__ void __launch_bounds__(kThreads, 7) decode_cluster_kernel(const CArgs
             if (r < rows) {
               const float pr = exp2f(x[it] - m);
               l += pr;
+              const float pv = kFp8 ? pr * vsc[i * TR + r] : pr;
               float vx[EPL];
-              Unpack<T>::run(*(const uint4 *)(vs + r * ROWB + sub * 16), vx);
+              unpack_lane<S>(vs + r * ROWB + sub * Lane<S>::VB, vx);
 #pragma unroll
-              for (int e = 0; e < EPL; ++e) acc[e] = fmaf(pr, vx[e], acc[e]);
+              for (int e = 0; e < EPL; ++e) acc[e] = fmaf(pv, vx[e], acc[e]);
             }
           }
         }
@@ -288,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, 7) decode_cluster_kernel(const CArgs
       }
       if (rank == 0 && warp == 0) {  // the new token, from the step inputs
         float kx[EPL];
-        Unpack<T>::run(*(const uint4 *)(in_k + sub * EPL), kx);
+        load_f32<T, EPL>(in_k + sub * EPL, kx);
         float dot = 0.f;
 #pragma unroll
         for (int e = 0; e < EPL; ++e) dot = fmaf(qv[e], kx[e], dot);
@@ -305,7 +320,7 @@ __global__ void __launch_bounds__(kThreads, 7) decode_cluster_kernel(const CArgs
           const float pr = exp2f(dot - m);
           l += pr;
           float vx[EPL];
-          Unpack<T>::run(*(const uint4 *)(in_v + sub * EPL), vx);
+          load_f32<T, EPL>(in_v + sub * EPL, vx);
 #pragma unroll
           for (int e = 0; e < EPL; ++e) acc[e] = fmaf(pr, vx[e], acc[e]);
         }
@@ -448,7 +463,28 @@ __global__ void __launch_bounds__(kThreads, 7) decode_cluster_kernel(const CArgs
           ps[j] = p;
           sc[j] = dec_w;
         }
-        if (warp == 0 && grp == 0) {  // lanes 0..LPR-1 copy the k_t / v_t row
+        constexpr int PER = D / 32;  // fp8: lane L quantises elements L*PER ..
+        uint32_t ck = 0u, cv = 0u;
+        if (kFp8) {  // warp-uniform branch (e is the same in every lane)
+          float xk[PER], xv[PER], sk, sv;
+#pragma unroll
+          for (int q = 0; q < PER; ++q) {
+            xk[q] = to_f32<T>(in_k[lane * PER + q]);
+            xv[q] = to_f32<T>(in_v[lane * PER + q]);
+          }
+          ck = quant_row_e4m3<PER>(xk, sk);
+          cv = quant_row_e4m3<PER>(xv, sv);
+          store_codes<PER>((uint8_t *)c.K + (hk + e) * ROWB, lane, ck);
+          store_codes<PER>((uint8_t *)c.V + (hk + e) * ROWB, lane, cv);
+          if (kResident) {
+            store_codes<PER>(kv + (size_t)j * ROWB, lane, ck);
+            store_codes<PER>(kv + (size_t)chunk * ROWB + (size_t)j * ROWB, lane, cv);
+          }
+          if (tid == 0) {
+            ksc[j] = sk;
+            vsc[j] = sv;
+          }
+        } else if (grp == 0) {  // lanes 0..LPR-1 copy the k_t / v_t row
           const int i = sub;
           const uint4 kq = *(const uint4 *)(in_k + i * EPL), vq = *(const uint4 *)(in_v + i * EPL);
           ((uint4 *)((T *)c.K + (hk + e) * D))[i] = kq;
@@ -466,8 +502,11 @@ __global__ void __launch_bounds__(kThreads, 7) decode_cluster_kernel(const CArgs
           const int gpos = g + j / TR;  // ring position of that slab (g = next step's first)
           const int st = gpos % kStages;
           if (!__all_sync(0xffffffffu, mbar_wait(&s_full[st], (gpos / kStages) & 1)) && lane == 0) s_abort = 1;
-          if (grp == 0) {
-            uint8_t *slab = kv + st * 2 * kStageBytes;
+          uint8_t *slab = kv + st * 2 * kStageBytes;
+          if (kFp8) {
+            store_codes<PER>(slab + (j % TR) * ROWB, lane, ck);
+            store_codes<PER>(slab + kStageBytes + (j % TR) * ROWB, lane, cv);
+          } else if (grp == 0) {
             ((uint4 *)(slab + (j % TR) * ROWB))[sub] = *(const uint4 *)(in_k + sub * EPL);
             ((uint4 *)(slab + kStageBytes + (j % TR) * ROWB))[sub] = *(const uint4 *)(in_v + sub * EPL);
           }
@@ -482,30 +521,38 @@ __global__ void __launch_bounds__(kThreads, 7) decode_cluster_kernel(const CArgs
   for (int j = tid; j < own; j += kThreads) {
     c.score[hk + s0 + j] = sc[j];
     c.pos[hk + s0 + j] = ps[j];
+    if (kFp8) {
+      c.Ksc[hk + s0 + j] = ksc[j];
+      c.Vsc[hk + s0 + j] = vsc[j];
+    }
   }
   cluster.sync();
 }
 
-template <typename T, int D>
+// Per-slot shared-memory words beside K/V: score, tag, logit (+ two scales
+// for an fp8 cache).
+template <typename S> constexpr int slot_words() { return is_fp8<S>() ? 5 : 3; }
+
+template <typename S, int D>
 int resident_rows_ok(int chunk) {
-  return 2 * chunk * Geo<T, D>::ROWB <= kResidentMaxBytes;
+  return 2 * chunk * Geo<S, D>::ROWB <= kResidentMaxBytes;
 }
 
-template <typename T, int D, bool R, int S>
+template <typename S, int D, bool R, int St>
 int smem_bytes(int chunk) {
-  return (R ? 2 * chunk * Geo<T, D>::ROWB : ring_bytes(S)) + 3 * chunk * 4;
+  return (R ? 2 * chunk * Geo<S, D>::ROWB : ring_bytes(St)) + slot_words<S>() * chunk * 4;
 }
 
-template <typename T, int D, bool R, int S>
+template <typename T, typename S, int D, bool R, int St>
 cudaError_t launch_cluster_t(const CacheView &c, const DecodeStep &s, int nsteps, cudaStream_t st) {
   const int P = c.nsplit;
   CArgs a{c, s, nsteps, (c.k + P - 1) / P, kLog2e / sqrtf((float)D)};
-  const int smem = smem_bytes<T, D, R, S>(a.chunk);
+  const int smem = smem_bytes<S, D, R, St>(a.chunk);
   if (smem > 200 * 1024) return cudaErrorInvalidValue;
   static bool attr_done[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 || !attr_done[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(decode_cluster_kernel<T, D, R, S>,
+    cudaError_t e = cudaFuncSetAttribute(decode_cluster_kernel<T, S, D, R, St>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_done[dev] = true;
@@ -522,21 +569,21 @@ cudaError_t launch_cluster_t(const CacheView &c, const DecodeStep &s, int nsteps
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_cluster_kernel<T, D, R, S>, a);
+  return cudaLaunchKernelEx(&cfg, decode_cluster_kernel<T, S, D, R, St>, a);
 }
 
-template <typename T, int D, bool R, int S>
+template <typename T, typename S, int D, bool R, int St>
 bool all_resident(const CacheView &c, int chunk) {
   int dev = 0, sms = 0, per_sm = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return false;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
-  const int smem = smem_bytes<T, D, R, S>(chunk);
+  const int smem = smem_bytes<S, D, R, St>(chunk);
   if (smem > 200 * 1024) return false;
-  if (cudaFuncSetAttribute(decode_cluster_kernel<T, D, R, S>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(decode_cluster_kernel<T, S, D, R, St>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            200 * 1024) != cudaSuccess)
     return false;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_cluster_kernel<T, D, R, S>, kThreads, smem) !=
-      cudaSuccess)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_cluster_kernel<T, S, D, R, St>, kThreads,
+                                                    smem) != cudaSuccess)
     return false;
   return (long long)c.nh * c.nsplit <= (long long)per_sm * sms;
 }
@@ -544,81 +591,78 @@ bool all_resident(const CacheView &c, int chunk) {
 // K/V resident in shared memory when a CTA's rows fit AND every CTA of the
 // grid is resident at once (each CTA runs all steps of its head, so a second
 // wave would start only when the first finished).
-template <typename T, int D>
+template <typename T, typename S, int D>
 bool resident_t(const CacheView &c) {
   const int chunk = (c.k + c.nsplit - 1) / c.nsplit;
-  return resident_rows_ok<T, D>(chunk) && all_resident<T, D, true, 1>(c, chunk);
+  return resident_rows_ok<S, D>(chunk) && all_resident<T, S, D, true, 1>(c, chunk);
 }
 
 // Streaming: a 3-stage ring, unless two stages are what lets every CTA be
 // resident at once (a partial last wave of whole-run CTAs streams at a
 // fraction of the bandwidth).
-template <typename T, int D>
+template <typename T, typename S, int D>
 cudaError_t dispatch_t(const CacheView &c, const DecodeStep &s, int nsteps, cudaStream_t st) {
   const int chunk = (c.k + c.nsplit - 1) / c.nsplit;
-  if (resident_t<T, D>(c)) return launch_cluster_t<T, D, true, 1>(c, s, nsteps, st);
-  if (!all_resident<T, D, false, 3>(c, chunk) && all_resident<T, D, false, 2>(c, chunk))
-    return launch_cluster_t<T, D, false, 2>(c, s, nsteps, st);
-  return launch_cluster_t<T, D, false, 3>(c, s, nsteps, st);
+  if (resident_t<T, S, D>(c)) return launch_cluster_t<T, S, D, true, 1>(c, s, nsteps, st);
+  if (!all_resident<T, S, D, false, 3>(c, chunk) && all_resident<T, S, D, false, 2>(c, chunk))
+    return launch_cluster_t<T, S, D, false, 2>(c, s, nsteps, st);
+  return launch_cluster_t<T, S, D, false, 3>(c, s, nsteps, st);
 }
+
+template <typename T, typename S, int D>
+bool cluster_waves_ok_t(const CacheView &c) {
+  const int chunk = (c.k + c.nsplit - 1) / c.nsplit;
+  if (resident_t<T, S, D>(c) || all_resident<T, S, D, false, 3>(c, chunk) ||
+      all_resident<T, S, D, false, 2>(c, chunk))
+    return true;
+  int dev = 0, sms = 0, per_sm = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_cluster_kernel<T, S, D, false, 3>, kThreads,
+                                                    smem_bytes<S, D, false, 3>(chunk)) != cudaSuccess)
+    return false;
+  return (long long)c.nh * c.nsplit >= 3LL * per_sm * sms;
+}
+
+#define H2O_CLUSTER_DISPATCH(FN, ...)                                              \
+  do {                                                                            \
+    if (c.dtype == 1 && c.kv_fp8) {                                               \
+      if (c.d == 128) return FN<__nv_bfloat16, e4m3, 128>(__VA_ARGS__);           \
+      if (c.d == 64) return FN<__nv_bfloat16, e4m3, 64>(__VA_ARGS__);             \
+    } else if (c.dtype == 1) {                                                    \
+      if (c.d == 128) return FN<__nv_bfloat16, __nv_bfloat16, 128>(__VA_ARGS__);  \
+      if (c.d == 64) return FN<__nv_bfloat16, __nv_bfloat16, 64>(__VA_ARGS__);    \
+    } else if (!c.kv_fp8) {                                                       \
+      if (c.d == 128) return FN<float, float, 128>(__VA_ARGS__);                  \
+      if (c.d == 64) return FN<float, float, 64>(__VA_ARGS__);                    \
+    }                                                                             \
+  } while (0)
 
 }  // namespace
 
 bool decode_cluster_resident(const CacheView &c) {
   if (c.nsplit < 1 || c.nsplit > kMaxCluster) return false;
-  if (c.dtype == 1) {
-    if (c.d == 128) return resident_t<__nv_bfloat16, 128>(c);
-    if (c.d == 64) return resident_t<__nv_bfloat16, 64>(c);
-  } else {
-    if (c.d == 128) return resident_t<float, 128>(c);
-    if (c.d == 64) return resident_t<float, 64>(c);
-  }
+  H2O_CLUSTER_DISPATCH(resident_t, c);
   return false;
-}
-
-template <typename T, int D>
-bool cluster_waves_ok_t(const CacheView &c) {
-  const int chunk = (c.k + c.nsplit - 1) / c.nsplit;
-  if (resident_t<T, D>(c) || all_resident<T, D, false, 3>(c, chunk) || all_resident<T, D, false, 2>(c, chunk))
-    return true;
-  int dev = 0, sms = 0, per_sm = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_cluster_kernel<T, D, false, 3>, kThreads,
-                                                    smem_bytes<T, D, false, 3>(chunk)) != cudaSuccess)
-    return false;
-  return (long long)c.nh * c.nsplit >= 3LL * per_sm * sms;
 }
 
 bool decode_cluster_preferred(const CacheView &c) {
   if (c.nsplit < 1 || c.nsplit > kMaxCluster) return false;
-  if (c.dtype == 1) {
-    if (c.d == 128) return cluster_waves_ok_t<__nv_bfloat16, 128>(c);
-    if (c.d == 64) return cluster_waves_ok_t<__nv_bfloat16, 64>(c);
-  } else {
-    if (c.d == 128) return cluster_waves_ok_t<float, 128>(c);
-    if (c.d == 64) return cluster_waves_ok_t<float, 64>(c);
-  }
+  H2O_CLUSTER_DISPATCH(cluster_waves_ok_t, c);
   return false;
 }
 
 bool decode_cluster_supported(const CacheView &c) {
   if (c.nsplit < 1 || c.nsplit > kMaxCluster) return false;
   const int chunk = (c.k + c.nsplit - 1) / c.nsplit;
-  const int row = c.d * (c.dtype == 1 ? 2 : 4);
+  const int row = c.d * (c.kv_fp8 ? 1 : c.dtype == 1 ? 2 : 4);
   const int kv = (2 * chunk * row <= kResidentMaxBytes) ? 2 * chunk * row : ring_bytes(3);
-  return kv + 3 * chunk * 4 <= 200 * 1024;
+  return kv + (c.kv_fp8 ? 5 : 3) * chunk * 4 <= 200 * 1024;
 }
 
 cudaError_t launch_decode_cluster(const CacheView &c, const DecodeStep &s, int nsteps, cudaStream_t st) {
   if (!decode_cluster_supported(c) || nsteps < 1) return cudaErrorInvalidValue;
-  if (c.dtype == 1) {
-    if (c.d == 128) return dispatch_t<__nv_bfloat16, 128>(c, s, nsteps, st);
-    if (c.d == 64) return dispatch_t<__nv_bfloat16, 64>(c, s, nsteps, st);
-  } else {
-    if (c.d == 128) return dispatch_t<float, 128>(c, s, nsteps, st);
-    if (c.d == 64) return dispatch_t<float, 64>(c, s, nsteps, st);
-  }
+  H2O_CLUSTER_DISPATCH(dispatch_t, c, s, nsteps, st);
   return cudaErrorInvalidValue;
 }
 

@@ -22,10 +22,14 @@ struct CacheView {
   int nsplit;
   int n_sink = 0;      // positions 0 .. n_sink-1 are never evicted (pinned attention sinks)
   int score_mode = 0;  // 0: rank by accumulated score; 1: by score / queries that attended
+  // fp8 cache (inputs bf16): K, V hold e4m3 codes [nh][k][d] and each row has
+  // one fp32 scale, Ksc / Vsc [nh][k]; a row reads back as code * scale.
+  int kv_fp8 = 0;
+  float *Ksc = nullptr, *Vsc = nullptr;
 };
 
 struct DecodeStep {
-  const void *q, *kn, *vn;  // [nh][d]
+  const void *q, *kn, *vn;  // [nh][d] in the input type (bf16 or fp32)
   void *out;                // [nh][d]
   int32_t *evicted;         // [nh] or nullptr
   int n_valid;              // filled slots before this step

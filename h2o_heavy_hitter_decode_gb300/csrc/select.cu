@@ -15,7 +15,9 @@
 // values.  A 4-pass radix select (8-bit digits, per-warp shared histograms)
 // finds the threshold pattern and how many of the equal-to-threshold
 // positions to keep; a block-wide ballot scan then assigns slots in ascending
-// position order, and the CTA copies the kept rows with 16-byte accesses.
+// position order, and the CTA copies the kept rows with 16-byte accesses (an
+// fp8 cache quantises each kept row instead: one warp per row, one scale per
+// row).
 #include "common.cuh"
 
 namespace h2o {
@@ -24,7 +26,8 @@ namespace {
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 
-template <typename T, int D>
+// T: input type of the prompt K/V; S: type of the stored cache rows.
+template <typename T, typename S, int D>
 __global__ void __launch_bounds__(kThreads) select_gather(const CacheView c, const T *__restrict__ K,
                                                           const T *__restrict__ V,
                                                           const float *__restrict__ colsum, int L) {
@@ -142,6 +145,28 @@ __global__ void __launch_bounds__(kThreads) select_gather(const CacheView c, con
   __syncthreads();
 
   const size_t hb = (size_t)h * L * D;
+  if constexpr (is_fp8<S>()) {
+    constexpr int PER = D / 32;  // lane L quantises elements L*PER ..
+    for (int s = warp; s < k; s += kWarps) {
+      const bool live = s < n;
+      const int j = live ? posh[s] : 0;
+      float xk[PER], xv[PER], sk, sv;
+#pragma unroll
+      for (int q = 0; q < PER; ++q) {
+        xk[q] = live ? to_f32<T>(K[hb + (size_t)j * D + lane * PER + q]) : 0.f;
+        xv[q] = live ? to_f32<T>(V[hb + (size_t)j * D + lane * PER + q]) : 0.f;
+      }
+      const uint32_t ck = quant_row_e4m3<PER>(xk, sk), cv = quant_row_e4m3<PER>(xv, sv);
+      const size_t slot = (size_t)h * k + s;
+      store_codes<PER>((uint8_t *)c.K + slot * D, lane, ck);
+      store_codes<PER>((uint8_t *)c.V + slot * D, lane, cv);
+      if (lane == 0) {
+        c.Ksc[slot] = sk;
+        c.Vsc[slot] = sv;
+      }
+    }
+    return;
+  }
   uint4 *Kc = (uint4 *)((T *)c.K + (size_t)h * k * D);
   uint4 *Vc = (uint4 *)((T *)c.V + (size_t)h * k * D);
   for (int idx = tid; idx < k * CH; idx += kThreads) {
@@ -157,10 +182,10 @@ __global__ void __launch_bounds__(kThreads) select_gather(const CacheView c, con
   }
 }
 
-template <typename T, int D>
+template <typename T, typename S, int D>
 cudaError_t select_t(const CacheView &c, const void *K, const void *V, const float *colsum, int L,
                      cudaStream_t st) {
-  select_gather<T, D><<<c.nh, kThreads, 0, st>>>(c, (const T *)K, (const T *)V, colsum, L);
+  select_gather<T, S, D><<<c.nh, kThreads, 0, st>>>(c, (const T *)K, (const T *)V, colsum, L);
   return cudaGetLastError();
 }
 
@@ -168,12 +193,15 @@ cudaError_t select_t(const CacheView &c, const void *K, const void *V, const flo
 
 cudaError_t launch_prefill_select(const CacheView &c, const void *K, const void *V, const float *colsum,
                                   int L, cudaStream_t st) {
-  if (c.dtype == 1) {
-    if (c.d == 128) return select_t<__nv_bfloat16, 128>(c, K, V, colsum, L, st);
-    if (c.d == 64) return select_t<__nv_bfloat16, 64>(c, K, V, colsum, L, st);
-  } else {
-    if (c.d == 128) return select_t<float, 128>(c, K, V, colsum, L, st);
-    if (c.d == 64) return select_t<float, 64>(c, K, V, colsum, L, st);
+  if (c.dtype == 1 && c.kv_fp8) {
+    if (c.d == 128) return select_t<__nv_bfloat16, e4m3, 128>(c, K, V, colsum, L, st);
+    if (c.d == 64) return select_t<__nv_bfloat16, e4m3, 64>(c, K, V, colsum, L, st);
+  } else if (c.dtype == 1) {
+    if (c.d == 128) return select_t<__nv_bfloat16, __nv_bfloat16, 128>(c, K, V, colsum, L, st);
+    if (c.d == 64) return select_t<__nv_bfloat16, __nv_bfloat16, 64>(c, K, V, colsum, L, st);
+  } else if (!c.kv_fp8) {
+    if (c.d == 128) return select_t<float, float, 128>(c, K, V, colsum, L, st);
+    if (c.d == 64) return select_t<float, float, 64>(c, K, V, colsum, L, st);
   }
   return cudaErrorInvalidValue;
 }

@@ -19,8 +19,8 @@
  *     the cache was created on (or memory that device can address); host
  *     pointers are ordinary host memory.  The caller owns all memory: the
  *     library allocates nothing on the device.
- *   - Tensors are dense row-major in the cache's dtype (fp32, or bf16 stored as
- *     uint16 bit patterns), with the head index flattened as b*H + h:
+ *   - Tensors are dense row-major in the cache's input type (fp32, or bf16
+ *     stored as uint16 bit patterns), with the head index flattened as b*H + h:
  *     prompt tensors [B][H][L][d]; one decode step [B][H][d]; n decode steps
  *     [n][B][H][d].  Device pointers must be 16-byte aligned.
  *   - Work is enqueued asynchronously on the cache's stream (set at create or
@@ -51,7 +51,16 @@ typedef enum {
   H2O_EUNSUPPORTED = 6 /* valid request this build does not handle (e.g. d not 64/128) */
 } h2o_status;
 
-typedef enum { H2O_F32 = 0, H2O_BF16 = 1 } h2o_dtype;
+/* Element types of a cache.  H2O_F32 / H2O_BF16: inputs, outputs and the
+ * stored K/V slots all in that type.  H2O_BF16_FP8KV: bf16 inputs and
+ * outputs; the K/V slots are stored as e4m3 codes (1 byte per element) with
+ * one fp32 scale per slot row, the way the explainer page's "Limitations"
+ * section says H2O composes with quantisation.  A row x written into a slot
+ * gets scale = max|x| / 448 (fp32; 0 for an all-zero row) and codes
+ * e4m3(x / scale) (fp32 division, nearest-even, saturating at 448); it reads
+ * back as code * scale.  The prefill passes and each decode step's own new
+ * token use the bf16 inputs themselves. */
+typedef enum { H2O_F32 = 0, H2O_BF16 = 1, H2O_BF16_FP8KV = 2 } h2o_dtype;
 
 /* Bytes of device workspace a cache of this shape needs (0 if the shape is
  * invalid).  The workspace holds, per head: the K and V slots [k][d], the
@@ -145,7 +154,8 @@ h2o_status h2o_cache_set_policy(h2o_cache_t cache, int n_sink, int score_mode);
 h2o_status h2o_cache_get_policy(h2o_cache_t cache, int *n_sink, int *score_mode);
 
 /* Copy the cache state out to device buffers: pos [B][H][k] int32,
- * score [B][H][k] fp32, K, V [B][H][k][d] (any may be NULL); next_pos and
+ * score [B][H][k] fp32, K, V [B][H][k][d] in the stored type (e4m3 codes for
+ * H2O_BF16_FP8KV; see h2o_cache_export_scales) (any may be NULL); next_pos and
  * n_valid (host, may be NULL) receive the position the next decode token
  * takes and the number of filled slots.  Asynchronous like every call. */
 h2o_status h2o_cache_export(h2o_cache_t cache, int32_t *pos, float *score, void *K, void *V,
@@ -157,6 +167,14 @@ h2o_status h2o_cache_export(h2o_cache_t cache, int32_t *pos, float *score, void 
  * 0 <= n_valid <= k. */
 h2o_status h2o_cache_import(h2o_cache_t cache, const int32_t *pos, const float *score,
                             const void *K, const void *V, int64_t next_pos, int n_valid);
+
+/* Per-row scales of an H2O_BF16_FP8KV cache: device (or host) fp32
+ * [B][H][k] arrays for K and V, in the slot order of h2o_cache_export (whose
+ * K/V then hold the e4m3 codes, 1 byte per element).  Export: either pointer
+ * may be NULL.  Import (both required) after h2o_cache_import, before the
+ * next decode call.  H2O_EUNSUPPORTED for other cache types.  Asynchronous. */
+h2o_status h2o_cache_export_scales(h2o_cache_t cache, float *K_scale, float *V_scale);
+h2o_status h2o_cache_import_scales(h2o_cache_t cache, const float *K_scale, const float *V_scale);
 
 /* Shape and counters of a cache (host pointers, any may be NULL). */
 h2o_status h2o_cache_info(h2o_cache_t cache, int *B, int *H, int *d, int *k_heavy, int *k_local,

@@ -10,7 +10,9 @@ Tolerances (fixed by the method's acceptance rules):
     oracle's state through h2o_cache_import, and the run continues;
   * attention outputs: max abs error <= 1e-4 (fp32 cache) or 2e-2 (bf16);
   * scores and column sums: relative error <= 1e-3;
-  * lse: abs error <= 1e-4 (fp32 output in both cases).
+  * lse: abs error <= 1e-4 (fp32 output in both cases);
+  * fp8 caches: the stored e4m3 codes and row scales of every cached
+    position are bit-exact (integer work: the same quantisation decisions).
 """
 from __future__ import annotations
 
@@ -75,15 +77,48 @@ def _rel(a, b):
     return float(np.max(np.abs(a - b) / np.maximum(np.abs(b), 1e-30))) if a.size else 0.0
 
 
+def fp8_codes(rows: np.ndarray, scale: np.ndarray) -> np.ndarray:
+    """e4m3 code values of oracle fp8 rows (row = code * scale exactly)."""
+    sc = scale[..., None]
+    return np.where(sc > 0, rows / np.where(sc > 0, sc, 1.0), 0.0)
+
+
 def import_oracle_state(cache: H2OCache, st: oracle.State, w, next_pos: int):
     B, H, k, d = w.B, w.H, w.k, w.d
     pos = torch.from_numpy(st.pos.reshape(B, H, k).copy()).cuda()
     score = torch.from_numpy(st.score.astype(np.float32).reshape(B, H, k)).cuda()
-    K = to_dev(storage_from_f64(st.K, w), w, (B, H, k, d))
-    V = to_dev(storage_from_f64(st.V, w), w, (B, H, k, d))
     nv = int(st.n_valid[0])
     assert (st.n_valid == nv).all()
+    if cache.kv_fp8:
+        to8 = lambda x: torch.from_numpy(x.astype(np.float32)).to(torch.float8_e4m3fn).reshape(B, H, k, d).cuda()
+        K, V = to8(fp8_codes(st.K, st.Ksc)), to8(fp8_codes(st.V, st.Vsc))
+        ksc = torch.from_numpy(st.Ksc.astype(np.float32).reshape(B, H, k)).cuda()
+        vsc = torch.from_numpy(st.Vsc.astype(np.float32).reshape(B, H, k)).cuda()
+        cache.import_state(pos, score, K, V, next_pos, nv, ksc, vsc)
+        return
+    K = to_dev(storage_from_f64(st.K, w), w, (B, H, k, d))
+    V = to_dev(storage_from_f64(st.V, w), w, (B, H, k, d))
     cache.import_state(pos, score, K, V, next_pos, nv)
+
+
+def compare_fp8_rows(ex, o_st: oracle.State, heads, nh, k, d):
+    """Stored codes and scales of every cached position, GPU vs oracle,
+    bit-exact (slots matched by position)."""
+    g_pos = ex["pos"].cpu().numpy().reshape(nh, k)
+    gK = ex["K"].float().cpu().numpy().reshape(nh, k, d)
+    gV = ex["V"].float().cpu().numpy().reshape(nh, k, d)
+    gks = ex["K_scale"].cpu().numpy().reshape(nh, k)
+    gvs = ex["V_scale"].cpu().numpy().reshape(nh, k)
+    oK, oV = fp8_codes(o_st.K, o_st.Ksc), fp8_codes(o_st.V, o_st.Vsc)
+    for i, h in enumerate(heads):
+        gslot = {int(p): s for s, p in enumerate(g_pos[h]) if p >= 0}
+        for s, p in enumerate(o_st.pos[i]):
+            if p < 0:
+                continue
+            g = gslot[int(p)]
+            assert gks[h, g] == np.float32(o_st.Ksc[i, s]) and gvs[h, g] == np.float32(o_st.Vsc[i, s]), (h, p)
+            np.testing.assert_array_equal(gK[h, g], oK[i, s], err_msg=f"K codes head {h} pos {p}")
+            np.testing.assert_array_equal(gV[h, g], oV[i, s], err_msg=f"V codes head {h} pos {p}")
 
 
 def compare_scores(rep: Report, g_pos, g_score, o_st: oracle.State, heads):
@@ -98,10 +133,11 @@ def compare_scores(rep: Report, g_pos, g_score, o_st: oracle.State, heads):
 
 
 def run_parity(w, T=None, heads=None, resync=True, check=True, prompt=None, dec=None, want_O=True,
-               decode_form="auto", policy=(0, 0)):
+               decode_form="auto", policy=(0, 0), kv_fp8=False):
     """Prefill + T decode steps on the GPU through the C ABI, against the
     oracle on `heads` (all heads when None; resynchronisation needs all).
-    `policy` = (n_sink, score_mode) of both sides."""
+    `policy` = (n_sink, score_mode) of both sides; `kv_fp8` stores the cache
+    rows as e4m3 with row scales on both sides."""
     T = w.T if T is None else T
     nh = w.nh
     hs = list(range(nh)) if heads is None else list(heads)
@@ -110,10 +146,10 @@ def run_parity(w, T=None, heads=None, resync=True, check=True, prompt=None, dec=
     rep = Report(heads_compared=len(hs))
     Qs, Ks, Vs = prompt if prompt is not None else synth.prompt(w)
 
-    cache = H2OCache(w.B, w.H, w.d, w.k_heavy, w.k_local, tdtype(w))
+    cache = H2OCache(w.B, w.H, w.d, w.k_heavy, w.k_local, tdtype(w), kv_fp8=kv_fp8)
     cache.set_decode_form(decode_form)
-    pol = dict(n_sink=policy[0], score_mode=policy[1])
-    cache.set_policy(**pol)
+    pol = dict(n_sink=policy[0], score_mode=policy[1], kv_fp8=kv_fp8)
+    cache.set_policy(policy[0], policy[1])
     shp = (w.B, w.H, w.L, w.d)
     O, lse, colsum = cache.prefill(to_dev(Qs, w, shp), to_dev(Ks, w, shp), to_dev(Vs, w, shp), want_O=want_O)
     torch.cuda.synchronize()
@@ -145,6 +181,8 @@ def run_parity(w, T=None, heads=None, resync=True, check=True, prompt=None, dec=
             rep.resyncs += 1
     else:
         compare_scores(rep, g_pos, ex["score"].cpu().numpy().reshape(nh, w.k), st0, hs)
+        if kv_fp8 and check:
+            compare_fp8_rows(ex, st0, hs, nh, w.k, w.d)
     if T == 0:
         return rep, cache
 
@@ -226,6 +264,9 @@ def run_parity(w, T=None, heads=None, resync=True, check=True, prompt=None, dec=
         sub = oracle.State(len(sel), w.k, w.d)
         sub.pos, sub.score = o_st.pos[sel], o_st.score[sel]
         compare_scores(rep, g_pos, g_sc, sub, [hs[i] for i in sel])
+        if kv_fp8 and check:
+            sub.K, sub.V, sub.Ksc, sub.Vsc = o_st.K[sel], o_st.V[sel], o_st.Ksc[sel], o_st.Vsc[sel]
+            compare_fp8_rows(ex, sub, [hs[i] for i in sel], nh, w.k, w.d)
     if check:
         assert rep.max_score_rel <= SCORE_RTOL, rep
         cache.check_device_error()

@@ -73,6 +73,8 @@ def test_null_handle_rejected(L):
     assert L.h2o_set_stream(None, None) == 1
     assert L.h2o_cache_set_policy(None, 0, 0) == 1
     assert L.h2o_cache_get_policy(None, None, None) == 1
+    assert L.h2o_cache_export_scales(None, None, None) == 1
+    assert L.h2o_cache_import_scales(None, None, None) == 1
     assert L.h2o_cache_destroy(None) == 0
 
 

@@ -115,6 +115,31 @@ template <typename T, int N> __device__ __forceinline__ void load_f32_nc(const T
   for (int i = 0; i < N / V; ++i) Unpack<T>::run(ld_nc16(p + i * V), x + i * V);
 }
 
+// Two products of packed 16-bit pairs accumulated in fp32 with the
+// mixed-precision FMA (fp32 accumulator, f16 / bf16 multiplicands): element 0
+// of each operand is its low half.  Products of two bf16 (or two f16) values
+// are exact in fp32, so this is an fp32 dot product without unpacking.
+__device__ __forceinline__ float fma2_bf16(uint32_t a, uint32_t b, float c) {
+  asm("{\n\t.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
+      "fma.rn.f32.bf16 %0, al, bl, %0;\n\tfma.rn.f32.bf16 %0, ah, bh, %0;\n\t}"
+      : "+f"(c)
+      : "r"(a), "r"(b));
+  return c;
+}
+__device__ __forceinline__ float fma2_f16(uint32_t a, uint32_t b, float c) {
+  asm("{\n\t.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
+      "fma.rn.f32.f16 %0, al, bl, %0;\n\tfma.rn.f32.f16 %0, ah, bh, %0;\n\t}"
+      : "+f"(c)
+      : "r"(a), "r"(b));
+  return c;
+}
+// Two e4m3 codes (low byte = element 0) as an f16x2 word (element 0 in the
+// low half); exact.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two & 0xffffu), __NV_E4M3);
+  return (uint32_t)h.x | ((uint32_t)h.y << 16);
+}
+
 template <typename T> __device__ __forceinline__ T from_f32(float x);
 template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
 template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
@@ -135,6 +160,110 @@ __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   return v;
+}
+
+// One lane's share of q for the K dot products of a stored row type S, kept
+// packed: bf16 rows take the raw bf16 q (mixed bf16 FMA), fp8 rows take q in
+// f16 (mixed f16 FMA after the e4m3 -> f16 conversion), fp32 rows keep
+// prescaled fp32 q.  `scale` is the factor that turns the accumulated dot
+// into the log2-domain logit (times the row's K scale for fp8).
+template <typename S, int EPL> struct QLane {
+  float v[EPL];
+  float scale;
+  template <typename T> __device__ __forceinline__ void load(const T *q, float qscale) {
+    load_f32<T, EPL>(q, v);
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) v[e] *= qscale;
+    scale = 1.f;
+  }
+  __device__ __forceinline__ float dot(const uint8_t *row) const {
+    float x[EPL];
+    unpack_lane<S>(row, x);
+    float d = 0.f;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) d = fmaf(v[e], x[e], d);
+    return d;
+  }
+};
+template <int EPL> struct QLane<__nv_bfloat16, EPL> {
+  uint32_t w[EPL / 2];
+  float scale;
+  template <typename T> __device__ __forceinline__ void load(const T *q, float qscale) {
+    static_assert(std::is_same<T, __nv_bfloat16>::value, "bf16 rows take bf16 queries");
+#pragma unroll
+    for (int i = 0; i < EPL / 8; ++i) {
+      const uint4 u = *(const uint4 *)(q + 8 * i);
+      w[4 * i] = u.x; w[4 * i + 1] = u.y; w[4 * i + 2] = u.z; w[4 * i + 3] = u.w;
+    }
+    scale = qscale;
+  }
+  __device__ __forceinline__ float dot(const uint8_t *row) const {
+    const uint4 k = *(const uint4 *)row;
+    float d = 0.f;
+    d = fma2_bf16(w[0], k.x, d);
+    d = fma2_bf16(w[1], k.y, d);
+    d = fma2_bf16(w[2], k.z, d);
+    d = fma2_bf16(w[3], k.w, d);
+    return d;
+  }
+};
+template <int EPL> struct QLane<e4m3, EPL> {
+  static_assert(EPL == 8, "an fp8 lane reads 8 codes");
+  uint32_t w[4];
+  float scale;
+  // q in f16: scaled by a power of two when max|q| would leave f16's range
+  // (undone in `scale`); warp-collective (every lane of the warp calls it).
+  template <typename T> __device__ __forceinline__ void load(const T *q, float qscale) {
+    float v[8];
+    load_f32<T, 8>(q, v);
+    float qmax = 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) qmax = fmaxf(qmax, fabsf(v[e]));
+    qmax = warp_max(qmax);
+    int ex = 0;
+    frexpf(qmax, &ex);  // qmax < 2^ex
+    const int sh = ex > 14 ? 14 - ex : 0;  // keep |q| below 2^14
+    const float qs = ldexpf(1.f, sh);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __half2 h = __floats2half2_rn(v[2 * i] * qs, v[2 * i + 1] * qs);
+      w[i] = *(const uint32_t *)&h;
+    }
+    scale = qscale * ldexpf(1.f, -sh);
+  }
+  __device__ __forceinline__ float dot(const uint8_t *row) const {
+    const uint2 k = *(const uint2 *)row;
+    float d = 0.f;
+    d = fma2_f16(w[0], e4m3x2_to_f16x2(k.x), d);
+    d = fma2_f16(w[1], e4m3x2_to_f16x2(k.x >> 16), d);
+    d = fma2_f16(w[2], e4m3x2_to_f16x2(k.y), d);
+    d = fma2_f16(w[3], e4m3x2_to_f16x2(k.y >> 16), d);
+    return d;
+  }
+};
+
+// Transposed butterfly reduction: each of the LPR lanes of a group holds
+// partial sums of the same ITER rows; afterwards lane `sub` of the group holds
+// the full sum of row sub / (LPR / ITER).  At each of the first log2(ITER)
+// levels a lane keeps half of its rows and sends the other half to its
+// partner, so the group spends (ITER - 1) + log2(LPR / ITER) shuffles instead
+// of ITER * log2(LPR).
+template <int ITER, int LPR>
+__device__ __forceinline__ float xreduce(float (&x)[ITER], int sub) {
+  static_assert(ITER >= 1 && ITER <= LPR && (ITER & (ITER - 1)) == 0, "ITER a power of two <= LPR");
+#pragma unroll
+  for (int n = ITER, o = LPR / 2; n > 1; n >>= 1, o >>= 1) {
+    const bool up = (sub & o) != 0;
+#pragma unroll
+    for (int j = 0; j < n / 2; ++j) {
+      const float send = up ? x[j] : x[j + n / 2];
+      const float keep = up ? x[j + n / 2] : x[j];
+      x[j] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+    }
+  }
+#pragma unroll
+  for (int o = LPR / (2 * ITER); o >= 1; o >>= 1) x[0] += __shfl_xor_sync(0xffffffffu, x[0], o);
+  return x[0];
 }
 
 // Warp-collective quantisation of one row of 32 * PER values into an fp8

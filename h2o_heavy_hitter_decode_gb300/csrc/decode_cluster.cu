@@ -228,15 +228,18 @@ __global__ void __launch_bounds__(kThreads, 7) decode_cluster_kernel(const CArgs
       }
       g += nst;
     } else if (!aborted) {
-      // ---- consumers: logits and per-warp online softmax over the owned rows
-      float qv[EPL];
-      load_f32<T, EPL>(in_q + sub * EPL, qv);
-#pragma unroll
-      for (int e = 0; e < EPL; ++e) qv[e] *= a.qscale;
+      // ---- consumers: logits and per-warp online softmax over the owned rows.
+      // A lane group (LPR lanes) takes ITER rows per slab: K dot products
+      // from packed q, one transposed reduction, one exp2 per lane for the
+      // row it ends up holding, broadcast back for the V rows.
+      QLane<S, EPL> qk;
+      qk.load(in_q + sub * EPL, a.qscale);
+      constexpr int LPI = LPR / ITER;  // lanes holding one reduced row
       float m = -INFINITY, l = 0.f, acc[EPL];
 #pragma unroll
       for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
       const int nslab = kResident ? (nrows + TR - 1) / TR : nst;
+      const int myit = sub / LPI;  // the row this lane holds after the reduction
       bool ok = true;
       for (int i = 0; i < nslab; ++i) {
         const uint8_t *ks, *vs;
@@ -252,43 +255,39 @@ __global__ void __launch_bounds__(kThreads, 7) decode_cluster_kernel(const CArgs
         }
         const int rows = min(TR, nrows - i * TR);
         float x[ITER];
-        float wmax = -INFINITY;
 #pragma unroll
         for (int it = 0; it < ITER; ++it) {
           const int r = warp * RPW + grp + it * kConsumers * RPW;
-          float kx[EPL];
-          unpack_lane<S>(ks + (r < rows ? r : 0) * ROWB + sub * Lane<S>::VB, kx);
-          float dot = 0.f;
-#pragma unroll
-          for (int e = 0; e < EPL; ++e) dot = fmaf(qv[e], kx[e], dot);
-#pragma unroll
-          for (int o = LPR / 2; o; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
-          if (kFp8) dot *= (r < rows) ? ksc[i * TR + r] : 0.f;
-          x[it] = (r < rows) ? dot : -INFINITY;
-          if (r < rows && sub == 0) lg[i * TR + r] = dot;
-          wmax = fmaxf(wmax, x[it]);
+          x[it] = qk.dot(ks + (r < rows ? r : 0) * ROWB + sub * Lane<S>::VB);
         }
+        const int rm = warp * RPW + grp + myit * kConsumers * RPW;
+        const bool valid = rm < rows;
+        float lgt = xreduce<ITER, LPR>(x, sub) * qk.scale;
+        if (kFp8) lgt *= valid ? ksc[i * TR + rm] : 0.f;
+        lgt = valid ? lgt : -INFINITY;
+        if (valid && sub % LPI == 0) lg[i * TR + rm] = lgt;
+        float wmax = lgt;  // over the warp's rows of this slab
 #pragma unroll
-        for (int o = LPR; o < 32; o <<= 1) wmax = fmaxf(wmax, __shfl_xor_sync(0xffffffffu, wmax, o));
-        if (wmax != -INFINITY) {
-          const float mn = fmaxf(m, wmax);
-          const float sc_ = exp2f(m - mn);
+        for (int o = LPI; o < 32; o <<= 1) wmax = fmaxf(wmax, __shfl_xor_sync(0xffffffffu, wmax, o));
+        if (wmax > m) {  // warp-uniform: rescale only when the running max grows
+          const float sc_ = ex2(m - wmax);
           l *= sc_;
 #pragma unroll
           for (int e = 0; e < EPL; ++e) acc[e] *= sc_;
-          m = mn;
+          m = wmax;
+        }
+        const float prm = valid ? ex2(lgt - m) : 0.f;
 #pragma unroll
-          for (int it = 0; it < ITER; ++it) {
-            const int r = warp * RPW + grp + it * kConsumers * RPW;
-            if (r < rows) {
-              const float pr = exp2f(x[it] - m);
-              l += pr;
-              const float pv = kFp8 ? pr * vsc[i * TR + r] : pr;
-              float vx[EPL];
-              unpack_lane<S>(vs + r * ROWB + sub * Lane<S>::VB, vx);
+        for (int it = 0; it < ITER; ++it) {
+          const int r = warp * RPW + grp + it * kConsumers * RPW;
+          const float pr = __shfl_sync(0xffffffffu, prm, grp * LPR + it * LPI);
+          if (r < rows) {
+            l += pr;
+            const float pv = kFp8 ? pr * vsc[i * TR + r] : pr;
+            float vx[EPL];
+            unpack_lane<S>(vs + r * ROWB + sub * Lane<S>::VB, vx);
 #pragma unroll
-              for (int e = 0; e < EPL; ++e) acc[e] = fmaf(pv, vx[e], acc[e]);
-            }
+            for (int e = 0; e < EPL; ++e) acc[e] = fmaf(pv, vx[e], acc[e]);
           }
         }
         if (!kResident) {
@@ -302,22 +301,24 @@ __global__ void __launch_bounds__(kThreads, 7) decode_cluster_kernel(const CArgs
         atomicOr(c.err, 1);
       }
       if (rank == 0 && warp == 0) {  // the new token, from the step inputs
-        float kx[EPL];
+        float qv[EPL], kx[EPL];
+        load_f32<T, EPL>(in_q + sub * EPL, qv);
         load_f32<T, EPL>(in_k + sub * EPL, kx);
         float dot = 0.f;
 #pragma unroll
         for (int e = 0; e < EPL; ++e) dot = fmaf(qv[e], kx[e], dot);
 #pragma unroll
         for (int o = LPR / 2; o; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+        dot *= a.qscale;
         if (lane == 0) s_lgnew = dot;
         const float mn = fmaxf(m, dot);
-        const float sc_ = exp2f(m - mn);
+        const float sc_ = ex2(m - mn);
         l *= sc_;
 #pragma unroll
         for (int e = 0; e < EPL; ++e) acc[e] *= sc_;
         m = mn;
         if (grp == 0) {
-          const float pr = exp2f(dot - m);
+          const float pr = ex2(dot - m);
           l += pr;
           float vx[EPL];
           load_f32<T, EPL>(in_v + sub * EPL, vx);

@@ -194,10 +194,14 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const Args a) {
     }
 
     // -------------------------------------------------------------- consumers
-    float qv[EPL];
-    load_f32_nc<T, EPL>((const T *)a.s.q + step * step_elems + (size_t)h * D + sub * EPL, qv);
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) qv[e] *= a.qscale;
+    // A lane group (LPR lanes) takes ITER rows per slab: K dot products from
+    // packed q, one transposed reduction, one exp2 per lane for the row it
+    // ends up holding, broadcast back for the V rows.
+    const T *qrow = (const T *)a.s.q + step * step_elems + (size_t)h * D + sub * EPL;
+    QLane<S, EPL> qk;
+    qk.load(qrow, a.qscale);
+    constexpr int LPI = LPR / ITER;  // lanes holding one reduced row
+    const int myit = sub / LPI;
     float m = -INFINITY, l = 0.f, acc[EPL];
 #pragma unroll
     for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
@@ -205,57 +209,52 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const Args a) {
     for (int i = 0; ok && i < nst; ++i, ++g) {
       const int st = g % kStages;
       const int rows = min(TR, nrows - i * TR);
-      float ksc[ITER], vsc[ITER];  // row scales of an fp8 cache (read before the slab wait)
+      const int rm = warp * RPW + grp + myit * kConsumers * RPW;
+      const bool valid = rm < rows;
+      float kscm = 1.f, vsc[ITER];  // row scales of an fp8 cache (read before the slab wait)
       if (kFp8) {
+        kscm = valid ? __ldcg(c.Ksc + hk + r0 + (size_t)i * TR + rm) : 0.f;
 #pragma unroll
         for (int it = 0; it < ITER; ++it) {
           const int r = warp * RPW + grp + it * kConsumers * RPW;
-          const size_t slot = hk + r0 + (size_t)i * TR + r;
-          ksc[it] = (r < rows) ? __ldcg(c.Ksc + slot) : 0.f;
-          vsc[it] = (r < rows) ? __ldcg(c.Vsc + slot) : 0.f;
+          vsc[it] = (r < rows) ? __ldcg(c.Vsc + hk + r0 + (size_t)i * TR + r) : 0.f;
         }
       }
       if (!(ok = __all_sync(0xffffffffu, mbar_wait(&s_full[st], (g / kStages) & 1)))) break;
       const uint8_t *ks = s_ring + st * 2 * kStageBytes;
       const uint8_t *vs = ks + kStageBytes;
       float x[ITER];
-      float wmax = -INFINITY;
 #pragma unroll
       for (int it = 0; it < ITER; ++it) {
         const int r = warp * RPW + grp + it * kConsumers * RPW;
-        float kx[EPL];
-        unpack_lane<S>(ks + r * ROWB + sub * Lane<S>::VB, kx);
-        float dot = 0.f;
-#pragma unroll
-        for (int e = 0; e < EPL; ++e) dot = fmaf(qv[e], kx[e], dot);
-#pragma unroll
-        for (int o = LPR / 2; o; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
-        if (kFp8) dot *= ksc[it];
-        x[it] = (r < rows) ? dot : -INFINITY;
-        if (r < rows && sub == 0) lg[r0 + i * TR + r] = dot;
-        wmax = fmaxf(wmax, x[it]);
+        x[it] = qk.dot(ks + (r < rows ? r : 0) * ROWB + sub * Lane<S>::VB);
       }
+      float lgt = xreduce<ITER, LPR>(x, sub) * qk.scale;
+      if (kFp8) lgt *= kscm;
+      lgt = valid ? lgt : -INFINITY;
+      if (valid && sub % LPI == 0) lg[r0 + i * TR + rm] = lgt;
+      float wmax = lgt;  // over the warp's rows of this slab
 #pragma unroll
-      for (int o = LPR; o < 32; o <<= 1) wmax = fmaxf(wmax, __shfl_xor_sync(0xffffffffu, wmax, o));
-      if (wmax != -INFINITY) {
-        const float mn = fmaxf(m, wmax);
-        const float sc = exp2f(m - mn);
+      for (int o = LPI; o < 32; o <<= 1) wmax = fmaxf(wmax, __shfl_xor_sync(0xffffffffu, wmax, o));
+      if (wmax > m) {  // warp-uniform: rescale only when the running max grows
+        const float sc = ex2(m - wmax);
         l *= sc;
 #pragma unroll
         for (int e = 0; e < EPL; ++e) acc[e] *= sc;
-        m = mn;
+        m = wmax;
+      }
+      const float prm = valid ? ex2(lgt - m) : 0.f;
 #pragma unroll
-        for (int it = 0; it < ITER; ++it) {
-          const int r = warp * RPW + grp + it * kConsumers * RPW;
-          if (r < rows) {
-            const float pr = exp2f(x[it] - m);
-            l += pr;
-            const float pv = kFp8 ? pr * vsc[it] : pr;
-            float vx[EPL];
-            unpack_lane<S>(vs + r * ROWB + sub * Lane<S>::VB, vx);
+      for (int it = 0; it < ITER; ++it) {
+        const int r = warp * RPW + grp + it * kConsumers * RPW;
+        const float pr = __shfl_sync(0xffffffffu, prm, grp * LPR + it * LPI);
+        if (r < rows) {
+          l += pr;
+          const float pv = kFp8 ? pr * vsc[it] : pr;
+          float vx[EPL];
+          unpack_lane<S>(vs + r * ROWB + sub * Lane<S>::VB, vx);
 #pragma unroll
-            for (int e = 0; e < EPL; ++e) acc[e] = fmaf(pv, vx[e], acc[e]);
-          }
+          for (int e = 0; e < EPL; ++e) acc[e] = fmaf(pv, vx[e], acc[e]);
         }
       }
       __syncwarp();
@@ -270,22 +269,24 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const Args a) {
     consumers_sync();
     if (*(volatile int *)&s_abort) break;
     if (has_new && warp == 0) {  // the new token, straight from the step inputs
-      float kx[EPL];
+      float qv[EPL], kx[EPL];
+      load_f32_nc<T, EPL>(qrow, qv);
       load_f32_nc<T, EPL>(kn + sub * EPL, kx);
       float dot = 0.f;
 #pragma unroll
       for (int e = 0; e < EPL; ++e) dot = fmaf(qv[e], kx[e], dot);
 #pragma unroll
       for (int o = LPR / 2; o; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+      dot *= a.qscale;
       if (lane == 0) lg[n] = dot;
       const float mn = fmaxf(m, dot);
-      const float sc = exp2f(m - mn);
+      const float sc = ex2(m - mn);
       l *= sc;
 #pragma unroll
       for (int e = 0; e < EPL; ++e) acc[e] *= sc;
       m = mn;
       if (grp == 0) {
-        const float pr = exp2f(dot - m);
+        const float pr = ex2(dot - m);
         l += pr;
         float vx[EPL];
         load_f32_nc<T, EPL>(vn + sub * EPL, vx);

@@ -89,11 +89,11 @@ __global__ void __launch_bounds__(kThreads, 7) decode_cluster_kernel(const CArgs
   // Exchange buffers, filled by the peers' DSMEM stores (pushes) before a
   // cluster barrier and read locally after it.
   // Each completes one phase per step when its bytes have arrived.
-  __shared__ __align__(8) uint64_t s_bml, s_bacc, s_bcand, s_bdec;
-  __shared__ __align__(16) uint64_t s_mlx[kMaxCluster];    // every rank's (m, l), in every CTA
+  __shared__ __align__(8) uint64_t s_bml, s_bacc, s_bcand;
+  // every rank's (m, l) (and rank 0's new-token logit), in every CTA
+  __shared__ __align__(16) uint4 s_mlx[kMaxCluster];
   __shared__ __align__(16) float s_accx[kMaxCluster][D];   // every rank's acc row (rank 0)
-  __shared__ __align__(16) uint4 s_candx[kMaxCluster];     // every rank's candidate (rank 0)
-  __shared__ __align__(16) uint64_t s_dec;                 // rank 0's decision (slot, weight), in every CTA
+  __shared__ __align__(16) uint4 s_candx[kMaxCluster];     // every rank's candidate, in every CTA
   __shared__ float s_ML[2], s_lgnew, s_f[kMaxCluster];
   __shared__ ArgMin s_am[kConsumers];
   __shared__ int s_abort;
@@ -131,7 +131,6 @@ __global__ void __launch_bounds__(kThreads, 7) decode_cluster_kernel(const CArgs
     mbar_init(&s_bml, 1);
     mbar_init(&s_bacc, 1);
     mbar_init(&s_bcand, 1);
-    mbar_init(&s_bdec, 1);
     s_abort = 0;
     s_spec = 0;
     fence_mbar_init();
@@ -176,12 +175,9 @@ __global__ void __launch_bounds__(kThreads, 7) decode_cluster_kernel(const CArgs
   for (int step = 0; step < a.nsteps; ++step) {
     if (*(volatile int *)&s_abort) break;  // uniform: read after the previous step's CTA barrier
     if (tid == 0) {  // bytes this CTA receives during the step
-      mbar_expect_tx(&s_bml, P * 8);
-      mbar_expect_tx(&s_bdec, 8);
-      if (rank == 0) {
-        mbar_expect_tx(&s_bacc, P * D * 4);
-        mbar_expect_tx(&s_bcand, P * 16);
-      }
+      mbar_expect_tx(&s_bml, P * 16);
+      mbar_expect_tx(&s_bcand, P * 16);
+      if (rank == 0) mbar_expect_tx(&s_bacc, P * D * 4);
     }
     // inputs of this step (buffer step&1) and, ahead, of the next one
     if (tid == kConsumerThreads && step + 1 < a.nsteps) fetch_inputs(step + 1);
@@ -358,8 +354,8 @@ __global__ void __launch_bounds__(kThreads, 7) decode_cluster_kernel(const CArgs
         float ls = 0.f;
 #pragma unroll
         for (int w = 0; w < kConsumers; ++w) ls = fmaf(f[w], s_wl[w], ls);
-        const uint64_t v = (uint64_t)__float_as_uint(M) | ((uint64_t)__float_as_uint(ls) << 32);
-        st_async_b64(mapa(&s_mlx[rank], tid), v, mapa(&s_bml, tid));
+        const uint4 v = make_uint4(__float_as_uint(M), __float_as_uint(ls), __float_as_uint(s_lgnew), 0u);
+        st_async_v4(mapa(&s_mlx[rank], tid), v, mapa(&s_bml, tid));
       }
     }
 
@@ -371,8 +367,8 @@ __global__ void __launch_bounds__(kThreads, 7) decode_cluster_kernel(const CArgs
       if (!__all_sync(0xffffffffu, got) && lane == 0) s_abort = 1;
       float mr = -INFINITY, lr = 0.f;
       if (lane < P) {
-        mr = __uint_as_float((uint32_t)s_mlx[lane]);
-        lr = __uint_as_float((uint32_t)(s_mlx[lane] >> 32));
+        mr = __uint_as_float(s_mlx[lane].x);
+        lr = __uint_as_float(s_mlx[lane].y);
       }
       const float Mg = warp_max(mr);
       const float fr = (mr == -INFINITY) ? 0.f : exp2f(mr - Mg);
@@ -410,7 +406,9 @@ __global__ void __launch_bounds__(kThreads, 7) decode_cluster_kernel(const CArgs
         }
       }
     }
-    const float w_new = (rank == 0) ? exp2f(s_lgnew - Mg) * invL : 0.f;
+    // the new token's weight, from rank 0's logit (every CTA: the owner of
+    // the slot it takes writes it as that slot's score)
+    const float w_new = exp2f(__uint_as_float(s_mlx[0].z) - Mg) * invL;
     if (rank == 0 && tid == 0 && c.kl == 0 && p >= c.n_sink) {
       const ArgMin cand{w_new, p, -1};  // attended by one query: its mean is its weight
       if (am_less(cand, best)) best = cand;
@@ -424,11 +422,13 @@ __global__ void __launch_bounds__(kThreads, 7) decode_cluster_kernel(const CArgs
       ArgMin b = s_am[0];
       for (int w = 1; w < kConsumers; ++w)
         if (am_less(s_am[w], b)) b = s_am[w];
-      st_async_v4(mapa(&s_candx[rank], 0), make_uint4(__float_as_uint(b.s), (uint32_t)b.p, (uint32_t)b.slot, 0u),
-                  mapa(&s_bcand, 0));  // to rank 0
+      const uint4 v = make_uint4(__float_as_uint(b.s), (uint32_t)b.p, (uint32_t)b.slot, 0u);
+      for (int r = 0; r < P; ++r) st_async_v4(mapa(&s_candx[rank], r), v, mapa(&s_bcand, r));  // to every rank
     }
 
-    if (rank == 0 && warp == 0) {  // lane r holds rank r's candidate
+    // ---- the decision, taken identically by warp 0 of every CTA (lane r
+    // holds rank r's candidate), then the owner's update
+    if (warp == 0) {
       if (!__all_sync(0xffffffffu, mbar_wait(&s_bcand, step & 1)) && lane == 0) s_abort = 1;
       ArgMin b{INFINITY, INT_MAX, -2};
       if (lane < P) {
@@ -440,24 +440,16 @@ __global__ void __launch_bounds__(kThreads, 7) decode_cluster_kernel(const CArgs
       if (n < c.k) {
         e = n;  // |S| < k: admit into the next free slot
       } else if (b.slot == -2) {
-        if (lane == 0) atomicOr(c.err, 1);  // no eviction candidate: inconsistent state
+        if (lane == 0 && rank == 0) atomicOr(c.err, 1);  // no eviction candidate: inconsistent state
       } else if (b.slot == -1) {
         ev = p;  // the new token itself scores lowest (k_local = 0)
       } else {
         e = b.slot;
         ev = b.p;
       }
-      if (lane == 0 && a.s.evicted) a.s.evicted[(size_t)step * c.nh + h] = ev;
-      if (lane < P) {  // decision to every rank
-        const uint64_t v = (uint64_t)(uint32_t)e | ((uint64_t)__float_as_uint(w_new) << 32);
-        st_async_b64(mapa(&s_dec, lane), v, mapa(&s_bdec, lane));
-      }
-    }
-
-    if (warp == 0) {  // the owner's update: warp 0 only
-      if (!__all_sync(0xffffffffu, mbar_wait(&s_bdec, step & 1)) && lane == 0) s_abort = 1;
-      const int e = (int)(uint32_t)s_dec;
-      const float dec_w = __uint_as_float((uint32_t)(s_dec >> 32));
+      if (lane == 0 && rank == 0 && a.s.evicted) a.s.evicted[(size_t)step * c.nh + h] = ev;
+      e = __shfl_sync(0xffffffffu, e, 0);
+      const float dec_w = w_new;
       if (e >= s0 && e < s0 + own) {  // this CTA owns the slot that takes the new token
         const int j = e - s0;
         if (tid == 0) {

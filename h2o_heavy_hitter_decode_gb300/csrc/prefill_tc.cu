@@ -5,15 +5,18 @@
 // accumulated attention score of key j is its causal column sum
 //   colsum_j = sum_{i >= j} exp(q_i.k_j / sqrt(d) - LSE_i).
 //
-// Column-sum pass (the score pass).  One CTA owns a tile of 128 keys, which is
+// Column-sum pass (the score pass).  A CTA owns a tile of 128 keys, which is
 // the MMA's A operand (M = 128 TMEM lanes, one key per thread) and stays in
 // shared memory; query tiles of 128 stream in through a two-stage TMA ring as
 // the B operand (N = 128).  S^T = K Q^T lands in one of two TMEM accumulator
-// buffers, so the MMA of query tile j+1 runs while the four warps turn tile j
-// into exp2(s * log2(e)/sqrt(d) - LSE_i * log2(e)) and add it along their TMEM
-// row: every key's sum stays in one thread, deterministic and atomic-free.
-// Only the first query tile touches the diagonal and needs the causal mask;
-// query rows past L are zero-filled by TMA and masked by LSE = +inf.
+// buffers, so the MMA of query tile j+1 runs while the epilogue warps turn
+// tile j into exp2(s * log2(e)/sqrt(d) - LSE_i * log2(e)) and add it along
+// their TMEM row: every key's sum stays in one thread, deterministic and
+// atomic-free.  Only the first query tile of a key tile touches the diagonal
+// and needs the causal mask; query rows past L are zero-filled by TMA and
+// masked by LSE = +inf.  Each CTA runs two key tiles back to back (tile p,
+// then tile nkt-1-p, reloading the resident tile in between), so every CTA
+// streams nkt + 1 query tiles whatever its place in the causal triangle.
 //
 // LSE pass.  The same pipeline with the roles swapped: a CTA owns 128 queries
 // (A operand, TMEM lanes) and streams the key tiles 0..diagonal; each thread
@@ -48,7 +51,8 @@ template <int D> struct TileGeo {
 };
 
 struct __align__(8) SmallState {
-  uint64_t res_bar;
+  uint64_t res_bar;           // resident tile landed (one phase per segment)
+  uint64_t a_free;            // the MMAs of the first segment are done with the resident tile
   uint64_t ld_bar[kStages];   // streamed tile landed
   uint64_t ld_free[kStages];  // the MMA that read the stage is done
   uint64_t mma_full[2];       // accumulator (and its column vector) ready
@@ -93,23 +97,35 @@ __device__ __forceinline__ void load_tile(uint8_t *dst, const CUtensorMap *map, 
   for (int b = 0; b < TileGeo<D>::kBoxes; ++b) tma_load_3d(dst + b * kBox, map, bar, b * 64, row, h);
 }
 
-// Shared skeleton, warp-specialised.  The resident tile (A) comes from row r0
-// of `mapA`; streamed tiles j = 0..n-1 of `mapB` from rows s0 + 128 j.  Warp 8
-// (the producer) issues the TMA loads and the MMAs into two TMEM accumulators
-// and, per tile, fills that tile's column vector with `prep(j, lane)` before
-// marking the accumulator full; warps 0-7 wait for it, call `epi(j, taddr)`
-// with the TMEM address of their 32 lanes and 64-column half, and release
-// the accumulator.  No CTA-wide barrier inside the loop.
+// One run of the pipeline: resident tile from row r0 of the A map, streamed
+// tiles j = 0..n-1 from rows s0 + 128 j of the B map.
+struct Seg {
+  int r0, s0, n;
+};
+
+// Shared skeleton, warp-specialised, over one or two segments that share the
+// ring and the accumulators (the streamed-tile count j runs on across the
+// segment boundary).  Warp 8 (the producer) issues the TMA loads and the MMAs
+// into two TMEM accumulators and, per tile, fills that tile's column vector
+// with `prep(j, lane)` before marking the accumulator full; warps 0-7 wait
+// for it, call `epi(segment, j_in_segment, taddr)` with the TMEM address of
+// their 32 lanes and 64-column half, and release the accumulator.  At the
+// segment boundary the producer waits for the first segment's last MMA
+// (a_free) and reloads the resident tile.  No CTA-wide barrier inside the
+// loop.
 template <int D, bool kPrep, class Prep, class Epi>
 __device__ __forceinline__ bool tile_pipeline(uint8_t *smem, SmallState &st, const CUtensorMap *mapA,
-                                              const CUtensorMap *mapB, int r0, int s0, int n, int h,
-                                              Prep &&prep, Epi &&epi) {
+                                              const CUtensorMap *mapB, Seg s0_, Seg s1_, int h, Prep &&prep,
+                                              Epi &&epi) {
   using G = TileGeo<D>;
+  const int n0 = s0_.n, n = s0_.n + s1_.n;
+  auto brow = [&](int j) { return j < n0 ? s0_.s0 + kRows * j : s1_.s0 + kRows * (j - n0); };
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   uint8_t *sA = smem;
   uint8_t *sB = smem + G::kTileBytes;
   if (tid == 0) {
     mbar_init(&st.res_bar, 1);
+    mbar_init(&st.a_free, 1);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&st.ld_bar[s], 1);
       mbar_init(&st.ld_free[s], 1);
@@ -134,11 +150,11 @@ __device__ __forceinline__ bool tile_pipeline(uint8_t *smem, SmallState &st, con
   if (warp == kEpiWarps) {
     // ------------------------------------------------------------ producer
     int loads = 0, mmas = 0;
-    bool ok = true;
+    bool ok = true, a_reloading = false;
     if (lane == 0) {
-      load_tile<D>(sA, mapA, &st.res_bar, r0, h);
+      load_tile<D>(sA, mapA, &st.res_bar, s0_.r0, h);
       for (; loads < n && loads < kStages; ++loads)
-        load_tile<D>(sB + loads * G::kTileBytes, mapB, &st.ld_bar[loads], s0 + kRows * loads, h);
+        load_tile<D>(sB + loads * G::kTileBytes, mapB, &st.ld_bar[loads], brow(loads), h);
       ok = mbar_wait(&st.res_bar, 0);
     }
     ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -147,12 +163,22 @@ __device__ __forceinline__ bool tile_pipeline(uint8_t *smem, SmallState &st, con
       // the whole warp observes the accumulator (and its column vector) free
       if (j >= 2 && !(ok = wait_warp(&st.acc_empty[j & 1], ((j - 2) >> 1) & 1))) break;
       if (lane == 0) {
-        ok = mbar_wait(&st.ld_bar[j % kStages], (j / kStages) & 1);
+        if (j == n0 && j > 0) {  // segment boundary: the resident tile of the second segment
+          ok = mbar_wait(&st.a_free, 0);
+          if (ok) {
+            load_tile<D>(sA, mapA, &st.res_bar, s1_.r0, h);
+            a_reloading = true;
+            ok = mbar_wait(&st.res_bar, 1);
+            a_reloading = !ok;
+          }
+        }
+        if (ok) ok = mbar_wait(&st.ld_bar[j % kStages], (j / kStages) & 1);
         if (ok) {
           tc_fence_after();
           mma_tile<D>(tbase + (uint32_t)(j & 1) * 128, smem_u32(sA), smem_u32(sB + (j % kStages) * G::kTileBytes));
           umma_commit(&st.mma_full[j & 1]);
           umma_commit(&st.ld_free[j % kStages]);
+          if (j == n0 - 1 && n > n0) umma_commit(&st.a_free);
           mmas = j + 1;
         }
       }
@@ -169,7 +195,7 @@ __device__ __forceinline__ bool tile_pipeline(uint8_t *smem, SmallState &st, con
         const int sj = (j - 1) % kStages;
         ok = mbar_wait(&st.ld_free[sj], ((j - 1) / kStages) & 1);
         if (ok) {
-          load_tile<D>(sB + sj * G::kTileBytes, mapB, &st.ld_bar[sj], s0 + kRows * loads, h);
+          load_tile<D>(sB + sj * G::kTileBytes, mapB, &st.ld_bar[sj], brow(loads), h);
           ++loads;
         }
       }
@@ -182,6 +208,7 @@ __device__ __forceinline__ bool tile_pipeline(uint8_t *smem, SmallState &st, con
       umma_commit(&st.drain);
       mbar_wait(&st.drain, 0);
       for (int j = mmas; j < loads; ++j) mbar_wait(&st.ld_bar[j % kStages], (j / kStages) & 1);
+      if (a_reloading) mbar_wait(&st.res_bar, 1);
     }
   } else {
     // ------------------------------------------------------------ epilogue
@@ -192,7 +219,7 @@ __device__ __forceinline__ bool tile_pipeline(uint8_t *smem, SmallState &st, con
         break;
       }
       tc_fence_after();
-      epi(j, tbase + lane_off + (uint32_t)(j & 1) * 128);
+      epi(j >= n0 ? 1 : 0, j >= n0 ? j - n0 : j, tbase + lane_off + (uint32_t)(j & 1) * 128);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&st.acc_empty[j & 1]);
@@ -207,6 +234,9 @@ __device__ __forceinline__ bool tile_pipeline(uint8_t *smem, SmallState &st, con
 }
 
 // ------------------------------------------------------------- column sums
+// A CTA takes key tile p and key tile nkt-1-p of one head (two segments of
+// the pipeline): nkt - p and p + 1 query tiles, nkt + 1 in all, so the causal
+// triangle splits into equal CTAs.
 template <int D>
 __global__ void __launch_bounds__(kThreads, 2)
     colsum_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -218,28 +248,31 @@ __global__ void __launch_bounds__(kThreads, 2)
   float *raw = nl2 + 2 * kRows;                                   // [3][128]: LSE slices in flight
   SmallState &st = *(SmallState *)(raw + 3 * kRows);
   if (*(volatile int *)err) return;
-  // Head-major (a head's CTAs share its Q tiles in L2), heaviest key tile first.
-  const int h = blockIdx.x / nkt, kt = blockIdx.x % nkt;
-  const int k0 = kt * kRows;
-  const int nq = (L - k0 + kRows - 1) / kRows;
+  // Head-major (a head's CTAs share its Q tiles in L2).
+  const int npair = (nkt + 1) / 2;
+  const int h = blockIdx.x / npair, pr = blockIdx.x % npair;
+  const int kta = pr, ktb = nkt - 1 - pr;
+  const int k0a = kta * kRows, k0b = ktb * kRows;
+  const int na = nkt - kta, nb = (ktb != kta) ? nkt - ktb : 0;  // query tiles of each segment
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int row = (warp & 3) * 32 + lane;  // key within the tile (TMEM lane)
   const int c_off = (warp >> 2) * 64;      // this warp's query columns
   const float *lse_h = lse + (size_t)h * L;
-  // Column vector of query tile j: -LSE * log2(e) (-inf past L, so those
-  // zero-filled query rows add nothing).  The producer lanes fetch each
-  // tile's LSE slice with asynchronous 4-byte copies two tiles ahead (a
-  // three-slot staging ring), so no global load latency sits on the path
-  // that issues the MMAs.
+  // Column vector of streamed tile j (query tile k0 + 128 j' of its
+  // segment): -LSE * log2(e) (-inf past L, so those zero-filled query rows
+  // add nothing).  The producer lanes fetch each tile's LSE slice with
+  // asynchronous 4-byte copies two tiles ahead (a three-slot staging ring),
+  // so no global load latency sits on the path that issues the MMAs.
   struct Prep {
     const float *lse_h;
     float *nl2, *raw;
-    int k0, L, n;
+    int k0a, k0b, na, L, n;
+    __device__ int q0(int j) const { return j < na ? k0a + kRows * j : k0b + kRows * (j - na); }
     __device__ void fetch(int j, int ln) {  // copies of tile j, one commit group
       if (j < n) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const int q = k0 + kRows * j + ln + 32 * i;
+          const int q = q0(j) + ln + 32 * i;
           if (q < L) {
             asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(
                              sm100::smem_u32(raw + (j % 3) * kRows + ln + 32 * i)),
@@ -260,35 +293,44 @@ __global__ void __launch_bounds__(kThreads, 2)
       asm volatile("cp.async.wait_group 1;" ::: "memory");
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const int q = k0 + kRows * j + ln + 32 * i;
+        const int q = q0(j) + ln + 32 * i;
         nl2[(j & 1) * kRows + ln + 32 * i] = q < L ? -raw[(j % 3) * kRows + ln + 32 * i] * kLog2e : -INFINITY;
       }
       fetch(j + 2, ln);
     }
-  } prep{lse_h, nl2, raw, k0, L, nq};
-  float acc = 0.f;
-  auto epi = [&](int j, uint32_t taddr) {
-    const float *nl = nl2 + (j & 1) * kRows + c_off;
+  } prep{lse_h, nl2, raw, k0a, k0b, na, L, na + nb};
+  float acc[2] = {0.f, 0.f};  // this thread's key row, per segment
+  auto epi = [&](int seg, int j, uint32_t taddr) {
+    const float *nl = nl2 + ((seg ? na + j : j) & 1) * kRows + c_off;
     uint32_t r[64];
     tmem_ld64(taddr, r);
+    float a = 0.f;
     if (j == 0) {  // diagonal tile: query column c contributes iff c >= key row
 #pragma unroll
       for (int i = 0; i < 64; ++i) {
         const float e = ex2(fmaf(__uint_as_float(r[i]), qscale, nl[i]));
-        acc += (c_off + i >= row) ? e : 0.f;
+        a += (c_off + i >= row) ? e : 0.f;
       }
     } else {
 #pragma unroll
-      for (int i = 0; i < 64; ++i) acc += ex2(fmaf(__uint_as_float(r[i]), qscale, nl[i]));
+      for (int i = 0; i < 64; ++i) a += ex2(fmaf(__uint_as_float(r[i]), qscale, nl[i]));
     }
+    if (seg) acc[1] += a;
+    else acc[0] += a;
   };
-  const bool ok = tile_pipeline<D, true>(smem, st, &tmK, &tmQ, k0, k0, nq, h, prep, epi);
-  // the two column halves of each key row: the second half hands its sum over
-  float *half = nl2;  // free after the pipeline
-  if (ok && warp >= 4 && warp < kEpiWarps) half[row] = acc;
+  const bool ok = tile_pipeline<D, true>(smem, st, &tmK, &tmQ, Seg{k0a, k0a, na}, Seg{k0b, k0b, nb}, h, prep, epi);
+  // the two column halves of each key row: the second half hands its sums over
+  float *half = nl2;  // [2][128], free after the pipeline
+  if (ok && warp >= 4 && warp < kEpiWarps) {
+    half[row] = acc[0];
+    half[kRows + row] = acc[1];
+  }
   __syncthreads();
   if (ok) {
-    if (warp < 4 && k0 + row < L) colsum[(size_t)h * L + k0 + row] = acc + half[row];
+    if (warp < 4) {
+      if (k0a + row < L) colsum[(size_t)h * L + k0a + row] = acc[0] + half[row];
+      if (nb > 0 && k0b + row < L) colsum[(size_t)h * L + k0b + row] = acc[1] + half[kRows + row];
+    }
   } else if (tid == 0) {
     atomicOr(err, 4);
   }
@@ -317,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     __device__ void load(int, int) {}
     __device__ void store(int, int) {}
   } prep;
-  auto epi = [&](int j, uint32_t taddr) {
+  auto epi = [&](int, int j, uint32_t taddr) {
     const bool diag = (j == nk - 1);
     uint32_t r[64];
     tmem_ld64(taddr, r);
@@ -337,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     l = l * ex2(m - mn) + sum;
     m = mn;
   };
-  const bool ok = tile_pipeline<D, false>(smem, st, &tmQ, &tmK, q0, 0, nk, h, prep, epi);
+  const bool ok = tile_pipeline<D, false>(smem, st, &tmQ, &tmK, Seg{q0, 0, nk}, Seg{0, 0, 0}, h, prep, epi);
   if (ok && warp >= 4 && warp < kEpiWarps) {
     xch[row] = m;
     xch[kRows + row] = l;
@@ -668,7 +710,7 @@ cudaError_t colsum_t(const CacheView &c, const void *Q, const void *K, const flo
   cudaError_t e = cudaFuncSetAttribute(colsum_tc<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int nkt = (L + kRows - 1) / kRows;
-  const long long grid = (long long)nkt * c.nh;
+  const long long grid = (long long)((nkt + 1) / 2) * c.nh;  // key-tile pairs
   colsum_tc<D><<<(unsigned)grid, kThreads, smem, st>>>(mq, mk, lse, colsum, L, nkt, kLog2e / sqrtf((float)D),
                                                       c.err);
   return cudaGetLastError();

@@ -67,6 +67,8 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
   tmem_ld32(taddr, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
   tmem_ld32(taddr + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
   tmem_ld_wait();
+  tmem_regs_ready(*reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+  tmem_regs_ready(*reinterpret_cast<uint32_t(*)[32]>(&r[32]));
 }
 
 // Bounded wait whose outcome is the same for the whole warp (so the warp's
@@ -304,17 +306,18 @@ __global__ void __launch_bounds__(kThreads, 2)
     const float *nl = nl2 + ((seg ? na + j : j) & 1) * kRows + c_off;
     uint32_t r[64];
     tmem_ld64(taddr, r);
-    float a = 0.f;
+    float a4[4] = {0.f, 0.f, 0.f, 0.f};  // four partial sums: short dependency chains
     if (j == 0) {  // diagonal tile: query column c contributes iff c >= key row
 #pragma unroll
       for (int i = 0; i < 64; ++i) {
         const float e = ex2(fmaf(__uint_as_float(r[i]), qscale, nl[i]));
-        a += (c_off + i >= row) ? e : 0.f;
+        a4[i & 3] += (c_off + i >= row) ? e : 0.f;
       }
     } else {
 #pragma unroll
-      for (int i = 0; i < 64; ++i) a += ex2(fmaf(__uint_as_float(r[i]), qscale, nl[i]));
+      for (int i = 0; i < 64; ++i) a4[i & 3] += ex2(fmaf(__uint_as_float(r[i]), qscale, nl[i]));
     }
+    const float a = (a4[0] + a4[1]) + (a4[2] + a4[3]);
     if (seg) acc[1] += a;
     else acc[0] += a;
   };
@@ -363,19 +366,21 @@ __global__ void __launch_bounds__(kThreads, 2)
     const bool diag = (j == nk - 1);
     uint32_t r[64];
     tmem_ld64(taddr, r);
-    float cm = -INFINITY;
+    float cm4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // partial maxima
 #pragma unroll
     for (int i = 0; i < 64; ++i) {
       float x = __uint_as_float(r[i]) * qscale;
       if (diag && c_off + i > row) x = -INFINITY;  // key after the query
       r[i] = __float_as_uint(x);
-      cm = fmaxf(cm, x);
+      cm4[i & 3] = fmaxf(cm4[i & 3], x);
     }
+    const float cm = fmaxf(fmaxf(cm4[0], cm4[1]), fmaxf(cm4[2], cm4[3]));
     if (cm == -INFINITY) return;  // every column masked (second half of the diagonal)
     const float mn = fmaxf(m, cm);
-    float sum = 0.f;
+    float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int i = 0; i < 64; ++i) sum += ex2(__uint_as_float(r[i]) - mn);
+    for (int i = 0; i < 64; ++i) s4[i & 3] += ex2(__uint_as_float(r[i]) - mn);
+    const float sum = (s4[0] + s4[1]) + (s4[2] + s4[3]);
     l = l * ex2(m - mn) + sum;
     m = mn;
   };
@@ -557,14 +562,15 @@ __global__ void __launch_bounds__(kOutThreads, 1)
       const bool diag = (j == n - 1);
       uint32_t r[64];
       tmem_ld64(tbase + lane_off + (uint32_t)(j & 1) * 128 + (uint32_t)c_off, r);
-      float hm = -INFINITY;
+      float hm4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // partial maxima
 #pragma unroll
       for (int i = 0; i < 64; ++i) {
         float x = __uint_as_float(r[i]) * qscale;
         if (diag && c_off + i > row) x = -INFINITY;  // key after the query
         r[i] = __float_as_uint(x);
-        hm = fmaxf(hm, x);
+        hm4[i & 3] = fmaxf(hm4[i & 3], x);
       }
+      const float hm = fmaxf(fmaxf(hm4[0], hm4[1]), fmaxf(hm4[2], hm4[3]));
       tc_fence_before();
       mbar_arrive(&st.sfree[j & 1]);  // the logits are in registers: S buffer free
       // Half-row maxima: each warp writes into the partner's rows of this P
@@ -594,6 +600,7 @@ __global__ void __launch_bounds__(kOutThreads, 1)
           const uint32_t ta = tO + lane_off + (uint32_t)(half * kHalfD + cc);
           tmem_ld32(ta, o);
           tmem_ld_wait();
+          tmem_regs_ready(o);
 #pragma unroll
           for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * f);
           tmem_st32(ta, o);
@@ -603,16 +610,16 @@ __global__ void __launch_bounds__(kOutThreads, 1)
       }
       m_run = m_new;
       uint32_t pk[32];
-      float ls = 0.f;
+      float ls4[4] = {0.f, 0.f, 0.f, 0.f};  // partial row sums
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
         const float a = ex2(__uint_as_float(r[2 * i]) - m_run);  // masked: exp2(-inf) = 0
         const float b = ex2(__uint_as_float(r[2 * i + 1]) - m_run);
-        ls += a + b;
+        ls4[i & 3] += a + b;
         __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
         pk[i] = *reinterpret_cast<uint32_t *>(&v);
       }
-      l_run += ls;
+      l_run += (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
       // 64 keys = one 128-byte row of box `half`: eight 16-byte chunks, swizzled by row.
       uint8_t *prow = pbuf + half * kBox + row * 128;
 #pragma unroll
@@ -640,6 +647,7 @@ __global__ void __launch_bounds__(kOutThreads, 1)
         uint32_t o[32];
         tmem_ld32(tO + lane_off + (uint32_t)(half * kHalfD + c0), o);
         tmem_ld_wait();
+        tmem_regs_ready(o);
         if (q < L) {
           uint32_t pk[16];
 #pragma unroll

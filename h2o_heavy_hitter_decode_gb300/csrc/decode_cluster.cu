@@ -92,7 +92,6 @@ __global__ void __launch_bounds__(kThreads, 7) decode_cluster_kernel(const CArgs
   __shared__ __align__(8) uint64_t s_bml, s_bacc, s_bcand;
   // every rank's (m, l) (and rank 0's new-token logit), in every CTA
   __shared__ __align__(16) uint4 s_mlx[kMaxCluster];
-  __shared__ __align__(16) float s_accx[kMaxCluster][D];   // every rank's acc row (rank 0)
   __shared__ __align__(16) uint4 s_candx[kMaxCluster];     // every rank's candidate, in every CTA
   __shared__ float s_ML[2], s_lgnew, s_f[kMaxCluster];
   __shared__ ArgMin s_am[kConsumers];
@@ -112,7 +111,8 @@ __global__ void __launch_bounds__(kThreads, 7) decode_cluster_kernel(const CArgs
   const size_t step_elems = (size_t)c.nh * D;
 
   // dynamic shared memory: [ring or resident K|V][score][pos][logit]
-  // (+ [K scale][V scale] for an fp8 cache)
+  // (+ [K scale][V scale] for an fp8 cache)[every rank's acc row, P x D, read
+  // on rank 0]
   uint8_t *kv = smem;
   const int kv_bytes = kResident ? 2 * chunk * ROWB : ring_bytes(kStages);
   float *sc = (float *)(smem + kv_bytes);
@@ -120,6 +120,7 @@ __global__ void __launch_bounds__(kThreads, 7) decode_cluster_kernel(const CArgs
   float *lg = (float *)(ps + chunk);
   float *ksc = lg + chunk;
   float *vsc = ksc + chunk;
+  float *accx = (float *)(smem + ((kv_bytes + (kFp8 ? 5 : 3) * chunk * 4 + 15) & ~15));
 
   if (tid == 0) {
     for (int i = 0; i < kStages; ++i) {
@@ -348,7 +349,7 @@ __global__ void __launch_bounds__(kThreads, 7) decode_cluster_kernel(const CArgs
         float t = 0.f;
 #pragma unroll
         for (int w = 0; w < kConsumers; ++w) t = fmaf(f[w], s_wacc[w][col], t);
-        st_async_b32(mapa(&s_accx[rank][col], 0), __float_as_uint(t), mapa(&s_bacc, 0));  // to rank 0
+        st_async_b32(mapa(&accx[rank * D + col], 0), __float_as_uint(t), mapa(&s_bacc, 0));  // to rank 0
       }
       if (tid < P) {  // (m, l) to every rank
         float ls = 0.f;
@@ -386,7 +387,7 @@ __global__ void __launch_bounds__(kThreads, 7) decode_cluster_kernel(const CArgs
       for (int col = tid; col < D; col += kThreads) {
         float o = 0.f;
         for (int r = 0; r < P; ++r)
-          if (s_f[r] != 0.f) o = fmaf(s_f[r], s_accx[r][col], o);
+          if (s_f[r] != 0.f) o = fmaf(s_f[r], accx[r * D + col], o);
         out[col] = from_f32<T>(o * invL);
       }
     }
@@ -532,15 +533,16 @@ int resident_rows_ok(int chunk) {
 }
 
 template <typename S, int D, bool R, int St>
-int smem_bytes(int chunk) {
-  return (R ? 2 * chunk * Geo<S, D>::ROWB : ring_bytes(St)) + slot_words<S>() * chunk * 4;
+int smem_bytes(int chunk, int P) {
+  const int base = (R ? 2 * chunk * Geo<S, D>::ROWB : ring_bytes(St)) + slot_words<S>() * chunk * 4;
+  return ((base + 15) & ~15) + P * D * 4;  // + every rank's acc row
 }
 
 template <typename T, typename S, int D, bool R, int St>
 cudaError_t launch_cluster_t(const CacheView &c, const DecodeStep &s, int nsteps, cudaStream_t st) {
   const int P = c.nsplit;
   CArgs a{c, s, nsteps, (c.k + P - 1) / P, kLog2e / sqrtf((float)D)};
-  const int smem = smem_bytes<S, D, R, St>(a.chunk);
+  const int smem = smem_bytes<S, D, R, St>(a.chunk, P);
   if (smem > 200 * 1024) return cudaErrorInvalidValue;
   static bool attr_done[64] = {};
   int dev = 0;
@@ -570,7 +572,7 @@ bool all_resident(const CacheView &c, int chunk) {
   int dev = 0, sms = 0, per_sm = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return false;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
-  const int smem = smem_bytes<S, D, R, St>(chunk);
+  const int smem = smem_bytes<S, D, R, St>(chunk, c.nsplit);
   if (smem > 200 * 1024) return false;
   if (cudaFuncSetAttribute(decode_cluster_kernel<T, S, D, R, St>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            200 * 1024) != cudaSuccess)
@@ -612,7 +614,7 @@ bool cluster_waves_ok_t(const CacheView &c) {
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_cluster_kernel<T, S, D, false, 3>, kThreads,
-                                                    smem_bytes<S, D, false, 3>(chunk)) != cudaSuccess)
+                                                    smem_bytes<S, D, false, 3>(chunk, c.nsplit)) != cudaSuccess)
     return false;
   return (long long)c.nh * c.nsplit >= 3LL * per_sm * sms;
 }
@@ -650,7 +652,7 @@ bool decode_cluster_supported(const CacheView &c) {
   const int chunk = (c.k + c.nsplit - 1) / c.nsplit;
   const int row = c.d * (c.kv_fp8 ? 1 : c.dtype == 1 ? 2 : 4);
   const int kv = (2 * chunk * row <= kResidentMaxBytes) ? 2 * chunk * row : ring_bytes(3);
-  return kv + (c.kv_fp8 ? 5 : 3) * chunk * 4 <= 200 * 1024;
+  return kv + (c.kv_fp8 ? 5 : 3) * chunk * 4 + 16 + c.nsplit * c.d * 4 <= 200 * 1024;
 }
 
 cudaError_t launch_decode_cluster(const CacheView &c, const DecodeStep &s, int nsteps, cudaStream_t st) {

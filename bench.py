@@ -17,7 +17,8 @@ Printed JSON line (rank 0):
   e2e       the same metric with host (pinned) buffers, copies timed;
   cpu_baseline  the fp64 oracle on the host cores on a sample of heads.
 
-`--impl reference` times the oracle alone (the reference arm of this build).
+`--impl reference` times the oracle alone (the reference arm: the method's
+reference semantics on the host cores).
 """
 from __future__ import annotations
 

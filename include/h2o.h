@@ -48,7 +48,7 @@ typedef enum {
   H2O_ECUDA = 3,    /* a CUDA runtime call failed; h2o_last_cuda_error() has the code */
   H2O_ENOMEM = 4,   /* host allocation failed */
   H2O_EDEVICE = 5,  /* the device flagged an internal inconsistency (h2o_get_error) */
-  H2O_EUNSUPPORTED = 6 /* valid request this build does not handle (e.g. d not 64/128) */
+  H2O_EUNSUPPORTED = 6 /* valid request this library does not handle (e.g. d not 64/128) */
 } h2o_status;
 
 /* Element types of a cache.  H2O_F32 / H2O_BF16: inputs, outputs and the

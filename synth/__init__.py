@@ -81,6 +81,7 @@ CONFIGS = [
     Workload("long_stream_B1H32d128_L256_T4194304_k128+128", 1, 32, 128, 256, 4194304, 128, 128, "bf16",
              BASE_SEED + 4),
 ]
+TINY, OPT_6_7B, OPT_30B, PREFILL_HEAVY, LONG_STREAM = CONFIGS
 
 
 def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:

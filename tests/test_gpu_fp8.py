@@ -53,18 +53,18 @@ def _sample(w, count, seed=5):
     return sorted(rng.choice(w.nh, size=min(count, w.nh), replace=False).tolist())
 
 
-@pytest.mark.parametrize("idx,count", [(1, 8), (2, 8), (3, 2)])
-def test_fp8_full_size_sampled_heads(idx, count):
+@pytest.mark.parametrize("w,count", [(synth.OPT_6_7B, 8), (synth.OPT_30B, 8), (synth.PREFILL_HEAVY, 2)],
+                         ids=lambda x: getattr(x, "name", str(x)))
+def test_fp8_full_size_sampled_heads(w, count):
     """Full-size workloads with an fp8 cache in the bench's launch
     configuration (automatic decode form) on a seeded head sample."""
-    w = synth.CONFIGS[idx]
     rep, cache = run_parity(w, heads=_sample(w, count), resync=False, kv_fp8=True)
     print(w.name, rep)
     assert rep.steps_compared >= w.T
 
 
 def test_fp8_long_stream_first_steps():
-    w = synth.CONFIGS[4]
+    w = synth.LONG_STREAM
     rep, cache = run_parity(w, T=8192, kv_fp8=True)
     print(w.name, rep)
     assert rep.steps_compared >= 8192

@@ -25,7 +25,7 @@ def small(name, B, H, d, L, T, kh, kl, dt, seed=77, planted=0.0):
 
 
 SMALL = [
-    synth.CONFIGS[0],
+    synth.TINY,
     small("bf16_multitile_ragged", 2, 3, 128, 300, 40, 64, 64, "bf16"),
     small("bf16_d64_prompt_shorter_than_budget", 1, 4, 64, 50, 80, 40, 30, "bf16"),
     small("bf16_no_local_block", 1, 2, 128, 100, 50, 32, 0, "bf16"),
@@ -80,9 +80,10 @@ def _sample(w, count, seed=5):
     return sorted(rng.choice(w.nh, size=min(count, w.nh), replace=False).tolist())
 
 
-@pytest.mark.parametrize("idx,count,want_O", [(1, 8, True), (2, 12, True), (3, 3, True), (3, 3, False)])
-def test_full_size_sampled_heads(idx, count, want_O):
-    w = synth.CONFIGS[idx]
+@pytest.mark.parametrize("w,count,want_O", [(synth.OPT_6_7B, 8, True), (synth.OPT_30B, 12, True),
+                                            (synth.PREFILL_HEAVY, 3, True), (synth.PREFILL_HEAVY, 3, False)],
+                         ids=lambda x: getattr(x, "name", str(x)))
+def test_full_size_sampled_heads(w, count, want_O):
     rep, cache = run_parity(w, heads=_sample(w, count), resync=False, want_O=want_O)
     print(w.name, rep)
     assert rep.steps_compared >= w.T
@@ -90,7 +91,7 @@ def test_full_size_sampled_heads(idx, count, want_O):
 
 def test_long_stream_first_steps():
     """The long-stream workload, checked on its first 65,536 decode steps."""
-    w = synth.CONFIGS[4]
+    w = synth.LONG_STREAM
     rep, cache = run_parity(w, T=65536)
     print(w.name, rep)
     assert rep.steps_compared >= 65536

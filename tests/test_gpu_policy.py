@@ -23,7 +23,7 @@ def small(name, B, H, d, L, T, kh, kl, dt, seed=91, planted=0.0):
 
 # (workload, [(n_sink, score_mode), ...]); n_sink = k_heavy is sinks + window
 CASES = [
-    (synth.CONFIGS[0], [(4, 0), (0, 1), (4, 1), (16, 0)]),
+    (synth.TINY, [(4, 0), (0, 1), (4, 1), (16, 0)]),
     (small("bf16_multitile_ragged", 2, 3, 128, 300, 40, 64, 64, "bf16"), [(8, 0), (0, 1), (8, 1), (64, 0)]),
     (small("bf16_no_local_block", 1, 2, 128, 100, 50, 32, 0, "bf16"), [(4, 1), (32, 0)]),
     (small("bf16_d64_prompt_shorter_than_budget", 1, 4, 64, 50, 80, 40, 30, "bf16"), [(10, 1)]),
@@ -51,11 +51,12 @@ def _sample(w, count, seed=5):
     return sorted(rng.choice(w.nh, size=min(count, w.nh), replace=False).tolist())
 
 
-@pytest.mark.parametrize("idx,count,policy", [(1, 8, (4, 1)), (1, 8, (256, 0)), (2, 8, (0, 1))])
-def test_policy_full_size_sampled_heads(idx, count, policy):
+@pytest.mark.parametrize("w,count,policy", [(synth.OPT_6_7B, 8, (4, 1)), (synth.OPT_6_7B, 8, (256, 0)),
+                                            (synth.OPT_30B, 8, (0, 1))],
+                         ids=lambda x: getattr(x, "name", str(x)))
+def test_policy_full_size_sampled_heads(w, count, policy):
     """Full-size workloads in the bench's launch configuration (automatic
     decode form) on a seeded head sample."""
-    w = synth.CONFIGS[idx]
     rep, cache = run_parity(w, heads=_sample(w, count), resync=False, policy=policy)
     print(w.name, policy, rep)
     assert rep.steps_compared >= w.T

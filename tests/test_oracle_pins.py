@@ -445,7 +445,7 @@ def test_naive_topk_is_not_h2o():
     """The page warns that a fresh Top-K each step is a different algorithm:
     keeping the k entries with the largest weight of the current step alone
     gives other cache sets than H2O on the tiny workload."""
-    w = synth.CONFIGS[0]
+    w = synth.TINY
     Q, K, V = (synth.as_f64(x, w.dtype) for x in synth.prompt(w))
     qd, kd, vd = (synth.as_f64(x, w.dtype) for x in synth.decode(w, 0, w.T))
     r = oracle.prefill(Q, K, V, w.k_heavy, w.k_local)

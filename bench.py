@@ -325,12 +325,15 @@ def run_ours(args, w, rank, world, local_rank):
     return line if rank == 0 else None
 
 
-def e2e(args, w, dev, hQ, hK, hV, hq, hk, hv, tdt, stream, world, dist, copy_streams=1):
+def e2e(args, w, dev, hQ, hK, hV, hq, hk, hv, tdt, stream, world, dist, row_groups=4, step_groups=4):
     """Same job from pinned host buffers: H2D of every input, prefill, decode,
-    D2H of the decode outputs, all inside the timed events.  The input copies
-    run on a side stream (more copy streams measured no faster); the
-    prefill waits for the prompt only, so the decode inputs land while it
-    runs."""
+    D2H of the decode outputs, all inside the timed events.  The prompt is
+    copied on a side stream in `row_groups` groups of batch rows and each
+    group is prefilled (h2o_prefill_rows) as soon as it has landed, so the
+    prefill of one group overlaps the copy of the next.  The decode inputs
+    follow in `step_groups` groups of steps; each group is decoded as soon as
+    its inputs have landed and its outputs are copied back while the next
+    group decodes."""
     import torch
     from h2o_heavy_hitter_decode_gb300 import H2OCache
     pin = [x.pin_memory() for x in (hQ, hK, hV, hq, hk, hv)]
@@ -341,37 +344,45 @@ def e2e(args, w, dev, hQ, hK, hV, hq, hk, hv, tdt, stream, world, dist, copy_str
     out = torch.empty(hq.shape, dtype=tdt, device=dev)
     hout = torch.empty(hq.shape, dtype=tdt).pin_memory()
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-    side = [torch.cuda.Stream(device=dev) for _ in range(copy_streams)]
-
-    def copy_group(idx, start_ev):
-        done = []
-        for s in side:
-            s.wait_event(start_ev)
-        for t in idx:
-            src, dst = pin[t].reshape(-1), dbuf[t].reshape(-1)
-            n = src.numel()
-            for i, s in enumerate(side):
-                lo, hi = n * i // len(side), n * (i + 1) // len(side)
-                with torch.cuda.stream(s):
-                    dst[lo:hi].copy_(src[lo:hi], non_blocking=True)
-        for s in side:
-            ev = torch.cuda.Event()
-            ev.record(s)
-            done.append(ev)
-        return done
+    side = torch.cuda.Stream(device=dev)
+    back = torch.cuda.Stream(device=dev)
+    ng = max(1, min(row_groups, w.B))
+    groups = [(w.B * g // ng, w.B * (g + 1) // ng) for g in range(ng)]
+    ns = max(1, min(step_groups, w.T))
+    sgroups = [(w.T * g // ns, w.T * (g + 1) // ns) for g in range(ns)]
 
     def job(start_ev):
-        prompt_done = copy_group((0, 1, 2), start_ev)
-        dec_done = copy_group((3, 4, 5), start_ev)
-        for ev in prompt_done:
-            stream.wait_event(ev)
+        side.wait_event(start_ev)
+        landed = []
+        with torch.cuda.stream(side):
+            for b0, b1 in groups:  # prompt rows, group by group
+                for t in (0, 1, 2):
+                    dbuf[t][b0:b1].copy_(pin[t][b0:b1], non_blocking=True)
+                ev = torch.cuda.Event()
+                ev.record(side)
+                landed.append(ev)
+            dec_landed = []
+            for t0, t1 in sgroups:  # decode inputs, behind the prompt, group by group
+                for t in (3, 4, 5):
+                    dbuf[t][t0:t1].copy_(pin[t][t0:t1], non_blocking=True)
+                ev = torch.cuda.Event()
+                ev.record(side)
+                dec_landed.append(ev)
         c = H2OCache(w.B, w.H, w.d, w.k_heavy, w.k_local, tdt, device=dev, kv_fp8=is_kvfp8(w))
         c.set_decode_form(args.decode_form)
-        c.prefill(dbuf[0], dbuf[1], dbuf[2], O=O, lse=lse, colsum=colsum)
-        for ev in dec_done:
+        for (b0, b1), ev in zip(groups, landed):
             stream.wait_event(ev)
-        c.steps(dbuf[3], dbuf[4], dbuf[5], out=out)
-        hout.copy_(out, non_blocking=True)
+            c.prefill_rows(b0, dbuf[0][b0:b1], dbuf[1][b0:b1], dbuf[2][b0:b1], O=O[b0:b1], lse=lse[b0:b1],
+                           colsum=colsum[b0:b1])
+        for (t0, t1), ev in zip(sgroups, dec_landed):
+            stream.wait_event(ev)
+            c.steps(dbuf[3][t0:t1], dbuf[4][t0:t1], dbuf[5][t0:t1], out=out[t0:t1])
+            done = torch.cuda.Event()
+            done.record(stream)
+            back.wait_event(done)
+            with torch.cuda.stream(back):
+                hout[t0:t1].copy_(out[t0:t1], non_blocking=True)
+        stream.wait_stream(back)  # the job ends when its outputs are on the host
         return c
 
     n = args.steps
@@ -395,7 +406,7 @@ def e2e(args, w, dev, hQ, hK, hV, hq, hk, hv, tdt, stream, world, dist, copy_str
     h2d = sum(x.numel() * x.element_size() for x in pin)
     d2h = hout.numel() * hout.element_size()
     return {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "ms_per_step": ms_step, "copy_streams": copy_streams}
+            "ms_per_step": ms_step, "prompt_row_groups": ng, "decode_step_groups": ns}
 
 
 # ------------------------------------------------------------ oracle timing

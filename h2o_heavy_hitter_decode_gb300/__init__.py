@@ -62,6 +62,7 @@ def lib():
         L.h2o_cache_destroy.argtypes = [vp]
         L.h2o_set_stream.argtypes = [vp, vp]
         L.h2o_prefill.argtypes = [vp, vp, vp, vp, i32, vp, vp, vp]
+        L.h2o_prefill_rows.argtypes = [vp, i32, i32, vp, vp, vp, i32, vp, vp, vp]
         L.h2o_decode_step.argtypes = [vp, vp, vp, vp, vp]
         L.h2o_decode_steps.argtypes = [vp, i32, vp, vp, vp, vp, vp]
         L.h2o_cache_export.argtypes = [vp, vp, vp, vp, vp, C.POINTER(i64), C.POINTER(i32)]
@@ -80,7 +81,8 @@ def lib():
         L.h2o_status_str.restype = C.c_char_p
         L.h2o_last_cuda_error.restype = i32
         L.h2o_build_arch.restype = i32
-        for f in ("h2o_cache_create", "h2o_cache_destroy", "h2o_set_stream", "h2o_prefill", "h2o_decode_step",
+        for f in ("h2o_cache_create", "h2o_cache_destroy", "h2o_set_stream", "h2o_prefill", "h2o_prefill_rows",
+                  "h2o_decode_step",
                   "h2o_decode_steps", "h2o_cache_export", "h2o_cache_import", "h2o_cache_info",
                   "h2o_get_error", "h2o_profile_enable", "h2o_profile_read", "h2o_set_decode_form",
                   "h2o_decode_form_used", "h2o_cache_set_policy", "h2o_cache_get_policy",
@@ -182,6 +184,29 @@ class H2OCache:
         self._sync_stream()
         _check(lib().h2o_prefill(self._h, _ptr(Q), _ptr(K), _ptr(V), int(Lp), _ptr(O), _ptr(lse), _ptr(colsum)),
                "h2o_prefill")
+        return O, lse, colsum
+
+    def prefill_rows(self, b0: int, Q, K, V, O=None, lse=None, colsum=None, want_O=True):
+        """Prefill of batch rows b0 .. b0+nb-1 (nb = Q.shape[0]); returns
+        (O, lse, colsum) of those rows.  Decode may start once every row is
+        prefilled, all with the same prompt length."""
+        nb, H, d = Q.shape[0], self.H, self.d
+        Lp = Q.shape[2]
+        shp = (nb, H, Lp, d)
+        self._arg(Q, shp, "Q"); self._arg(K, shp, "K"); self._arg(V, shp, "V")
+        if O is None and want_O:
+            O = torch.empty(shp, dtype=self.dtype, device=self.device)
+        if O is not None:
+            self._arg(O, shp, "O")
+        if lse is None:
+            lse = torch.empty((nb, H, Lp), dtype=torch.float32, device=self.device)
+        if colsum is None:
+            colsum = torch.empty((nb, H, Lp), dtype=torch.float32, device=self.device)
+        self._arg(lse, (nb, H, Lp), "lse", torch.float32)
+        self._arg(colsum, (nb, H, Lp), "colsum", torch.float32)
+        self._sync_stream()
+        _check(lib().h2o_prefill_rows(self._h, int(b0), int(nb), _ptr(Q), _ptr(K), _ptr(V), int(Lp), _ptr(O),
+                                      _ptr(lse), _ptr(colsum)), "h2o_prefill_rows")
         return O, lse, colsum
 
     def step(self, q, k, v, out=None):

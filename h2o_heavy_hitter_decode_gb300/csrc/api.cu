@@ -35,6 +35,9 @@ struct h2o_cache {
   int64_t next_pos;
   int n_valid;
   bool prefilled;
+  std::vector<char> row_done;  // batch rows prefilled so far (h2o_prefill_rows)
+  int rows_done = 0;
+  int prefill_L = 0;           // prompt length shared by every row
   cudaStream_t stream;
   int device;
   CacheView view;
@@ -254,13 +257,35 @@ h2o_status h2o_set_stream(h2o_cache_t c, void *s) {
 
 h2o_status h2o_prefill(h2o_cache_t c, const void *Q, const void *K, const void *V, int L, void *O,
                        float *lse, float *colsum) {
+  if (!c) return H2O_EINVAL;
+  return h2o_prefill_rows(c, 0, c->B, Q, K, V, L, O, lse, colsum);
+}
+
+h2o_status h2o_prefill_rows(h2o_cache_t c, int b0, int nb, const void *Q, const void *K, const void *V, int L,
+                            void *O, float *lse, float *colsum) {
   if (!c || !Q || !K || !V || !lse || !colsum) return H2O_EINVAL;
   if (L < 1 || (int64_t)L >= kMaxPos) return H2O_EINVAL;
+  if (b0 < 0 || nb < 1 || b0 > c->B - nb) return H2O_EINVAL;
   if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || (O && !aligned16(O)) || !aligned16(lse) ||
       !aligned16(colsum))
     return H2O_EINVAL;
   if (c->prefilled) return H2O_ESTATE;
-  const CacheView &v = c->view;
+  if (c->rows_done > 0 && L != c->prefill_L) return H2O_EINVAL;  // one prompt length per cache
+  if ((int)c->row_done.size() != c->B) c->row_done.assign((size_t)c->B, 0);
+  for (int b = b0; b < b0 + nb; ++b)
+    if (c->row_done[(size_t)b]) return H2O_ESTATE;  // a row is prefilled once
+  // The rows' heads are a contiguous block of the slot-major workspace.
+  CacheView v = c->view;
+  const size_t hoff = (size_t)b0 * c->H, slots = hoff * c->k;
+  v.nh = nb * c->H;
+  v.K = (char *)v.K + slots * c->d * c->ssize;
+  v.V = (char *)v.V + slots * c->d * c->ssize;
+  v.pos += slots;
+  v.score += slots;
+  if (v.kv_fp8) {
+    v.Ksc += slots;
+    v.Vsc += slots;
+  }
   cudaError_t e;
   const bool tc = prefill_tc_supported(v, L);
   {
@@ -283,9 +308,14 @@ h2o_status h2o_prefill(h2o_cache_t c, const void *Q, const void *K, const void *
     if (e != cudaSuccess) return cuda_fail(e);
     pt.done();
   }
-  c->next_pos = L;
-  c->n_valid = L < c->k ? L : c->k;
-  c->prefilled = true;
+  for (int b = b0; b < b0 + nb; ++b) c->row_done[(size_t)b] = 1;
+  c->rows_done += nb;
+  c->prefill_L = L;
+  if (c->rows_done == c->B) {  // every row has its initial cache: decode may start
+    c->next_pos = L;
+    c->n_valid = L < c->k ? L : c->k;
+    c->prefilled = true;
+  }
   return H2O_OK;
 }
 

@@ -99,6 +99,17 @@ h2o_status h2o_set_stream(h2o_cache_t cache, void *cuda_stream);
 h2o_status h2o_prefill(h2o_cache_t cache, const void *Q, const void *K, const void *V, int L,
                        void *O, float *lse, float *colsum);
 
+/* The same prefill for batch rows b0 .. b0+nb-1 only (every head of those
+ * rows), so a caller can prefill sequences as their prompts arrive, or
+ * overlap the copy of one group of rows with the prefill of another.
+ * Q, K, V, O, lse, colsum point at those rows: [nb][H][L][d] and
+ * [nb][H][L].  Every row of a cache is prefilled exactly once and with the
+ * same L (H2O_EINVAL for a different L, H2O_ESTATE for a row already done);
+ * decode may start once all B rows are done (H2O_ESTATE before).
+ * h2o_prefill is this call with b0 = 0, nb = B. */
+h2o_status h2o_prefill_rows(h2o_cache_t cache, int b0, int nb, const void *Q, const void *K, const void *V,
+                            int L, void *O, float *lse, float *colsum);
+
 /* One decode step ("Algorithm / figure walkthrough" steps 2-4) for every head,
  * one kernel launch: attend over the cached entries plus the new token,
  * add the exact weights into the scores, evict, write the new token in place.

@@ -74,6 +74,7 @@ def test_null_handle_rejected(L):
     assert L.h2o_cache_set_policy(None, 0, 0) == 1
     assert L.h2o_cache_get_policy(None, None, None) == 1
     assert L.h2o_cache_export_scales(None, None, None) == 1
+    assert L.h2o_prefill_rows(None, 0, 1, None, None, None, 4, None, None, None) == 1
     assert L.h2o_cache_import_scales(None, None, None) == 1
     assert L.h2o_cache_destroy(None) == 0
 

@@ -126,3 +126,34 @@ def test_position_overflow_rejected():
         c.steps(x, x, x)
     c.steps(x[:2], x[:2], x[:2])  # the last two positions still fit
     torch.cuda.synchronize()
+
+
+def test_zero_steps_and_form_reporting():
+    """n = 0 decode steps is a no-op; the form that ran is reported."""
+    w = synth.Workload("forms_report", 1, 4, 128, 64, 3, 16, 16, "bf16", 55)
+    Q, K, V = synth.prompt(w)
+    shp = (w.B, w.H, w.L, w.d)
+    from parity_helpers import to_dev
+    from h2o_heavy_hitter_decode_gb300 import H2OCache
+    c = H2OCache(w.B, w.H, w.d, w.k_heavy, w.k_local, torch.bfloat16)
+    c.prefill(to_dev(Q, w, shp), to_dev(K, w, shp), to_dev(V, w, shp))
+    assert c.decode_form_used() == ""
+    q, k, v = (to_dev(x, w, (w.T, w.B, w.H, w.d)) for x in synth.decode(w, 0, w.T))
+    before = c.export()
+    c.steps(q[:0], k[:0], v[:0])
+    after = c.export()
+    assert after["next_pos"] == before["next_pos"] and torch.equal(after["pos"], before["pos"])
+    assert c.decode_form_used() == ""
+    c.step(q[0], k[0], v[0])
+    assert c.decode_form_used() == "per_step"
+    c.set_decode_form("per_step")
+    c.steps(q[1:], k[1:], v[1:])
+    assert c.decode_form_used() == "per_step"
+    c2 = H2OCache(w.B, w.H, w.d, w.k_heavy, w.k_local, torch.bfloat16)
+    c2.prefill(to_dev(Q, w, shp), to_dev(K, w, shp), to_dev(V, w, shp))
+    c2.set_decode_form("cluster")
+    c2.steps(q, k, v)
+    assert c2.decode_form_used() == "cluster"
+    torch.cuda.synchronize()
+    c.check_device_error()
+    c2.check_device_error()

@@ -11,26 +11,33 @@
 // Scores, position tags and the step's logits of its slots live in the CTA's
 // shared memory for the whole launch (read at the start, written back at the
 // end); K/V rows are streamed from HBM each step (4 KB cp.async.bulk slabs in
-// a 3-stage ring fed by a producer warp) or, when a CTA's rows fit, loaded
-// once and kept in shared memory.  Per step:
-//   1. consumer warps: logits of the owned rows (and, on rank 0, of the new
-//      token), per-warp online softmax -> the CTA's (m, l, acc[d]);
-//   2. cluster barrier; every CTA reads all (m, l) over DSMEM -> global (M, L);
-//      rank 0 merges the acc[d] partials into the output row;
-//   3. every CTA turns its logits into exact weights exp2(s - M) / L, adds them
-//      to its scores and takes its local (score, position) argmin over
-//      eligible slots (warp shuffles); cluster barrier;
-//   4. rank 0 reduces the P candidates, decides (admit / evict / drop the new
-//      token) and publishes the decision; cluster barrier;
-//   5. the owner of the chosen slot writes the new token's K/V row (HBM, and
-//      its resident copy) and its position tag and score.
+// a 2- or 3-stage ring fed by a producer warp, which also issues the next
+// step's first slabs while the cluster exchanges partials) or, when a CTA's
+// rows fit and the grid is co-resident, loaded once and kept in shared
+// memory.  Per step:
+//   1. consumer warps: K dot products from packed q, a transposed reduction
+//      per lane group, per-warp online softmax -> the CTA's (m, l, acc[d])
+//      (rank 0 also takes the new token);
+//   2. each CTA pushes (m, l) (and rank 0 its new-token logit) to every rank
+//      and its acc row to rank 0 with st.async stores that complete on the
+//      receiver's mbarrier; every CTA derives the global (M, L), rank 0
+//      merges the acc rows into the output row;
+//   3. every CTA turns its logits into exact weights exp2(s - M) / L, adds
+//      them to its scores, takes its local (key, position) argmin over
+//      eligible slots and pushes it to every rank;
+//   4. every CTA reduces the P candidates to the same decision (admit /
+//      evict / drop the new token);
+//   5. the owner of the chosen slot writes the new token's K/V row (HBM, its
+//      resident copy, and the next step's slab if it was already loaded) and
+//      its position tag and score.
 // An fp8 cache (S = e4m3) streams 1-byte codes; the owned rows' K and V
 // scales stay in shared memory beside the scores, each logit is scaled by its
 // K scale and each V row weighted by its V scale, and the owner quantises the
 // new token's row (one scale per row) when it writes it.
-// All synchronisation is the cluster's hardware barrier or a CTA mbarrier
-// (bounded waits); there is no global atomic, fence round trip or spin between
-// CTAs, and clusters never wait on one another.
+// All synchronisation is a CTA barrier or an mbarrier (bounded waits; the
+// cluster barrier only at the start and the end); there is no global atomic,
+// fence round trip or spin between CTAs, and clusters never wait on one
+// another.
 #include <cooperative_groups.h>
 
 #include <climits>

@@ -326,7 +326,8 @@ def run_ours(args, w, rank, world, local_rank):
     }
 
     if not args.no_e2e:
-        line["e2e"] = e2e(args, w, dev, hQ, hK, hV, hq, hk, hv, tdt, stream, world, dist)
+        line["e2e"] = e2e(args, w, dev, hQ, hK, hV, hq, hk, hv, tdt, stream, world, dist,
+                          row_groups=args.e2e_row_groups, step_groups=args.e2e_step_groups)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args)
     if dist:
@@ -485,6 +486,8 @@ def main():
     ap.add_argument("--kv", choices=["native", "fp8"], default="native",
                     help="K/V cache storage: the workload's dtype, or e4m3 codes with a row scale (bf16 workloads)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-row-groups", type=int, default=4, help="prompt row groups copied/prefilled in turn")
+    ap.add_argument("--e2e-step-groups", type=int, default=4, help="decode step groups copied/decoded in turn")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -174,7 +174,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const Args a) {
         int issued = 0;
         for (; ok && issued < nst; ++issued) {
           const int gi = g + issued, st = gi % kStages;
-          if (gi >= kStages && !(ok = mbar_wait(&s_empty[st], ((gi / kStages) - 1) & 1))) break;
+          if (gi >= kStages && !(ok = mbar_wait_backoff(&s_empty[st], ((gi / kStages) - 1) & 1))) break;
           const uint32_t bytes = (uint32_t)(min(TR, nrows - issued * TR) * ROWB);
           mbar_expect_tx(&s_full[st], 2 * bytes);
           bulk_load(s_ring + st * 2 * kStageBytes, Kc + (size_t)issued * TR * ROWB, bytes, &s_full[st]);

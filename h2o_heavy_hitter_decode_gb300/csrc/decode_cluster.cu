@@ -205,7 +205,7 @@ __global__ void __launch_bounds__(kThreads, 7) decode_cluster_kernel(const CArgs
         bool ok = true;
         auto issue = [&](int i, int step_rows) -> bool {  // slab i of a step with `step_rows` owned rows
           const int st = gp % kStages;
-          if (gp >= kStages && !mbar_wait(&s_empty[st], ((gp / kStages) - 1) & 1)) return false;
+          if (gp >= kStages && !mbar_wait_backoff(&s_empty[st], ((gp / kStages) - 1) & 1)) return false;
           const uint32_t bytes = (uint32_t)(min(TR, step_rows - i * TR) * ROWB);
           const size_t off = (hk + s0 + (size_t)i * TR) * ROWB;
           mbar_expect_tx(&s_full[st], 2 * bytes);

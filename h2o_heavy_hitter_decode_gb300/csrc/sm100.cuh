@@ -55,6 +55,17 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
     if (mbar_try_wait(bar, parity)) return true;
   return false;
 }
+// The same wait with a short sleep between polls, for a thread whose wake-up
+// latency is hidden (a producer refilling a ring ahead of its consumers): it
+// then takes few issue slots from the warps doing the work.  False after
+// kSpinLimit polls (each followed by at most about 0.1 us of sleep).
+__device__ __forceinline__ bool mbar_wait_backoff(uint64_t *bar, uint32_t parity) {
+  for (uint32_t i = 0; i < kSpinLimit; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    __nanosleep(64);
+  }
+  return false;
+}
 
 // ------------------------------------------------------------------- copies
 // Make generic-proxy shared-memory writes visible to the async proxy (tensor

@@ -335,7 +335,7 @@ def run_ours(args, w, rank, world, local_rank):
     return line if rank == 0 else None
 
 
-def e2e(args, w, dev, hQ, hK, hV, hq, hk, hv, tdt, stream, world, dist, row_groups=4, step_groups=4):
+def e2e(args, w, dev, hQ, hK, hV, hq, hk, hv, tdt, stream, world, dist, row_groups=8, step_groups=4):
     """Same job from pinned host buffers: H2D of every input, prefill, decode,
     D2H of the decode outputs, all inside the timed events.  The prompt is
     copied on a side stream in `row_groups` groups of batch rows and each
@@ -486,7 +486,7 @@ def main():
     ap.add_argument("--kv", choices=["native", "fp8"], default="native",
                     help="K/V cache storage: the workload's dtype, or e4m3 codes with a row scale (bf16 workloads)")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--e2e-row-groups", type=int, default=4, help="prompt row groups copied/prefilled in turn")
+    ap.add_argument("--e2e-row-groups", type=int, default=8, help="prompt row groups copied/prefilled in turn")
     ap.add_argument("--e2e-step-groups", type=int, default=4, help="decode step groups copied/decoded in turn")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

@@ -306,6 +306,7 @@ def run_ours(args, w, rank, world, local_rank):
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": w.dtype, "impl": "ours",
+        "dtype_note": "stored K/V and tensor-core operands in this type; accumulation, softmax and scores in fp32",
         "data": "synthetic: seeded per-head generator (Pareto-shifted keys along a hidden direction)",
         "config": workload_config(w, {"decode_form": args.decode_form}),
         "decode": {"form": form, "tokens_per_s": w.B * world / (dec_launch_ms / 1e3), "us_per_step": dec_launch_ms * 1e3,

@@ -93,9 +93,9 @@ __global__ void __launch_bounds__(kThreads, 7) decode_cluster_kernel(const CArgs
   __shared__ __align__(16) T s_in[2][3][D];            // q, k_t, v_t of two steps
   __shared__ float s_wm[kConsumers], s_wl[kConsumers];
   __shared__ float s_wacc[kConsumers][D];
-  // Exchange buffers, filled by the peers' DSMEM stores (pushes) before a
-  // cluster barrier and read locally after it.
-  // Each completes one phase per step when its bytes have arrived.
+  // Exchange buffers, filled by the peers' asynchronous DSMEM stores
+  // (pushes), each tracked by an mbarrier of this CTA that completes one
+  // phase per step when its bytes have arrived; read locally after the wait.
   __shared__ __align__(8) uint64_t s_bml, s_bacc, s_bcand;
   // every rank's (m, l) (and rank 0's new-token logit), in every CTA
   __shared__ __align__(16) uint4 s_mlx[kMaxCluster];

@@ -47,8 +47,8 @@ bool decode_persistent_fits(const CacheView &c);
 cudaError_t launch_decode_persistent(const CacheView &c, const DecodeStep &s, int nsteps, int *done,
                                      cudaStream_t st);
 // Multi-step decode with one thread-block cluster per head (c.nsplit CTAs,
-// at most 8): scores/tags/logits in shared memory, DSMEM exchange, hardware
-// cluster barriers; no global scratch.
+// at most 8): scores/tags/logits in shared memory, DSMEM pushes completing on
+// the receivers' mbarriers; no global scratch.
 bool decode_cluster_supported(const CacheView &c);
 bool decode_cluster_resident(const CacheView &c);  // each CTA's K/V rows stay in shared memory
 // The cluster grid runs in one wave, or in enough waves that a partial last

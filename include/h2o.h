@@ -134,8 +134,10 @@ h2o_status h2o_decode_steps(h2o_cache_t cache, int n, const void *q, const void 
  *   2  one cooperative launch: each (head, split) CTA loops over the steps,
  *      waiting (bounded, acquire) only on its own head's previous step;
  *   3  one launch with a thread-block cluster of up to 8 CTAs per head:
- *      scores and tags stay in shared memory, partials and the eviction
- *      decision move over distributed shared memory, cluster barriers only.
+ *      scores and tags stay in shared memory, partials and eviction
+ *      candidates move over distributed shared memory (asynchronous stores
+ *      completing on the receivers' mbarriers), every CTA takes the same
+ *      decision; no global scratch.
  * A form the shape or device cannot run makes h2o_decode_steps return
  * H2O_EUNSUPPORTED (nothing launched). */
 h2o_status h2o_set_decode_form(h2o_cache_t cache, int form);

@@ -439,32 +439,35 @@ def oracle_job(w, data):
     return time.perf_counter() - t
 
 
+CPU_SAMPLE_HEADS = 256  # the whole default workload; seconds of work on a many-core host
+
+
 def cpu_baseline(w, args):
     import oracle
     cores = os.cpu_count() or 1
     oracle.set_threads(cores)
-    hs, data = oracle_sample(w, cores)
+    hs, data = oracle_sample(w, CPU_SAMPLE_HEADS)
     secs = oracle_job(w, data)
     scale = w.nh / len(hs)
     return {"value": w.B * w.T / (secs * scale), "unit": "tokens/s", "cores": int(oracle.max_threads()),
             "kind": "oracle",
             "sample": f"{len(hs)} of {w.nh} heads, full job (prefill L={w.L} + {w.T} decode steps), "
-                      f"{secs:.2f} s; rate extrapolated linearly to all heads"}
+                      f"{secs:.2f} s" + ("" if len(hs) == w.nh else "; rate extrapolated linearly to all heads")}
 
 
 def run_reference(args, w):
     import oracle
     cores = os.cpu_count() or 1
     oracle.set_threads(cores)
-    hs, data = oracle_sample(w, cores)
+    hs, data = oracle_sample(w, CPU_SAMPLE_HEADS)
     for _ in range(args.warmup):
         oracle_job(w, data)
     secs = [oracle_job(w, data) for _ in range(args.steps)]
     scale = w.nh / len(hs)
     per_job = float(np.mean(secs)) * scale
     value = w.B * w.T / per_job
-    sample = (f"each step: {len(hs)} of {w.nh} heads, full job (prefill L={w.L} + {w.T} decode steps); "
-              "rate extrapolated linearly to all heads")
+    sample = (f"each step: {len(hs)} of {w.nh} heads, full job (prefill L={w.L} + {w.T} decode steps)"
+              + ("" if len(hs) == w.nh else "; rate extrapolated linearly to all heads"))
     return {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": per_job * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "impl": "reference",

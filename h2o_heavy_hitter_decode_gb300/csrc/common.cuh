@@ -315,16 +315,23 @@ __device__ __forceinline__ bool am_less(const ArgMin &a, const ArgMin &b) {
   if (b.slot == -2) return true;
   return a.s < b.s || (a.s == b.s && a.p < b.p);
 }
+// Warp-wide am_less minimum, the same in every lane.  Candidate keys are
+// non-negative floats (sums of softmax weights, or those over a positive
+// count), whose bit patterns order like their values, and positions are
+// non-negative: two unsigned min-reductions give the lexicographic (key,
+// position) minimum ("none" entries carry all-ones bits and lose), a ballot
+// finds the lane holding it.
 __device__ __forceinline__ ArgMin warp_argmin(ArgMin a) {
-#pragma unroll
-  for (int o = 16; o; o >>= 1) {
-    ArgMin b;
-    b.s = __shfl_xor_sync(0xffffffffu, a.s, o);
-    b.p = __shfl_xor_sync(0xffffffffu, a.p, o);
-    b.slot = __shfl_xor_sync(0xffffffffu, a.slot, o);
-    if (am_less(b, a)) a = b;
-  }
-  return a;
+  const unsigned kb = (a.slot == -2) ? 0xFFFFFFFFu : __float_as_uint(a.s);
+  const unsigned kmin = __reduce_min_sync(0xffffffffu, kb);
+  const unsigned pb = (kb == kmin) ? (unsigned)a.p : 0xFFFFFFFFu;
+  const unsigned pmin = __reduce_min_sync(0xffffffffu, pb);
+  const int src = __ffs(__ballot_sync(0xffffffffu, kb == kmin && pb == pmin)) - 1;
+  ArgMin r;
+  r.s = __shfl_sync(0xffffffffu, a.s, src);
+  r.p = __shfl_sync(0xffffffffu, a.p, src);
+  r.slot = __shfl_sync(0xffffffffu, a.slot, src);
+  return r;
 }
 
 }  // namespace h2o

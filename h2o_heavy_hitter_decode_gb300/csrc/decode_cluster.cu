@@ -378,9 +378,14 @@ __global__ void __launch_bounds__(kThreads, 7) decode_cluster_kernel(const CArgs
         mr = __uint_as_float(s_mlx[lane].x);
         lr = __uint_as_float(s_mlx[lane].y);
       }
-      const float Mg = warp_max(mr);
+      // lanes 0..P-1 (P <= 8) hold values: three butterfly levels reduce them
+      float Mg = mr;
+#pragma unroll
+      for (int o = kMaxCluster / 2; o; o >>= 1) Mg = fmaxf(Mg, __shfl_xor_sync(0xffffffffu, Mg, o));
       const float fr = (mr == -INFINITY) ? 0.f : exp2f(mr - Mg);
-      const float Lg = warp_sum(fr * lr);
+      float Lg = fr * lr;
+#pragma unroll
+      for (int o = kMaxCluster / 2; o; o >>= 1) Lg += __shfl_xor_sync(0xffffffffu, Lg, o);
       if (lane < P) s_f[lane] = fr;
       if (lane == 0) {
         s_ML[0] = Mg;

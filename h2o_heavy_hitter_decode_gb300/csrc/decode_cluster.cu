@@ -20,8 +20,9 @@
 //      (rank 0 also takes the new token);
 //   2. each CTA pushes (m, l) (and rank 0 its new-token logit) to every rank
 //      and its acc row to rank 0 with st.async stores that complete on the
-//      receiver's mbarrier; every CTA derives the global (M, L), rank 0
-//      merges the acc rows into the output row;
+//      receiver's mbarrier; every CTA derives the global (M, L), and rank
+//      0's producer warp merges the acc rows into the output row while its
+//      consumer warps go on with step 3;
 //   3. every CTA turns its logits into exact weights exp2(s - M) / L, adds
 //      them to its scores, takes its local (key, position) argmin over
 //      eligible slots and pushes it to every rank;
@@ -52,22 +53,26 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kConsumers = 4;
-constexpr int kConsumerThreads = 32 * kConsumers;
-constexpr int kThreads = kConsumerThreads + 32;  // + one producer warp
+// Consumer warps per CTA (NC, a template argument): two when a CTA owns at
+// most kShortChunk slots — each warp takes more rows per slab (the per-slab
+// wait, reduction and arrive spread over more rows) and fewer warps run the
+// per-step code — and four for longer per-CTA streams, which need more loads
+// in flight per CTA (both measured on GB300).
+constexpr int kShortChunk = 256;
+constexpr int threads_for(int nc) { return 32 * nc + 32; }  // + one producer warp
 constexpr int kMaxCluster = 8;
 constexpr int kStageBytes = 4096;  // per operand per slab
 constexpr int ring_bytes(int stages) { return stages * 2 * kStageBytes; }
 constexpr int kResidentMaxBytes = 96 * 1024;  // K+V rows of one CTA kept in shared memory
 
-template <typename S, int D> struct Geo {
+template <typename S, int D, int NC> struct Geo {
   static constexpr int EPL = Lane<S>::VB / (int)sizeof(S);  // elements per lane per load
   static constexpr int LPR = D / EPL;
   static constexpr int RPW = 32 / LPR;
   static constexpr int ROWB = D * (int)sizeof(S);
   static constexpr int TR = kStageBytes / ROWB;  // rows per slab
-  static constexpr int ITER = TR / (kConsumers * RPW);
-  static_assert(ITER >= 1 && TR % (kConsumers * RPW) == 0, "slab must split evenly over warps");
+  static constexpr int ITER = TR / (NC * RPW);
+  static_assert(ITER >= 1 && TR % (NC * RPW) == 0, "slab must split evenly over warps");
 };
 
 struct CArgs {
@@ -78,12 +83,16 @@ struct CArgs {
   float qscale;  // log2(e) / sqrt(d)
 };
 
-__device__ __forceinline__ void consumers_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+template <int NC> __device__ __forceinline__ void consumers_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(32 * NC) : "memory");
+}
 
-// T: type of the step inputs and outputs; S: type of the stored K/V rows.
-template <typename T, typename S, int D, bool kResident, int kStages>
-__global__ void __launch_bounds__(kThreads, 7) decode_cluster_kernel(const CArgs a) {
-  using G = Geo<S, D>;
+// T: type of the step inputs and outputs; S: type of the stored K/V rows;
+// NC: consumer warps.
+template <typename T, typename S, int D, bool kResident, int kStages, int NC>
+__global__ void __launch_bounds__(threads_for(NC), 7) decode_cluster_kernel(const CArgs a) {
+  constexpr int kConsumers = NC, kConsumerThreads = 32 * NC, kThreads = threads_for(NC);
+  using G = Geo<S, D, NC>;
   constexpr bool kFp8 = is_fp8<S>();
   constexpr int EPL = G::EPL, LPR = G::LPR, RPW = G::RPW, ROWB = G::ROWB, TR = G::TR, ITER = G::ITER;
   cg::cluster_group cluster = cg::this_cluster();
@@ -344,7 +353,7 @@ __global__ void __launch_bounds__(kThreads, 7) decode_cluster_kernel(const CArgs
         s_wm[warp] = m;
         s_wl[warp] = l;
       }
-      consumers_sync();
+      consumers_sync<NC>();
       // merge the warps into this CTA's partial (published for rank 0)
       float M = s_wm[0];
 #pragma unroll
@@ -394,14 +403,25 @@ __global__ void __launch_bounds__(kThreads, 7) decode_cluster_kernel(const CArgs
     }
     __syncthreads();
     const float Mg = s_ML[0], invL = 1.f / s_ML[1];
-    if (rank == 0) {  // the step's output row
+    if (rank == 0 && warp == kConsumers) {
+      // the step's output row, by the producer warp while the consumers add
+      // the weights (off the path to the decision); its reads of the acc rows
+      // precede the CTA barrier below, so no peer can push next step's rows
+      // before they are done
       T *out = (T *)a.s.out + step * step_elems + (size_t)h * D;
-      for (int col = tid; col < D; col += kThreads) {
-        float o = 0.f;
-        for (int r = 0; r < P; ++r)
-          if (s_f[r] != 0.f) o = fmaf(s_f[r], accx[r * D + col], o);
-        out[col] = from_f32<T>(o * invL);
+      constexpr int CPL = D / 32;
+      float o[CPL];
+#pragma unroll
+      for (int q = 0; q < CPL; ++q) o[q] = 0.f;
+      for (int r = 0; r < P; ++r) {
+        const float fr = s_f[r];
+        if (fr != 0.f) {
+#pragma unroll
+          for (int q = 0; q < CPL; ++q) o[q] = fmaf(fr, accx[r * D + lane * CPL + q], o[q]);
+        }
       }
+#pragma unroll
+      for (int q = 0; q < CPL; ++q) out[lane * CPL + q] = from_f32<T>(o[q] * invL);
     }
 
     // ---- exact weights into the owned scores; local argmin
@@ -539,34 +559,38 @@ __global__ void __launch_bounds__(kThreads, 7) decode_cluster_kernel(const CArgs
 // for an fp8 cache).
 template <typename S> constexpr int slot_words() { return is_fp8<S>() ? 5 : 3; }
 
+template <typename S, int D> constexpr int row_bytes() { return D * (int)sizeof(S); }
+
 template <typename S, int D>
 int resident_rows_ok(int chunk) {
-  return 2 * chunk * Geo<S, D>::ROWB <= kResidentMaxBytes;
+  return 2 * chunk * row_bytes<S, D>() <= kResidentMaxBytes;
 }
 
 template <typename S, int D, bool R, int St>
 int smem_bytes(int chunk, int P) {
-  const int base = (R ? 2 * chunk * Geo<S, D>::ROWB : ring_bytes(St)) + slot_words<S>() * chunk * 4;
+  const int base = (R ? 2 * chunk * row_bytes<S, D>() : ring_bytes(St)) + slot_words<S>() * chunk * 4;
   return ((base + 15) & ~15) + P * D * 4;  // + every rank's acc row
 }
 
-template <typename T, typename S, int D, bool R, int St>
+int chunk_of(const CacheView &c) { return (c.k + c.nsplit - 1) / c.nsplit; }
+
+template <typename T, typename S, int D, bool R, int St, int NC>
 cudaError_t launch_cluster_t(const CacheView &c, const DecodeStep &s, int nsteps, cudaStream_t st) {
   const int P = c.nsplit;
-  CArgs a{c, s, nsteps, (c.k + P - 1) / P, kLog2e / sqrtf((float)D)};
+  CArgs a{c, s, nsteps, chunk_of(c), kLog2e / sqrtf((float)D)};
   const int smem = smem_bytes<S, D, R, St>(a.chunk, P);
   if (smem > 200 * 1024) return cudaErrorInvalidValue;
   static bool attr_done[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 || !attr_done[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(decode_cluster_kernel<T, S, D, R, St>,
+    cudaError_t e = cudaFuncSetAttribute(decode_cluster_kernel<T, S, D, R, St, NC>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_done[dev] = true;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(c.nh * P));
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(threads_for(NC));
   cfg.dynamicSmemBytes = (size_t)smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
@@ -576,59 +600,78 @@ cudaError_t launch_cluster_t(const CacheView &c, const DecodeStep &s, int nsteps
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_cluster_kernel<T, S, D, R, St>, a);
+  return cudaLaunchKernelEx(&cfg, decode_cluster_kernel<T, S, D, R, St, NC>, a);
 }
 
-template <typename T, typename S, int D, bool R, int St>
-bool all_resident(const CacheView &c, int chunk) {
+// CTAs of this instance that fit on the device at once (0 on an error).
+template <typename T, typename S, int D, bool R, int St, int NC>
+long long resident_ctas(const CacheView &c, int chunk) {
   int dev = 0, sms = 0, per_sm = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return false;
-  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
   const int smem = smem_bytes<S, D, R, St>(chunk, c.nsplit);
-  if (smem > 200 * 1024) return false;
-  if (cudaFuncSetAttribute(decode_cluster_kernel<T, S, D, R, St>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (smem > 200 * 1024) return 0;
+  if (cudaFuncSetAttribute(decode_cluster_kernel<T, S, D, R, St, NC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            200 * 1024) != cudaSuccess)
-    return false;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_cluster_kernel<T, S, D, R, St>, kThreads,
-                                                    smem) != cudaSuccess)
-    return false;
-  return (long long)c.nh * c.nsplit <= (long long)per_sm * sms;
+    return 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_cluster_kernel<T, S, D, R, St, NC>,
+                                                    threads_for(NC), smem) != cudaSuccess)
+    return 0;
+  return (long long)per_sm * sms;
+}
+
+template <typename T, typename S, int D, bool R, int St, int NC>
+bool all_resident(const CacheView &c, int chunk) {
+  const long long fit = resident_ctas<T, S, D, R, St, NC>(c, chunk);
+  return fit > 0 && (long long)c.nh * c.nsplit <= fit;
 }
 
 // K/V resident in shared memory when a CTA's rows fit AND every CTA of the
 // grid is resident at once (each CTA runs all steps of its head, so a second
 // wave would start only when the first finished).
-template <typename T, typename S, int D>
-bool resident_t(const CacheView &c) {
-  const int chunk = (c.k + c.nsplit - 1) / c.nsplit;
-  return resident_rows_ok<S, D>(chunk) && all_resident<T, S, D, true, 1>(c, chunk);
+template <typename T, typename S, int D, int NC>
+bool resident_nc(const CacheView &c) {
+  const int chunk = chunk_of(c);
+  return resident_rows_ok<S, D>(chunk) && all_resident<T, S, D, true, 1, NC>(c, chunk);
 }
 
 // Streaming: a 3-stage ring, unless two stages are what lets every CTA be
 // resident at once (a partial last wave of whole-run CTAs streams at a
 // fraction of the bandwidth).
+template <typename T, typename S, int D, int NC>
+cudaError_t dispatch_nc(const CacheView &c, const DecodeStep &s, int nsteps, cudaStream_t st) {
+  const int chunk = chunk_of(c);
+  if (resident_nc<T, S, D, NC>(c)) return launch_cluster_t<T, S, D, true, 1, NC>(c, s, nsteps, st);
+  if (!all_resident<T, S, D, false, 3, NC>(c, chunk) && all_resident<T, S, D, false, 2, NC>(c, chunk))
+    return launch_cluster_t<T, S, D, false, 2, NC>(c, s, nsteps, st);
+  return launch_cluster_t<T, S, D, false, 3, NC>(c, s, nsteps, st);
+}
+
+template <typename T, typename S, int D, int NC>
+bool waves_ok_nc(const CacheView &c) {
+  const int chunk = chunk_of(c);
+  if (resident_nc<T, S, D, NC>(c) || all_resident<T, S, D, false, 3, NC>(c, chunk) ||
+      all_resident<T, S, D, false, 2, NC>(c, chunk))
+    return true;
+  const long long fit = resident_ctas<T, S, D, false, 3, NC>(c, chunk);
+  return fit > 0 && (long long)c.nh * c.nsplit >= 3 * fit;
+}
+
+// The consumer-warp count for a CTA that owns chunk_of(c) slots.
+template <typename T, typename S, int D>
+bool resident_t(const CacheView &c) {
+  return chunk_of(c) > kShortChunk ? resident_nc<T, S, D, 4>(c) : resident_nc<T, S, D, 2>(c);
+}
+
 template <typename T, typename S, int D>
 cudaError_t dispatch_t(const CacheView &c, const DecodeStep &s, int nsteps, cudaStream_t st) {
-  const int chunk = (c.k + c.nsplit - 1) / c.nsplit;
-  if (resident_t<T, S, D>(c)) return launch_cluster_t<T, S, D, true, 1>(c, s, nsteps, st);
-  if (!all_resident<T, S, D, false, 3>(c, chunk) && all_resident<T, S, D, false, 2>(c, chunk))
-    return launch_cluster_t<T, S, D, false, 2>(c, s, nsteps, st);
-  return launch_cluster_t<T, S, D, false, 3>(c, s, nsteps, st);
+  return chunk_of(c) > kShortChunk ? dispatch_nc<T, S, D, 4>(c, s, nsteps, st)
+                                   : dispatch_nc<T, S, D, 2>(c, s, nsteps, st);
 }
 
 template <typename T, typename S, int D>
 bool cluster_waves_ok_t(const CacheView &c) {
-  const int chunk = (c.k + c.nsplit - 1) / c.nsplit;
-  if (resident_t<T, S, D>(c) || all_resident<T, S, D, false, 3>(c, chunk) ||
-      all_resident<T, S, D, false, 2>(c, chunk))
-    return true;
-  int dev = 0, sms = 0, per_sm = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_cluster_kernel<T, S, D, false, 3>, kThreads,
-                                                    smem_bytes<S, D, false, 3>(chunk, c.nsplit)) != cudaSuccess)
-    return false;
-  return (long long)c.nh * c.nsplit >= 3LL * per_sm * sms;
+  return chunk_of(c) > kShortChunk ? waves_ok_nc<T, S, D, 4>(c) : waves_ok_nc<T, S, D, 2>(c);
 }
 
 #define H2O_CLUSTER_DISPATCH(FN, ...)                                              \

@@ -289,7 +289,11 @@ def run_ours(args, w, rank, world, local_rank):
         roof = {"kernel": dec_kernel, "decode_form": form, "bound": "hbm", "achieved": dec_alg_gbs,
                 "peak": pk["hbm_gbs"], "unit": "GB/s", "traffic": traffic_for(dec_kernel, w),
                 "per": "decode step (algorithmic bytes and DRAM traffic per step)",
-                "algorithmic_bytes_per_launch": decode_alg_bytes(w), "avg_launch_ms": dec_launch_ms}
+                "algorithmic_bytes_per_launch": decode_alg_bytes(w), "avg_launch_ms": dec_launch_ms,
+                "cache_in_l2": kv_read_bytes(w) < 120e6}
+        if roof["cache_in_l2"]:
+            roof["note"] = ("the K/V cache fits in L2 and stays there across steps, so the steps read it from L2 "
+                            "(see traffic: DRAM bytes per step); the fraction is of the HBM copy bandwidth")
     elif top == "prefill_colsum":
         roof = {"kernel": "prefill_colsum", "bound": "tensor", "achieved": cs_tf, "peak": pk["bf16_tflops"],
                 "unit": "TFLOP/s", "traffic": traffic_for("prefill_colsum", w),

@@ -48,6 +48,19 @@ def test_fp8_with_policy(form):
     assert rep.steps_compared >= w.T
 
 
+@pytest.mark.parametrize("w", [small("fp8_cluster_long_chunks_resident", 1, 2, 128, 2600, 24, 1300, 1100),
+                               small("fp8_d64_cluster_long_chunks_resident", 1, 2, 64, 2500, 24, 1200, 1200)],
+                         ids=lambda w: w.name)
+def test_fp8_cluster_long_chunks(w):
+    """300 fp8 slots per cluster CTA: their rows (77 KB or 38 KB of codes) stay
+    resident in shared memory and four consumer warps read them."""
+    rep, cache = run_parity(w, decode_form="cluster", kv_fp8=True)
+    print(w.name, rep)
+    assert cache.decode_form_used() == "cluster"
+    assert -(-w.k // min(cache.info()["n_split"], 8)) > 256  # slots per CTA
+    assert rep.steps_compared >= w.T
+
+
 def _sample(w, count, seed=5):
     rng = np.random.default_rng(seed)
     return sorted(rng.choice(w.nh, size=min(count, w.nh), replace=False).tolist())

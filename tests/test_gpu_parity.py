@@ -75,6 +75,27 @@ def test_decode_forms(w, form):
     assert rep.steps_compared >= w.T
 
 
+# Budgets of 2400 slots over few heads: the cluster form splits each head over
+# 8 CTAs of 300 slots, more than the 256 above which a CTA runs four consumer
+# warps instead of two (streamed rows for bf16 and fp32).  In the last case the
+# prompt is shorter than the budget, so most CTAs own no filled slot for the
+# whole run.
+LONG_CHUNKS = [
+    small("bf16_cluster_long_chunks", 1, 2, 128, 2600, 24, 1300, 1100, "bf16"),
+    small("f32_d64_cluster_long_chunks", 1, 2, 64, 2500, 24, 1200, 1200, "f32"),
+    small("bf16_d64_cluster_long_chunks_short_prompt", 1, 3, 64, 700, 40, 1400, 1000, "bf16"),
+]
+
+
+@pytest.mark.parametrize("w", LONG_CHUNKS, ids=lambda w: w.name)
+def test_cluster_long_chunks(w):
+    rep, cache = run_parity(w, decode_form="cluster")
+    print(w.name, rep)
+    assert cache.decode_form_used() == "cluster"
+    assert -(-w.k // min(cache.info()["n_split"], 8)) > 256  # slots per CTA
+    assert rep.steps_compared >= w.T
+
+
 def _sample(w, count, seed=5):
     rng = np.random.default_rng(seed)
     return sorted(rng.choice(w.nh, size=min(count, w.nh), replace=False).tolist())

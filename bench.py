@@ -88,6 +88,14 @@ def attn_pass_flops(w):
     return 2 * score_pass_flops(w)
 
 
+def causal_exps(w):
+    """One exponential per causal (query, key) pair in each prefill pass."""
+    return w.nh * w.L * (w.L + 1) // 2
+
+
+EX2_PER_CLK_PER_SM = 32  # ex2.approx.f32 issue rate, measured on GB300 with a register-resident loop
+
+
 def workload_config(w, extra=None):
     c = {"workload": w.name, "B": w.B, "H": w.H, "d": w.d, "prompt_L": w.L, "decode_T": w.T,
          "k_heavy": w.k_heavy, "k_local": w.k_local,
@@ -283,6 +291,13 @@ def run_ours(args, w, rank, world, local_rank):
     cs_tf = score_pass_flops(w) / (cs_ms / 1e3) / 1e12
     at_tf = attn_pass_flops(w) / (at_ms / 1e3) / 1e12
 
+    clk_sum = clk.summary()
+    sm_mhz = clk_sum.get("sm_mhz") or clk_sum.get("sm_max_mhz")
+    n_sms = torch.cuda.get_device_properties(dev).multi_processor_count
+
+    def exp_rate(ms):  # exponentials per SM clock per SM over the pass
+        return causal_exps(w) / (ms / 1e3 * sm_mhz * 1e6 * n_sms) if sm_mhz else None
+
     shares = {"decode": dec_ms, "prefill_colsum": cs_ms, "prefill_attn": at_ms, "prefill_select": sel_ms}
     top = max(shares, key=shares.get)
     if top == "decode":
@@ -320,13 +335,15 @@ def run_ours(args, w, rank, world, local_rank):
                    "cache_bytes": kv_read_bytes(w), "l2_resident": kv_read_bytes(w) < 120e6},
         "prefill": {"score_pass_tflops": cs_tf, "score_pass_frac_measured_bf16": cs_tf / pk["bf16_tflops"],
                     "attn_pass_tflops": at_tf, "attn_pass_frac_measured_bf16": at_tf / pk["bf16_tflops"],
-                    "ms": {"attn": at_ms, "colsum": cs_ms, "select_gather": sel_ms}},
+                    "ms": {"attn": at_ms, "colsum": cs_ms, "select_gather": sel_ms},
+                    "exp_per_clk_per_sm": {"score_pass": exp_rate(cs_ms), "attn_pass": exp_rate(at_ms),
+                                           "ex2_unit": EX2_PER_CLK_PER_SM, "sm_mhz": sm_mhz, "sms": n_sms}},
         "phase_ms_per_step": shares,
         "roofline": roof,
         "gpu_launches": int(phases["prefill_attn"][1] + phases["prefill_colsum"][1] + phases["prefill_select"][1]
                             + phases["decode"][1]),
         "wall_s_timed": t_wall,
-        "clocks": clk.summary(),
+        "clocks": clk_sum,
         "peaks": {**pk, "source": pk_src},
     }
 

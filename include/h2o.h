@@ -118,8 +118,8 @@ h2o_status h2o_prefill_rows(h2o_cache_t cache, int b0, int nb, const void *Q, co
 h2o_status h2o_decode_step(h2o_cache_t cache, const void *q_t, const void *k_t, const void *v_t,
                            void *out);
 
-/* n decode steps in sequence (n launches on the stream, or one persistent
- * launch for small B*H), inputs [n][B][H][d], out [n][B][H][d].
+/* n decode steps in sequence (one launch per step, or one launch for all of
+ * them: see h2o_set_decode_form), inputs [n][B][H][d], out [n][B][H][d].
  * evicted: device [n][B][H] int32 or NULL; receives the position evicted at
  * each step (-1 when the new token was admitted without eviction; the new
  * position itself when it was the lowest-scoring candidate, which can only
@@ -129,7 +129,9 @@ h2o_status h2o_decode_steps(h2o_cache_t cache, int n, const void *q, const void 
 
 /* How h2o_decode_steps runs n >= 2 steps (all forms compute the same thing;
  * single steps always use form 1):
- *   0  automatic (default): 3 if the shape allows it, else 2, else 1;
+ *   0  automatic (default): 3 when its grid of clusters runs in one wave of
+ *      co-resident CTAs or in at least three waves, else 2 when all its
+ *      CTAs fit on the device at once, else 3 if the shape allows it, else 1;
  *   1  one launch per step, chained with programmatic dependent launch;
  *   2  one cooperative launch: each (head, split) CTA loops over the steps,
  *      waiting (bounded, acquire) only on its own head's previous step;

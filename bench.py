@@ -452,12 +452,14 @@ def oracle_sample(w, n_heads):
 
 
 def oracle_job(w, data):
+    """Wall-clock seconds of one oracle job on the sample: (prefill, decode)."""
     import oracle
     Q, K, V, q, k, v = data
-    t = time.perf_counter()
+    t0 = time.perf_counter()
     r = oracle.prefill(Q, K, V, w.k_heavy, w.k_local, kv_fp8=is_kvfp8(w))
+    t1 = time.perf_counter()
     oracle.decode(r["state"], w.L, q, k, v, w.k_heavy, w.k_local, kv_fp8=is_kvfp8(w))
-    return time.perf_counter() - t
+    return t1 - t0, time.perf_counter() - t1
 
 
 CPU_SAMPLE_HEADS = 256  # the whole default workload; seconds of work on a many-core host
@@ -468,10 +470,11 @@ def cpu_baseline(w, args):
     cores = os.cpu_count() or 1
     oracle.set_threads(cores)
     hs, data = oracle_sample(w, CPU_SAMPLE_HEADS)
-    secs = oracle_job(w, data)
+    pre, dec = oracle_job(w, data)
+    secs = pre + dec
     scale = w.nh / len(hs)
     return {"value": w.B * w.T / (secs * scale), "unit": "tokens/s", "cores": int(oracle.max_threads()),
-            "kind": "oracle",
+            "kind": "oracle", "phases_s": {"prefill": pre, "decode": dec},
             "sample": f"{len(hs)} of {w.nh} heads, full job (prefill L={w.L} + {w.T} decode steps), "
                       f"{secs:.2f} s" + ("" if len(hs) == w.nh else "; rate extrapolated linearly to all heads")}
 
@@ -483,9 +486,9 @@ def run_reference(args, w):
     hs, data = oracle_sample(w, CPU_SAMPLE_HEADS)
     for _ in range(args.warmup):
         oracle_job(w, data)
-    secs = [oracle_job(w, data) for _ in range(args.steps)]
+    phases = np.array([oracle_job(w, data) for _ in range(args.steps)])
     scale = w.nh / len(hs)
-    per_job = float(np.mean(secs)) * scale
+    per_job = float(np.mean(phases.sum(axis=1))) * scale
     value = w.B * w.T / per_job
     sample = (f"each step: {len(hs)} of {w.nh} heads, full job (prefill L={w.L} + {w.T} decode steps)"
               + ("" if len(hs) == w.nh else "; rate extrapolated linearly to all heads"))
@@ -494,7 +497,9 @@ def run_reference(args, w):
             "vs_baseline": None, "dtype": "f64", "impl": "reference",
             "data": "synthetic: seeded per-head generator", "config": workload_config(w),
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": int(oracle.max_threads()),
-                             "kind": "oracle", "sample": sample},
+                             "kind": "oracle", "sample": sample,
+                             "phases_s": {"prefill": float(np.mean(phases[:, 0])),
+                                          "decode": float(np.mean(phases[:, 1]))}},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 

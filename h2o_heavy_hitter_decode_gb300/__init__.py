@@ -18,7 +18,7 @@ import re
 
 import torch
 
-__all__ = ["H2OCache", "H2OError", "lib", "LIB_PATH", "HEADER_PATH", "declared_functions"]
+__all__ = ["H2OCache", "H2OError", "lib", "LIB_PATH", "HEADER_PATH", "declared_functions", "kernel_arch"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libh2o.so")
@@ -81,6 +81,8 @@ def lib():
         L.h2o_status_str.restype = C.c_char_p
         L.h2o_last_cuda_error.restype = i32
         L.h2o_build_arch.restype = i32
+        L.h2o_kernel_arch.argtypes = [C.POINTER(i32), C.POINTER(i32)]
+        L.h2o_kernel_arch.restype = i32
         for f in ("h2o_cache_create", "h2o_cache_destroy", "h2o_set_stream", "h2o_prefill", "h2o_prefill_rows",
                   "h2o_decode_step",
                   "h2o_decode_steps", "h2o_cache_export", "h2o_cache_import", "h2o_cache_info",
@@ -90,6 +92,14 @@ def lib():
             getattr(L, f).restype = i32
         _lib = L
     return _lib
+
+
+def kernel_arch():
+    """(ptx_version, binary_version) of the library's kernels as loaded on
+    the current device (103, 103 for the sm_103a build)."""
+    ptx, binv = C.c_int32(), C.c_int32()
+    _check(lib().h2o_kernel_arch(C.byref(ptx), C.byref(binv)), "h2o_kernel_arch")
+    return ptx.value, binv.value
 
 
 def _check(rc: int, what: str):

@@ -533,4 +533,13 @@ int h2o_last_cuda_error(void) { return g_last_cuda; }
 
 int h2o_build_arch(void) { return 1030; }
 
+h2o_status h2o_kernel_arch(int *ptx_version, int *binary_version) {
+  cudaFuncAttributes a;
+  const cudaError_t e = kernel_attributes(&a);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (ptx_version) *ptx_version = a.ptxVersion;
+  if (binary_version) *binary_version = a.binaryVersion;
+  return H2O_OK;
+}
+
 }  // extern "C"

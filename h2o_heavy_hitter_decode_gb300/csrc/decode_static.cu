@@ -5,6 +5,8 @@
 // kernel is the regular decode kernel (decode.cu); only where its scratch
 // lives differs.  Nothing here calls cudaMalloc, cudaFree or any allocating
 // library routine.
+#include <cuda.h>
+
 #include <mutex>
 
 #include "../../include/h2o.h"
@@ -23,6 +25,28 @@ static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
 
 std::mutex g_setup_mu;
 void *g_scratch_addr[kMaxDevices];  // device address of g_scratch, per device
+CUcontext g_scratch_ctx[kMaxDevices];  // the context that address belongs to
+
+// The calling thread's current context (null if it cannot be read): the
+// array's address is looked up again when a device is used under another
+// context than the one it was looked up in (each context loads the library's
+// module separately).
+CUcontext current_context() {
+  using Fn = CUresult (*)(CUcontext *);
+  static Fn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {  // under g_setup_mu
+    tried = true;
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (Fn)p;
+  }
+  CUcontext ctx = nullptr;
+  if (!fn || fn(&ctx) != CUDA_SUCCESS) return nullptr;
+  return ctx;
+}
 
 size_t up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
 
@@ -66,10 +90,13 @@ extern "C" h2o_status h2o_decode_step_static(int B, int H, int d, int k_heavy, i
   void *base = nullptr;
   {
     std::lock_guard<std::mutex> lock(g_setup_mu);
-    if (!g_scratch_addr[dev]) {
+    // cudaGetDevice above made the runtime's context for `dev` current.
+    const CUcontext ctx = current_context();
+    if (!g_scratch_addr[dev] || ctx != g_scratch_ctx[dev]) {
       void *p = nullptr;
       if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess || !p) return H2O_ECUDA;
       g_scratch_addr[dev] = p;
+      g_scratch_ctx[dev] = ctx;
     }
     base = g_scratch_addr[dev];
   }

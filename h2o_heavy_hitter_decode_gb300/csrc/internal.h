@@ -70,4 +70,7 @@ cudaError_t launch_prefill_select(const CacheView &c, const void *K, const void 
 
 int num_sms_current_device();
 
+// cudaFuncGetAttributes of a library kernel on the current device.
+cudaError_t kernel_attributes(cudaFuncAttributes *a);
+
 }  // namespace h2o

@@ -191,6 +191,12 @@ cudaError_t select_t(const CacheView &c, const void *K, const void *V, const flo
 
 }  // namespace
 
+// Attributes of one kernel of this library as the runtime loaded it on the
+// current device (binaryVersion 103 = an sm_103 cubin, not JIT-compiled PTX).
+cudaError_t kernel_attributes(cudaFuncAttributes *a) {
+  return cudaFuncGetAttributes(a, select_gather<__nv_bfloat16, __nv_bfloat16, 128>);
+}
+
 cudaError_t launch_prefill_select(const CacheView &c, const void *K, const void *V, const float *colsum,
                                   int L, cudaStream_t st) {
   if (c.dtype == 1 && c.kv_fp8) {

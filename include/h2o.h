@@ -240,6 +240,11 @@ h2o_status h2o_profile_read(h2o_cache_t cache, double *ms, int64_t *launches);
  * and must be serialised by the caller.  The first call on a device looks up
  * the array's device address (cudaGetSymbolAddress, with that device
  * current); make that first call before any stream capture on that device.
+ * The address is kept per device together with the context it was looked up
+ * in, and looked up again when the calling thread runs that device under
+ * another context.  A cudaDeviceReset of the device can reload the library's
+ * module at another address under the same primary-context handle, so this
+ * entry point is not supported on a device after it has been reset.
  * A CUDA failure returns H2O_ECUDA; the kernel's own consistency flag lives
  * in the shared scratch and is not reported here. */
 #define H2O_STATIC_SCRATCH_BYTES (16u << 20)
@@ -260,6 +265,13 @@ int h2o_last_cuda_error(void);
 
 /* Compiled-in target, for checks: returns 1030 for sm_103a. */
 int h2o_build_arch(void);
+
+/* What the CUDA runtime loaded on the current device for this library's
+ * kernels (cudaFuncGetAttributes of one of them): the PTX ISA target and the
+ * binary architecture, major*10 + minor (103 and 103 for an sm_103a build
+ * running as its own cubin).  Host pointers, either may be NULL.
+ * H2O_ECUDA without a usable device. */
+h2o_status h2o_kernel_arch(int *ptx_version, int *binary_version);
 
 #ifdef __cplusplus
 }

@@ -194,3 +194,59 @@ def as_f64(x: np.ndarray, dtype: str) -> np.ndarray:
     if dtype == "bf16":
         return bf16_bits_to_f32(x).astype(np.float64)
     return np.asarray(x, dtype=np.float32).astype(np.float64)
+
+
+# ------------------------------------------------------------- exact ties
+# A second recipe, for parity cases whose eviction and selection decisions
+# are exact ties in fp32 as well as in fp64.  Every query is q = 8 e_0.  A
+# "live" key has e_0 component 0 (its logit is exactly 0 under any rounding);
+# a "dead" key has e_0 component -2048 (logit -2048 at d = 64, -1448 at
+# d = 128), so its softmax weight underflows to exactly 0 next to any live
+# key and its accumulated score stays exactly 0.  Dead entries therefore tie
+# at score 0 and only the tie rule separates them.  Position 0 is always
+# live, so every query attends to at least one live key.  The other
+# components of keys, and all values, are N(0, 1).
+TIE_Q = 8.0
+TIE_DEAD = -2048.0
+TIE_STREAM = 1 << 30
+
+
+def _tie_rows(w: Workload, b: int, h: int, segment: int, first_pos: int, n: int, dead_frac: float):
+    rng = np.random.default_rng([w.seed, b, h, TIE_STREAM, segment])  # apart from the main recipe's streams
+    k = rng.standard_normal((n, w.d), dtype=np.float32)
+    v = rng.standard_normal((n, w.d), dtype=np.float32)
+    dead = rng.random(n) < dead_frac
+    if first_pos == 0:
+        dead[0] = False
+    k[:, 0] = np.where(dead, np.float32(TIE_DEAD), np.float32(0.0))
+    q = np.zeros((n, w.d), np.float32)
+    q[:, 0] = TIE_Q
+    return q, k, v
+
+
+def tie_prompt(w: Workload, dead_frac: float, heads=None):
+    """Prompt Q, K, V of the exact-tie recipe, like prompt()."""
+    hs = _heads(w, heads)
+    st = np.uint16 if w.dtype == "bf16" else np.float32
+    Q = np.empty((len(hs), w.L, w.d), st)
+    K = np.empty_like(Q)
+    V = np.empty_like(Q)
+    for i, f in enumerate(hs):
+        b, h = divmod(f, w.H)
+        q, k, v = _tie_rows(w, b, h, 0, 0, w.L, dead_frac)
+        Q[i], K[i], V[i] = _store(q, w.dtype), _store(k, w.dtype), _store(v, w.dtype)
+    return Q, K, V
+
+
+def tie_decode(w: Workload, dead_frac: float, heads=None):
+    """Decode inputs of all w.T steps of the exact-tie recipe, like decode()."""
+    hs = _heads(w, heads)
+    st = np.uint16 if w.dtype == "bf16" else np.float32
+    q = np.empty((w.T, len(hs), w.d), st)
+    k = np.empty_like(q)
+    v = np.empty_like(q)
+    for i, f in enumerate(hs):
+        b, h = divmod(f, w.H)
+        qq, kk, vv = _tie_rows(w, b, h, 1, w.L, w.T, dead_frac)
+        q[:, i], k[:, i], v[:, i] = _store(qq, w.dtype), _store(kk, w.dtype), _store(vv, w.dtype)
+    return q, k, v

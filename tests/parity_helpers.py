@@ -5,9 +5,12 @@ Tolerances (fixed by the method's acceptance rules):
   * cache sets: bit-exact; a mismatch is permitted only where the oracle's
     eviction margin (gap between the two lowest candidate ranking keys; for
     prefill the gap between the smallest kept and largest dropped key; the
-    key is the score, or the mean weight under score_mode 1) is at or
-    below 1e-5, and it is then counted, the GPU is resynchronised from the
-    oracle's state through h2o_cache_import, and the run continues;
+    key is the score, or the mean weight under score_mode 1) is above 0 and
+    at or below 1e-5, and it is then counted, the GPU is resynchronised from
+    the oracle's state through h2o_cache_import, and the run continues.  At
+    a margin of exactly 0 the tie rule (eviction: lowest position; prefill:
+    the higher positions survive) makes the answer unique, so a mismatch
+    there fails; such exact ties are counted (Report.ties_*);
   * attention outputs: max abs error <= 1e-4 (fp32 cache) or 2e-2 (bf16);
   * scores and column sums: relative error <= 1e-3;
   * lse: abs error <= 1e-4 (fp32 output in both cases);
@@ -71,6 +74,14 @@ class Report:
     max_score_rel: float = 0.0
     steps_compared: int = 0
     heads_compared: int = 0
+    ties_prefill: int = 0  # heads whose prefill selection was an exact tie (oracle margin 0)
+    ties_decode: int = 0   # (head, step) evictions that were exact ties, among the compared ones
+
+
+def permitted(margin) -> bool:
+    """A set mismatch is allowed only at a near-tie: 0 < margin <= 1e-5."""
+    m = np.asarray(margin, dtype=np.float64)
+    return bool(np.all((m > 0.0) & (m <= MARGIN_TOL)))
 
 
 def _rel(a, b):
@@ -171,11 +182,12 @@ def run_parity(w, T=None, heads=None, resync=True, check=True, prompt=None, dec=
     o_sets = st0.sets()
     bad = [i for i, h in enumerate(hs) if not np.array_equal(np.sort(g_pos[h][g_pos[h] >= 0]), o_sets[i])]
     rep.min_margin_seen = min(rep.min_margin_seen, float(np.min(r["margin"])))
+    rep.ties_prefill = int(np.sum(r["margin"] == 0.0))
     if bad:
         rep.set_mismatch_prefill = len(bad)
         rep.max_margin_at_mismatch = max(rep.max_margin_at_mismatch, float(np.max(r["margin"][bad])))
         if check:
-            assert np.all(r["margin"][bad] <= MARGIN_TOL), (bad, r["margin"][bad])
+            assert permitted(r["margin"][bad]), (bad, r["margin"][bad])
         if resync:
             import_oracle_state(cache, st0, w, w.L)
             rep.resyncs += 1
@@ -210,6 +222,7 @@ def run_parity(w, T=None, heads=None, resync=True, check=True, prompt=None, dec=
         finite = o_mg[:, alive][np.isfinite(o_mg[:, alive])]
         if finite.size:
             rep.min_margin_seen = min(rep.min_margin_seen, float(finite.min()))
+        zero = (o_mg == 0.0)  # exact ties of this chunk (counted where compared)
         qd = to_dev(qs, w, (n, w.B, w.H, w.d))
         kd = to_dev(ks, w, (n, w.B, w.H, w.d))
         vd = to_dev(vs, w, (n, w.B, w.H, w.d))
@@ -226,18 +239,20 @@ def run_parity(w, T=None, heads=None, resync=True, check=True, prompt=None, dec=
                     f = int(np.argmax(diff[:, i])) if diff[:, i].any() else m
                     upto = min(f + 1, m)
                     rep.max_out_err = max(rep.max_out_err, float(np.abs(g_out[:upto, i] - o_out[t:t + upto, i]).max()))
+                    rep.ties_decode += int(np.sum(zero[t:t + upto, i]))
                     if f < m:
                         alive[i] = False
                         rep.set_mismatch_decode += 1
                         rep.max_margin_at_mismatch = max(rep.max_margin_at_mismatch, float(o_mg[t + f, i]))
                         if check:
-                            assert o_mg[t + f, i] <= MARGIN_TOL, (t0 + t + f, hs[i], o_mg[t + f, i])
+                            assert permitted(o_mg[t + f, i]), (t0 + t + f, hs[i], o_mg[t + f, i])
                 rep.steps_compared += m
                 break
             first = int(np.argmax(diff.any(1))) if diff.any() else m
             upto = min(first + 1, m)  # the divergent step's output is still comparable
             rep.max_out_err = max(rep.max_out_err, float(np.abs(g_out[:upto] - o_out[t:t + upto]).max()))
             rep.steps_compared += upto
+            rep.ties_decode += int(np.sum(zero[t:t + upto]))
             if first == m:
                 break
             cols = np.nonzero(diff[first])[0]
@@ -245,7 +260,7 @@ def run_parity(w, T=None, heads=None, resync=True, check=True, prompt=None, dec=
             rep.set_mismatch_decode += len(cols)
             rep.max_margin_at_mismatch = max(rep.max_margin_at_mismatch, float(mg.max()))
             if check:
-                assert np.all(mg <= MARGIN_TOL), (t0 + t + first, [hs[c] for c in cols], mg)
+                assert permitted(mg), (t0 + t + first, [hs[c] for c in cols], mg)
             st = st_start.copy()
             oracle.decode(st, w.L + t0, q64[:t + first + 1], k64[:t + first + 1], v64[:t + first + 1],
                           w.k_heavy, w.k_local, want_out=False, **pol)

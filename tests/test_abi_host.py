@@ -38,7 +38,10 @@ def test_every_declared_symbol_is_exported(L):
         getattr(L, n)  # resolvable through ctypes too
 
 
-def test_built_for_sm103a(L):
+def test_build_targets_sm103a_only(L):
+    """Every translation unit is compiled for sm_103a and nothing else (the
+    device-side check of what actually loads is in test_gpu_arch.py)."""
+    assert hbuild.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
     assert L.h2o_build_arch() == 1030
 
 

@@ -44,3 +44,22 @@ def test_reference_arm_line():
     assert line["e2e"] == {"value": line["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
                            "d2h_bytes_per_step": 0}
     assert line["config"]["workload"] == synth.TINY.name
+
+
+def test_default_workload_is_the_largest_single_gpu_one():
+    """The bench line is quoted on the 8K-prompt shape: the largest K/V cache
+    and the most prefill work of the single-GPU workloads."""
+    w = synth.CONFIGS[bench.DEFAULT_CONFIG]
+    assert w is synth.PREFILL_HEAVY
+    single = [c for c in synth.CONFIGS if not bench.streamed(c)]
+    assert bench.kv_read_bytes(w) == max(bench.kv_read_bytes(c) for c in single)
+    assert bench.score_pass_flops(w) == max(bench.score_pass_flops(c) for c in single)
+    assert bench.kv_read_bytes(w) > bench.L2_RESIDENT_BYTES  # read from HBM every step
+
+
+def test_oracle_sample_heads_are_bounded():
+    cores = 16
+    assert bench.sample_heads(synth.PREFILL_HEAVY, cores) == cores  # one 8K-prompt head per thread
+    assert bench.sample_heads(synth.OPT_6_7B, cores) == synth.OPT_6_7B.nh  # the whole job
+    assert bench.sample_heads(synth.TINY, cores) == synth.TINY.nh
+    assert bench.sample_heads(synth.OPT_30B, cores) == bench.CPU_SAMPLE_HEADS

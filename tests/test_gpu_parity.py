@@ -178,3 +178,16 @@ def test_zero_steps_and_form_reporting():
     torch.cuda.synchronize()
     c.check_device_error()
     c2.check_device_error()
+
+
+@pytest.mark.parametrize("w,T", [(synth.OPT_30B, 32), (synth.OPT_6_7B, 64)], ids=lambda x: getattr(x, "name", str(x)))
+def test_full_size_all_heads(w, T):
+    """Every head of a full-size workload against the oracle (with
+    resynchronisation at permitted near-ties), in the launch configuration the
+    bench times (the automatic decode form does not depend on the number of
+    steps): on the OPT-30B shape that is all 3,584 heads over several waves of
+    cluster CTAs, so no CTA wave goes unchecked."""
+    rep, cache = run_parity(w, T=T)
+    print(w.name, cache.decode_form_used(), rep)
+    assert rep.heads_compared == w.nh
+    assert rep.steps_compared >= T

@@ -6,7 +6,9 @@ receive device pointers from another runtime, latency-critical loops that
 cannot afford cudaMalloc — so this entry point keeps its scratch in a fixed
 array inside the library.  Here it is called through the C ABI on two
 consecutive decode steps and must reproduce the regular entry point
-(h2o_decode_step on a cache) within the parity tolerances used elsewhere.
+(h2o_decode_steps on a cache: the same evicted positions, cache sets, and
+outputs and scores within the parity tolerances used elsewhere) and the fp64
+oracle (outputs, evicted positions, cache sets and scores after each call).
 
 This file is collected last on purpose (test_zz_*): it runs alone in a fresh
 process as well as after every other test.
@@ -20,9 +22,10 @@ import pytest
 import torch
 
 import h2o_heavy_hitter_decode_gb300 as h2o
+import oracle
 import synth
 from h2o_heavy_hitter_decode_gb300 import H2OCache
-from parity_helpers import SCORE_RTOL, out_atol, tdtype, to_dev
+from parity_helpers import MARGIN_TOL, SCORE_RTOL, out_atol, tdtype, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -61,8 +64,13 @@ def test_static_scratch_matches_regular_step(w):
     qd, kd, vd = to_dev(qs, w, dshp), to_dev(ks, w, dshp), to_dev(vs, w, dshp)
     stream = torch.cuda.current_stream()
     dt = 1 if w.dtype == "bf16" else 0
+    cv = lambda x: synth.as_f64(x, w.dtype)
+    o_st = oracle.prefill(cv(Qs), cv(Ks), cv(Vs), w.k_heavy, w.k_local)["state"]
     for t in range(2):  # two calls in a row on the same scratch
-        ref = cache.step(qd[t], kd[t], vd[t])
+        ev_ref = torch.full((1, w.B, w.H), -7, dtype=torch.int32, device="cuda")
+        ref = cache.steps(qd[t:t + 1], kd[t:t + 1], vd[t:t + 1], evicted=ev_ref)[0]
+        od = oracle.decode(o_st, position, cv(qs[t:t + 1]), cv(ks[t:t + 1]), cv(vs[t:t + 1]), w.k_heavy,
+                           w.k_local)
         out = torch.full_like(ref, float("nan"))
         ev = torch.full((w.B, w.H), -7, dtype=torch.int32, device="cuda")
         rc = f(w.B, w.H, w.d, w.k_heavy, w.k_local, dt, _p(K), _p(V), _p(pos), _p(score), n_valid, position,
@@ -73,6 +81,20 @@ def test_static_scratch_matches_regular_step(w):
         torch.cuda.synchronize()
         err = (out.float() - ref.float()).abs().max().item()
         assert err <= out_atol(w.dtype), err
+        assert torch.equal(ev, ev_ref[0]), "evicted positions differ from the regular step"
+        # against the oracle: outputs, evicted positions (margins here are far
+        # from the near-tie band), sets and scores
+        o_err = float(np.abs(out.float().cpu().numpy().reshape(w.nh, w.d) - od["out"][0]).max())
+        assert o_err <= out_atol(w.dtype), o_err
+        assert np.all(od["margin"][0] > MARGIN_TOL), od["margin"][0]
+        np.testing.assert_array_equal(ev.cpu().numpy().reshape(w.nh), od["evicted"][0])
+        for h, o_set in enumerate(o_st.sets()):
+            g_set = np.sort(pos.cpu().numpy().reshape(w.nh, w.k)[h])
+            assert np.array_equal(g_set[g_set >= 0], o_set), f"step {t} head {h}: set differs from the oracle"
+        g_sc = dict(zip(zip(np.repeat(np.arange(w.nh), w.k), pos.cpu().numpy().ravel()), score.cpu().numpy().ravel()))
+        o_live = [(h, int(p_), float(s_)) for h in range(w.nh) for p_, s_ in zip(o_st.pos[h], o_st.score[h]) if p_ >= 0]
+        rel = max(abs(g_sc[(h, p_)] - s_) / max(abs(s_), 1e-30) for h, p_, s_ in o_live)
+        assert rel <= SCORE_RTOL, rel
         ref_state = cache.export()
         torch.cuda.synchronize()
         gp, rp = pos.cpu().numpy().reshape(w.nh, w.k), ref_state["pos"].cpu().numpy().reshape(w.nh, w.k)
@@ -84,7 +106,6 @@ def test_static_scratch_matches_regular_step(w):
         a = np.array([gs[key] for key in live], np.float64)
         b = np.array([rs[key] for key in live], np.float64)
         assert np.max(np.abs(a - b) / np.maximum(np.abs(b), 1e-30)) <= SCORE_RTOL
-        assert (ev >= -1).all().item()
     assert cache.info()["n_valid"] == n_valid and cache.info()["next_pos"] == position
 
 

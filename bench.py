@@ -294,12 +294,12 @@ def l2_read_gbs(dev, nbytes):
     a = torch.ones(n, dtype=torch.float32, device=dev)
     r = torch.empty((), dtype=torch.float32, device=dev)
     for _ in range(10):
-        torch.sum(a, out=r)
+        torch.sum(a, dim=0, out=r)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     reps = 200
     e0.record()
     for _ in range(reps):
-        torch.sum(a, out=r)
+        torch.sum(a, dim=0, out=r)
     e1.record()
     torch.cuda.synchronize()
     return n * 4 * reps / (e0.elapsed_time(e1) / 1e3) / 1e9, n * 4

@@ -18,14 +18,20 @@
 // then tile nkt-1-p, reloading the resident tile in between), so every CTA
 // streams nkt + 1 query tiles whatever its place in the causal triangle.
 //
-// LSE pass.  The same pipeline with the roles swapped: a CTA owns 128 queries
-// (A operand, TMEM lanes) and streams the key tiles 0..diagonal; each thread
-// keeps an online (max, sum) of its row in base 2.
+// LSE pass (when the caller does not want O).  The same pipeline with the
+// roles swapped: a CTA owns 128 queries (A operand, TMEM lanes) and streams
+// the key tiles 0..diagonal; each thread keeps an online (max, sum) of its
+// row in base 2.
 //
-// Warp roles: thread 0 issues TMA and MMA; all four warps run the epilogue
-// (warp w reads TMEM lanes 32w..32w+31).  Every mbarrier wait is bounded; on
-// a timeout the CTA flags the cache's error word, drains what it issued and
-// frees its TMEM before returning.
+// Warp roles of these two: warp 8 issues TMA and MMA; warps 0-7 run the
+// epilogue (warp w reads TMEM lanes 32(w%4)..+31, columns 64(w/4)..+63).
+//
+// Attention pass (O and LSE, pass 1 of the prefill): two query tiles per CTA
+// ping-ponging on the tensor core, P kept in tensor memory (attn_pair_tc,
+// described at the kernel).
+//
+// Every mbarrier wait is bounded; on a timeout the CTA flags the cache's error
+// word, drains what it issued and frees its TMEM before returning.
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
@@ -402,75 +408,96 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
 }
 
-// ------------------------------------------------------- attention pass
-// Causal attention over the prompt in one pass: O and the row log-sum-exp.
-// One CTA per 128 queries.  Warp 8 is the producer: TMA for Q (resident) and
-// the K and V rings, the S = Q K^T MMAs into two TMEM buffers and the
-// O += P V MMAs (V is the MN-major B operand) into a TMEM accumulator.  Warps
-// 0-7 (two per TMEM lane quarter, 64 key columns each) turn S into bf16
-// P = exp2(s*c - m) in shared memory (128-byte swizzled K-major layout, the A
-// operand of the PV MMA) with an online row max m and an fp32 row sum l.  The
-// two warps of a row exchange their half-row maxima through each other's P
-// rows.  O is rescaled (tcgen05.ld/st) only when a row's max grows by more
-// than 2^8 over the max its P values were taken against, so P stays <= 256
-// and rescales are rare; O / l and LSE = (m + log2 l) ln 2 are written at the
-// end.  Barriers: kfull/vfull (TMA landed), sfull (S_j computed), sfree (S_j
-// read), pfull (P_j written), pvdone (O += P_j V_j done: P buffer and V stage
-// free), pair (half-row exchange between the two warps of a row).
-template <int D> struct OutGeo {
+// ------------------------------------------ attention pass, two query tiles
+// Causal attention over the prompt, O and the row log-sum-exp, with two
+// adjacent 128-query tiles per CTA (A = tile 2p, B = tile 2p+1) sharing every
+// K/V tile, so the tensor core works on one tile while the other tile's
+// softmax runs.  Warp 9 loads (TMA: both Q tiles, then a two-stage K ring and
+// a two-stage V ring); warp 8 issues the MMAs; warps 0-3 are tile A's softmax
+// and warps 4-7 tile B's, one thread per query row (TMEM lane), all 128 key
+// columns of the row in registers, so a row's maximum needs no exchange.
+// TMEM (512 columns): S_A at 0, O_A at 128, S_B at 256, O_B at 384.  The
+// softmax turns S into bf16 P = exp2(s*c - m) and stores it back into the
+// first 64 columns of the same S region; the PV MMA reads P as its A operand
+// straight from tensor memory (V is the MN-major B operand in shared memory).
+// MMA order per key tile j: PV_A(j), S_A(j+1), PV_B(j), S_B(j+1) — the
+// tensor core executes one CTA's MMAs in issue order, so S_A(j+1) overwrites
+// P_A(j) only after PV_A(j) has read it.  O is rescaled in TMEM (lazily, when
+// a row's max grows by more than 8 in base 2) by the row's own thread after
+// the previous PV has landed.  Barriers: q_full, k_full/v_full (TMA landed),
+// k_empty/v_empty (the MMAs that read a stage are done), s_full[t] (S ready),
+// p_full[t] (P written: one arrive per softmax warp), pv_done[t].
+template <int D> struct PairGeo {
   static constexpr int kTile = TileGeo<D>::kTileBytes;  // 128 rows x D bf16
-  static constexpr int kP = 128 * 128 * 2;               // P tile: 128 queries x 128 keys
-  static constexpr int kSmem = kTile * 5 + kP * 2 + 256 + 1024;
+  static constexpr int kSmem = kTile * 6 + 256 + 1024;   // V[2], K[2], Q_A, Q_B, barriers, alignment
 };
 
-struct __align__(8) OutState {
-  uint64_t res, kfull[2], vfull[2], sfull[2], sfree[2], pfull[2], pvdone[2], drain;
-  uint64_t pair[2][4];  // [tile parity][lane quarter]: both warps of a row wrote their half-row max
-  uint64_t pair_l[4];   // [lane quarter]: both warps wrote their half-row sum
+struct __align__(8) PairState {
+  uint64_t q_full, k_full[2], v_full[2], k_empty[2], v_empty[2];
+  uint64_t s_full[2], p_full[2], pv_done[2];  // per query tile
+  uint64_t drain;
   uint32_t tmem_base;
   int abort;
 };
 
-constexpr int kOutSoftmaxWarps = 8;  // 2 per TMEM lane quarter, 64 key columns each
-constexpr int kOutThreads = 32 * (kOutSoftmaxWarps + 1);
+constexpr int kPairMmaWarp = 8, kPairLoadWarp = 9;
+constexpr int kPairThreads = 32 * 10;
+
+// This warp's 32 TMEM lanes x 128 columns: four loads in flight, one wait.
+__device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t (&r)[128]) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c) tmem_ld32(taddr + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&r[32 * c]));
+  tmem_ld_wait();
+#pragma unroll
+  for (int c = 0; c < 4; ++c) tmem_regs_ready(*reinterpret_cast<uint32_t(*)[32]>(&r[32 * c]));
+}
+
+// D[tmem] (+)= A[tmem] * B[smem], issued by one thread (A: M lanes x K, two
+// bf16 per 32-bit column).
+__device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 
 template <int D>
-__global__ void __launch_bounds__(kOutThreads, 1)
-    attn_out_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                const __grid_constant__ CUtensorMap tmV, float *__restrict__ lse, __nv_bfloat16 *__restrict__ O,
-                int L, int nh, int nqt, float qscale, int *err) {
-  using G = OutGeo<D>;
+__global__ void __launch_bounds__(kPairThreads, 1)
+    attn_pair_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                 const __grid_constant__ CUtensorMap tmV, float *__restrict__ lse, __nv_bfloat16 *__restrict__ O,
+                 int L, int nqt, int npair, float qscale, int *err) {
+  using G = PairGeo<D>;
   constexpr int kT = G::kTile;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = align1024(smem_raw);
-  uint8_t *sV = smem;              // 2 stages (first: keeps MMA reads of V inside the tile area)
-  uint8_t *sK = smem + 2 * kT;     // 2 stages
-  uint8_t *sQ = smem + 4 * kT;     // resident
-  uint8_t *sP = smem + 5 * kT;     // 2 buffers of kP
-  OutState &st = *(OutState *)(sP + 2 * G::kP);
+  uint8_t *sV = smem;           // 2 stages
+  uint8_t *sK = smem + 2 * kT;  // 2 stages
+  uint8_t *sQ = smem + 4 * kT;  // tile A, then tile B
+  PairState &st = *(PairState *)(smem + 6 * kT);
   if (*(volatile int *)err) return;
-  // Head-major (a head's CTAs share its K/V tiles in L2), heaviest query tile first.
-  const int h = blockIdx.x / nqt, qt = nqt - 1 - blockIdx.x % nqt;
-  const int q0 = qt * kRows;
-  const int n = qt + 1;  // key tiles 0 .. diagonal
-  const int tid = threadIdx.x, warp = tid >> 5;
+  // Head-major (a head's CTAs share its K/V tiles in L2), heaviest pair first.
+  const int h = blockIdx.x / npair, pr = npair - 1 - blockIdx.x % npair;
+  const int qtA = 2 * pr, qtB = 2 * pr + 1;
+  const int nA = qtA + 1;                    // key tiles 0 .. diagonal
+  const int nB = qtB < nqt ? qtB + 1 : 0;    // 0: no tile B (odd tile count)
+  const int nK = nB ? nB : nA;               // key tiles loaded
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
   if (tid == 0) {
-    mbar_init(&st.res, 1);
+    mbar_init(&st.q_full, 1);
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&st.kfull[b], 1);
-      mbar_init(&st.vfull[b], 1);
-      mbar_init(&st.sfull[b], 1);
-      mbar_init(&st.sfree[b], 32 * kOutSoftmaxWarps);
-      mbar_init(&st.pfull[b], 32 * kOutSoftmaxWarps);
-      mbar_init(&st.pvdone[b], 1);
+      mbar_init(&st.k_full[b], 1);
+      mbar_init(&st.v_full[b], 1);
+      mbar_init(&st.k_empty[b], 1);
+      mbar_init(&st.v_empty[b], 1);
+      mbar_init(&st.s_full[b], 1);
+      mbar_init(&st.p_full[b], 4);
+      mbar_init(&st.pv_done[b], 1);
     }
     mbar_init(&st.drain, 1);
-    for (int qq = 0; qq < 4; ++qq) {
-      mbar_init(&st.pair[0][qq], 64);
-      mbar_init(&st.pair[1][qq], 64);
-      mbar_init(&st.pair_l[qq], 64);
-    }
     st.abort = 0;
     fence_mbar_init();
   }
@@ -481,106 +508,118 @@ __global__ void __launch_bounds__(kOutThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tbase = st.tmem_base;  // S buffers at columns 0 and 128, O at 256
-  const uint32_t tO = tbase + 256;
+  const uint32_t tbase = st.tmem_base;
+  auto tS = [&](int t) { return tbase + (uint32_t)(t * 256); };
+  auto tO = [&](int t) { return tbase + (uint32_t)(t * 256 + 128); };
 
-  if (warp == kOutSoftmaxWarps) {
-    if ((tid & 31) == 0) {
-      constexpr uint32_t idO = idesc_bf16_f32(128, D, true);
-      int kl = 0, vl = 0, mS = 0, mPV = 0;  // TMA loads and MMAs issued
+  if (warp == kPairLoadWarp) {
+    // ------------------------------------------------------------- loads
+    if (lane == 0) {
       bool ok = true;
-      load_tile<D>(sQ, &tmQ, &st.res, q0, h);
-      for (; kl < n && kl < 2; ++kl) load_tile<D>(sK + kl * kT, &tmK, &st.kfull[kl], kRows * kl, h);
-      for (; vl < n && vl < 2; ++vl) load_tile<D>(sV + vl * kT, &tmV, &st.vfull[vl], kRows * vl, h);
-      ok = mbar_wait(&st.res, 0);
-      auto issue_S = [&](int j) -> bool {
-        if (!mbar_wait(&st.kfull[j & 1], (j >> 1) & 1)) return false;
-        if (j >= 2 && !mbar_wait(&st.sfree[j & 1], ((j - 2) >> 1) & 1)) return false;
-        tc_fence_after();
-        mma_tile<D>(tbase + (uint32_t)(j & 1) * 128, smem_u32(sQ), smem_u32(sK + (j & 1) * kT));
-        umma_commit(&st.sfull[j & 1]);
-        return true;
-      };
-      if (ok) ok = issue_S(0);
-      if (ok) mS = 1;
-      for (int j = 0; ok && j < n; ++j) {
-        if (j + 1 < n) {
-          if (!(ok = issue_S(j + 1))) break;
-          mS = j + 2;
-        }
-        if (j >= 1 && vl < n) {  // V stage of tile j-1 frees when its PV is done
-          if (!(ok = mbar_wait(&st.pvdone[(j - 1) & 1], ((j - 1) >> 1) & 1))) break;
-          load_tile<D>(sV + (vl & 1) * kT, &tmV, &st.vfull[vl & 1], kRows * vl, h);
-          ++vl;
-        }
-        if (kl < n) {  // K stage of tile j frees when S_j is done
-          if (!(ok = mbar_wait(&st.sfull[j & 1], (j >> 1) & 1))) break;
-          load_tile<D>(sK + (kl & 1) * kT, &tmK, &st.kfull[kl & 1], kRows * kl, h);
-          ++kl;
-        }
-        if (!(ok = mbar_wait(&st.pfull[j & 1], (j >> 1) & 1))) break;
-        if (!(ok = mbar_wait(&st.vfull[j & 1], (j >> 1) & 1))) break;
-        tc_fence_after();
-        const uint32_t pa = smem_u32(sP + (j & 1) * G::kP), va = smem_u32(sV + (j & 1) * kT);
+      int kl = 0, vl = 0;
+      mbar_expect_tx(&st.q_full, (nB ? 2 : 1) * G::kTile);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {  // 128 keys, 16 per MMA
-          const uint64_t ad = sdesc_sw128(pa + (uint32_t)((kk >> 2) * kBox + (kk & 3) * 32), 16, 1024);
-          const uint64_t bd = sdesc_sw128(va + (uint32_t)(kk * 2048), kBox, 1024);
-          umma_bf16(tO, ad, bd, idO, (j > 0 || kk > 0) ? 1u : 0u);
-        }
-        umma_commit(&st.pvdone[j & 1]);
-        mPV = j + 1;
+      for (int b = 0; b < TileGeo<D>::kBoxes; ++b) {
+        tma_load_3d(sQ + b * kBox, &tmQ, &st.q_full, b * 64, qtA * kRows, h);
+        if (nB) tma_load_3d(sQ + kT + b * kBox, &tmQ, &st.q_full, b * 64, qtB * kRows, h);
+      }
+      for (int j = 0; j < nK; ++j) {
+        const int s = j & 1;
+        if (j >= 2 && !(ok = mbar_wait_backoff(&st.k_empty[s], ((j - 2) >> 1) & 1))) break;
+        load_tile<D>(sK + s * kT, &tmK, &st.k_full[s], kRows * j, h);
+        kl = j + 1;
+        if (j >= 2 && !(ok = mbar_wait_backoff(&st.v_empty[s], ((j - 2) >> 1) & 1))) break;
+        load_tile<D>(sV + s * kT, &tmV, &st.v_full[s], kRows * j, h);
+        vl = j + 1;
       }
       if (!ok) {
         st.abort = 1;
-        // Drain every MMA and TMA copy this CTA issued before releasing
-        // shared memory and TMEM.
+        // the copies still in flight land before shared memory is released
+        mbar_wait(&st.q_full, 0);
+        for (int j = kl > 2 ? kl - 2 : 0; j < kl; ++j) mbar_wait(&st.k_full[j & 1], (j >> 1) & 1);
+        for (int j = vl > 2 ? vl - 2 : 0; j < vl; ++j) mbar_wait(&st.v_full[j & 1], (j >> 1) & 1);
+      }
+    }
+  } else if (warp == kPairMmaWarp) {
+    // -------------------------------------------------------------- MMAs
+    if (lane == 0) {
+      constexpr uint32_t idO = idesc_bf16_f32(128, D, true);
+      auto issue_S = [&](int t, int j) {
+        mma_tile<D>(tS(t), smem_u32(sQ + t * kT), smem_u32(sK + (j & 1) * kT));
+        umma_commit(&st.s_full[t]);
+      };
+      auto issue_PV = [&](int t, int j) {
+        const uint32_t va = smem_u32(sV + (j & 1) * kT);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)  // 128 keys, 16 per MMA; P holds two keys per column
+          umma_bf16_ts(tO(t), tS(t) + (uint32_t)(kk * 8), sdesc_sw128(va + (uint32_t)(kk * 2048), kBox, 1024), idO,
+                       (j > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(&st.pv_done[t]);
+      };
+      bool ok = mbar_wait(&st.q_full, 0) && mbar_wait(&st.k_full[0], 0);
+      if (ok) {
+        tc_fence_after();
+        issue_S(0, 0);
+        if (nB) issue_S(1, 0);
+        umma_commit(&st.k_empty[0]);
+      }
+      for (int j = 0; ok && j < nK; ++j) {
+        const int s = j & 1;
+        bool v_ready = false;
+        if (j < nA) {
+          if (!(ok = mbar_wait(&st.p_full[0], j & 1) && mbar_wait(&st.v_full[s], (j >> 1) & 1))) break;
+          v_ready = true;
+          tc_fence_after();
+          issue_PV(0, j);
+        }
+        const bool next = j + 1 < nK;
+        if (next) {
+          if (!(ok = mbar_wait(&st.k_full[(j + 1) & 1], ((j + 1) >> 1) & 1))) break;
+          tc_fence_after();
+          if (j + 1 < nA) issue_S(0, j + 1);
+        }
+        if (j < nB) {
+          if (!(ok = mbar_wait(&st.p_full[1], j & 1) && (v_ready || mbar_wait(&st.v_full[s], (j >> 1) & 1)))) break;
+          tc_fence_after();
+          issue_PV(1, j);
+        }
+        umma_commit(&st.v_empty[s]);
+        if (next) {
+          if (j + 1 < nB) issue_S(1, j + 1);
+          umma_commit(&st.k_empty[(j + 1) & 1]);
+        }
+      }
+      if (!ok) {
+        st.abort = 1;
+        // every MMA this CTA issued completes before TMEM and shared memory go
         umma_commit(&st.drain);
         mbar_wait(&st.drain, 0);
-        for (int j = mS; j < kl; ++j) mbar_wait(&st.kfull[j & 1], (j >> 1) & 1);
-        for (int j = mPV; j < vl; ++j) mbar_wait(&st.vfull[j & 1], (j >> 1) & 1);
       }
-      (void)mPV;
     }
   } else {
-    // Softmax warps: query row `row` (TMEM lane), key columns c_off .. c_off+63.
-    const int lane = tid & 31;
-    const int quarter = warp & 3;
+    // ----------------------------------------------------------- softmax
+    const int t = warp >> 2;          // query tile
+    const int quarter = warp & 3;     // TMEM lanes 32*quarter ..
     const int row = quarter * 32 + lane;
-    const int half = warp >> 2;
-    const int c_off = half * 64;
-    const int q = q0 + row;
+    const int n = t ? nB : nA;
+    const int q = (t ? qtB : qtA) * kRows + row;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    const int sw = row & 7;
-    constexpr int kHalfD = D / 2;  // output columns of this warp
-    float m_run = -INFINITY, l_run = 0.f;
+    float m_run = -INFINITY, l_run = 0.f;  // base-2 running max (scaled) and sum of this row
     bool ok = true;
     for (int j = 0; j < n; ++j) {
-      if (j >= 2 && !(ok = wait_warp(&st.pvdone[j & 1], ((j - 2) >> 1) & 1))) break;
-      if (!(ok = wait_warp(&st.sfull[j & 1], (j >> 1) & 1))) break;
+      if (!(ok = wait_warp(&st.s_full[t], j & 1))) break;
       tc_fence_after();
-      const bool diag = (j == n - 1);
-      uint32_t r[64];
-      tmem_ld64(tbase + lane_off + (uint32_t)(j & 1) * 128 + (uint32_t)c_off, r);
-      float hm4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // partial maxima
+      uint32_t r[128];
+      tmem_ld128(tS(t) + lane_off, r);
+      if (j == n - 1) {  // diagonal tile: key column c is visible iff c <= row
 #pragma unroll
-      for (int i = 0; i < 64; ++i) {
-        float x = __uint_as_float(r[i]) * qscale;
-        if (diag && c_off + i > row) x = -INFINITY;  // key after the query
-        r[i] = __float_as_uint(x);
-        hm4[i & 3] = fmaxf(hm4[i & 3], x);
+        for (int i = 0; i < 128; ++i)
+          if (i > row) r[i] = __float_as_uint(-INFINITY);
       }
-      const float hm = fmaxf(fmaxf(hm4[0], hm4[1]), fmaxf(hm4[2], hm4[3]));
-      tc_fence_before();
-      mbar_arrive(&st.sfree[j & 1]);  // the logits are in registers: S buffer free
-      // Half-row maxima: each warp writes into the partner's rows of this P
-      // buffer (free: its last PV is done), which the partner reads before it
-      // overwrites them with its own P.
-      uint8_t *pbuf = sP + (j & 1) * G::kP;
-      *reinterpret_cast<float *>(pbuf + (1 - half) * kBox + row * 128) = hm;
-      mbar_arrive(&st.pair[j & 1][quarter]);
-      if (!(ok = wait_warp(&st.pair[j & 1][quarter], (j >> 1) & 1))) break;
-      const float m_tile = fmaxf(hm, *reinterpret_cast<const float *>(pbuf + half * kBox + row * 128));
+      float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int i = 0; i < 128; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], __uint_as_float(r[i]));
+      const float m_tile = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * qscale;
       float m_new = m_run;
       bool resc = false;
       if (m_run == -INFINITY) {
@@ -590,62 +629,53 @@ __global__ void __launch_bounds__(kOutThreads, 1)
         resc = true;
       }
       if (__any_sync(0xffffffffu, resc)) {
-        // O must hold every earlier P V before it is rescaled
-        if (!(ok = wait_warp(&st.pvdone[(j - 1) & 1], ((j - 1) >> 1) & 1))) break;
+        // O must hold every earlier P V before it is rescaled (j >= 1 here)
+        if (!(ok = wait_warp(&st.pv_done[t], (j - 1) & 1))) break;
         tc_fence_after();
         const float f = resc ? ex2(m_run - m_new) : 1.f;
 #pragma unroll 1
-        for (int cc = 0; cc < kHalfD; cc += 32) {
+        for (int cc = 0; cc < D; cc += 32) {
           uint32_t o[32];
-          const uint32_t ta = tO + lane_off + (uint32_t)(half * kHalfD + cc);
-          tmem_ld32(ta, o);
+          tmem_ld32(tO(t) + lane_off + (uint32_t)cc, o);
           tmem_ld_wait();
           tmem_regs_ready(o);
 #pragma unroll
           for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * f);
-          tmem_st32(ta, o);
+          tmem_st32(tO(t) + lane_off + (uint32_t)cc, o);
         }
         tmem_st_wait();
         l_run *= f;
       }
       m_run = m_new;
-      uint32_t pk[32];
+      const float nm = -m_run;
+      uint32_t pk[64];
       float ls4[4] = {0.f, 0.f, 0.f, 0.f};  // partial row sums
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const float a = ex2(__uint_as_float(r[2 * i]) - m_run);  // masked: exp2(-inf) = 0
-        const float b = ex2(__uint_as_float(r[2 * i + 1]) - m_run);
+      for (int i = 0; i < 64; ++i) {  // masked logits are -inf: exp2 gives 0
+        const float a = ex2(fmaf(__uint_as_float(r[2 * i]), qscale, nm));
+        const float b = ex2(fmaf(__uint_as_float(r[2 * i + 1]), qscale, nm));
         ls4[i & 3] += a + b;
         __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
         pk[i] = *reinterpret_cast<uint32_t *>(&v);
       }
       l_run += (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
-      // 64 keys = one 128-byte row of box `half`: eight 16-byte chunks, swizzled by row.
-      uint8_t *prow = pbuf + half * kBox + row * 128;
-#pragma unroll
-      for (int cch = 0; cch < 8; ++cch)
-        *reinterpret_cast<uint4 *>(prow + ((cch ^ sw) << 4)) =
-            make_uint4(pk[4 * cch], pk[4 * cch + 1], pk[4 * cch + 2], pk[4 * cch + 3]);
-      fence_proxy_async_smem();
+      // P over the first 64 columns of the S region (two keys per column)
+      tmem_st32(tS(t) + lane_off, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+      tmem_st32(tS(t) + lane_off + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+      tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&st.pfull[j & 1]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&st.p_full[t]);
     }
-    if (ok) ok = wait_warp(&st.pvdone[(n - 1) & 1], ((n - 1) >> 1) & 1);
-    if (ok) {
+    if (ok && n > 0) ok = wait_warp(&st.pv_done[t], (n - 1) & 1);
+    if (ok && n > 0) {
       tc_fence_after();
-      // Row sum: the halves hand each other l through P buffer 0 (free now).
-      *reinterpret_cast<float *>(sP + (1 - half) * kBox + row * 128 + 4) = l_run;
-      mbar_arrive(&st.pair_l[quarter]);
-      ok = wait_warp(&st.pair_l[quarter], 0);
-    }
-    if (ok) {
-      const float l_row = l_run + *reinterpret_cast<const float *>(sP + half * kBox + row * 128 + 4);
-      const float inv = 1.f / l_row;
-      __nv_bfloat16 *orow = O + ((size_t)h * L + (q < L ? q : 0)) * D + half * kHalfD;
+      const float inv = 1.f / l_run;
+      __nv_bfloat16 *orow = O + ((size_t)h * L + (q < L ? q : 0)) * D;
 #pragma unroll 1
-      for (int c0 = 0; c0 < kHalfD; c0 += 32) {  // collective loads: every lane, every chunk
+      for (int c0 = 0; c0 < D; c0 += 32) {  // collective loads: every lane, every chunk
         uint32_t o[32];
-        tmem_ld32(tO + lane_off + (uint32_t)(half * kHalfD + c0), o);
+        tmem_ld32(tO(t) + lane_off + (uint32_t)c0, o);
         tmem_ld_wait();
         tmem_regs_ready(o);
         if (q < L) {
@@ -661,8 +691,8 @@ __global__ void __launch_bounds__(kOutThreads, 1)
           for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
         }
       }
-      if (half == 0 && q < L) lse[(size_t)h * L + q] = (m_run + __log2f(l_row)) * kLn2;
-    } else {
+      if (q < L) lse[(size_t)h * L + q] = (m_run + __log2f(l_run)) * kLn2;
+    } else if (!ok) {
       st.abort = 1;
     }
   }
@@ -724,19 +754,25 @@ cudaError_t colsum_t(const CacheView &c, const void *Q, const void *K, const flo
   return cudaGetLastError();
 }
 
+// One CTA per SM: 512 TMEM columns each (the d = 64 instance requests the
+// d = 128 shared-memory footprint so that no second CTA waits in
+// tcgen05.alloc).
+constexpr int kPairSmem = PairGeo<128>::kSmem;
+
 template <int D>
-cudaError_t attn_out_t(const CacheView &c, const void *Q, const void *K, const void *V, float *lse, void *O,
-                       int L, cudaStream_t st) {
+cudaError_t attn_pair_t(const CacheView &c, const void *Q, const void *K, const void *V, float *lse, void *O,
+                        int L, cudaStream_t st) {
   CUtensorMap mq, mk, mv;
   if (!make_map(&mq, Q, D, L, c.nh) || !make_map(&mk, K, D, L, c.nh) || !make_map(&mv, V, D, L, c.nh))
     return cudaErrorInvalidValue;
-  const int smem = OutGeo<D>::kSmem;
-  cudaError_t e = cudaFuncSetAttribute(attn_out_tc<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  const int smem = kPairSmem;
+  cudaError_t e = cudaFuncSetAttribute(attn_pair_tc<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int nqt = (L + kRows - 1) / kRows;
-  const long long grid = (long long)nqt * c.nh;
-  attn_out_tc<D><<<(unsigned)grid, kOutThreads, smem, st>>>(mq, mk, mv, lse, (__nv_bfloat16 *)O, L, c.nh, nqt,
-                                                     kLog2e / sqrtf((float)D), c.err);
+  const int npair = (nqt + 1) / 2;
+  const long long grid = (long long)npair * c.nh;
+  attn_pair_tc<D><<<(unsigned)grid, kPairThreads, smem, st>>>(mq, mk, mv, lse, (__nv_bfloat16 *)O, L, nqt, npair,
+                                                             kLog2e / sqrtf((float)D), c.err);
   return cudaGetLastError();
 }
 
@@ -765,7 +801,7 @@ bool prefill_tc_supported(const CacheView &c, int L) {
 cudaError_t launch_prefill_attn_tc(const CacheView &c, const void *Q, const void *K, const void *V, void *O,
                                    float *lse, int L, cudaStream_t st) {
   if (!O) return c.d == 128 ? lse_t<128>(c, Q, K, lse, L, st) : lse_t<64>(c, Q, K, lse, L, st);
-  return c.d == 128 ? attn_out_t<128>(c, Q, K, V, lse, O, L, st) : attn_out_t<64>(c, Q, K, V, lse, O, L, st);
+  return c.d == 128 ? attn_pair_t<128>(c, Q, K, V, lse, O, L, st) : attn_pair_t<64>(c, Q, K, V, lse, O, L, st);
 }
 
 cudaError_t launch_prefill_colsum_tc(const CacheView &c, const void *Q, const void *K, const float *lse,

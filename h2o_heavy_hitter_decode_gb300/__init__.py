@@ -18,7 +18,7 @@ import re
 
 import torch
 
-__all__ = ["H2OCache", "H2OError", "lib", "LIB_PATH", "HEADER_PATH", "declared_functions", "kernel_arch"]
+__all__ = ["H2OCache", "H2OError", "lib", "LIB_PATH", "HEADER_PATH", "declared_functions", "kernel_arch", "probe_read_gbs"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libh2o.so")
@@ -81,6 +81,8 @@ def lib():
         L.h2o_status_str.restype = C.c_char_p
         L.h2o_last_cuda_error.restype = i32
         L.h2o_build_arch.restype = i32
+        L.h2o_probe_read.argtypes = [vp, sz, i32, vp, vp]
+        L.h2o_probe_read.restype = i32
         L.h2o_kernel_arch.argtypes = [C.POINTER(i32), C.POINTER(i32)]
         L.h2o_kernel_arch.restype = i32
         for f in ("h2o_cache_create", "h2o_cache_destroy", "h2o_set_stream", "h2o_prefill", "h2o_prefill_rows",
@@ -100,6 +102,26 @@ def kernel_arch():
     ptx, binv = C.c_int32(), C.c_int32()
     _check(lib().h2o_kernel_arch(C.byref(ptx), C.byref(binv)), "h2o_kernel_arch")
     return ptx.value, binv.value
+
+
+def probe_read_gbs(nbytes: int, reps: int = 50, device=None) -> float:
+    """Read bandwidth (GB/s) of a device buffer of `nbytes`, measured with the
+    library's read kernel (h2o_probe_read): `reps` sweeps after a warm-up,
+    timed with CUDA events on the current stream."""
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    n = max(16, int(nbytes) // 16 * 16)
+    buf = torch.ones(n // 4, dtype=torch.int32, device=dev)
+    sink = torch.zeros(1, dtype=torch.int32, device=dev)
+    s = torch.cuda.current_stream(dev)
+    run = lambda r: _check(lib().h2o_probe_read(_ptr(buf), n, int(r), _ptr(sink), C.c_void_p(s.cuda_stream)),
+                           "h2o_probe_read")
+    run(2)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    run(reps)
+    e1.record(s)
+    e1.synchronize()
+    return n * reps / (e0.elapsed_time(e1) / 1e3) / 1e9
 
 
 def _check(rc: int, what: str):

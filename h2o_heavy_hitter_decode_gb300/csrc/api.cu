@@ -330,11 +330,11 @@ h2o_status h2o_decode_steps(h2o_cache_t c, int n, const void *q, const void *k, 
   if (c->next_pos + n > kMaxPos) return H2O_EINVAL;
   const size_t step = (size_t)c->nh * c->d * c->esize;
   CacheView vc = c->view;  // cluster form: one cluster of <= 8 CTAs per head
-  if (vc.nsplit > 8) vc.nsplit = 8;
-  // Automatic choice (measured on GB300): the cluster form when its grid runs
-  // in one wave (or in >= 3 waves, so the last one still saturates HBM), else
-  // the cooperative grid when all (head, split) CTAs fit at once, else the
-  // cluster form anyway, else one launch per step.
+  vc.nsplit = decode_cluster_size(c->nh, c->k, num_sms_current_device());
+  // Automatic choice (measured on GB300 with the cluster size above: the
+  // cluster form was the fastest on every workload): the cluster form, else
+  // the cooperative grid when all (head, split) CTAs fit at once, else one
+  // launch per step.
   const int form = c->decode_form;
   const bool cluster_ok = n >= 2 && decode_cluster_supported(vc);
   const bool coop_ok = n >= 2 && (form == 0 || form == 2) && decode_persistent_fits(c->view);
@@ -344,12 +344,10 @@ h2o_status h2o_decode_steps(h2o_cache_t c, int n, const void *q, const void *k, 
   } else if (form == 2) {
     use_coop = coop_ok;
   } else if (form == 0) {
-    if (cluster_ok && decode_cluster_preferred(vc))
+    if (cluster_ok)
       use_cluster = true;
     else if (coop_ok)
       use_coop = true;
-    else
-      use_cluster = cluster_ok;
   }
   if (n >= 2 && ((form == 3 && !use_cluster) || (form == 2 && !use_coop))) return H2O_EUNSUPPORTED;
   PhaseTimer pt(c, 3, use_cluster ? 1 : use_coop ? (n + 16383) / 16384 : n);

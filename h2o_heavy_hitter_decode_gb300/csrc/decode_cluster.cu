@@ -647,16 +647,6 @@ cudaError_t dispatch_nc(const CacheView &c, const DecodeStep &s, int nsteps, cud
   return launch_cluster_t<T, S, D, false, 3, NC>(c, s, nsteps, st);
 }
 
-template <typename T, typename S, int D, int NC>
-bool waves_ok_nc(const CacheView &c) {
-  const int chunk = chunk_of(c);
-  if (resident_nc<T, S, D, NC>(c) || all_resident<T, S, D, false, 3, NC>(c, chunk) ||
-      all_resident<T, S, D, false, 2, NC>(c, chunk))
-    return true;
-  const long long fit = resident_ctas<T, S, D, false, 3, NC>(c, chunk);
-  return fit > 0 && (long long)c.nh * c.nsplit >= 3 * fit;
-}
-
 // The consumer-warp count for a CTA that owns chunk_of(c) slots.
 template <typename T, typename S, int D>
 bool resident_t(const CacheView &c) {
@@ -667,11 +657,6 @@ template <typename T, typename S, int D>
 cudaError_t dispatch_t(const CacheView &c, const DecodeStep &s, int nsteps, cudaStream_t st) {
   return chunk_of(c) > kShortChunk ? dispatch_nc<T, S, D, 4>(c, s, nsteps, st)
                                    : dispatch_nc<T, S, D, 2>(c, s, nsteps, st);
-}
-
-template <typename T, typename S, int D>
-bool cluster_waves_ok_t(const CacheView &c) {
-  return chunk_of(c) > kShortChunk ? waves_ok_nc<T, S, D, 4>(c) : waves_ok_nc<T, S, D, 2>(c);
 }
 
 #define H2O_CLUSTER_DISPATCH(FN, ...)                                              \
@@ -696,10 +681,22 @@ bool decode_cluster_resident(const CacheView &c) {
   return false;
 }
 
-bool decode_cluster_preferred(const CacheView &c) {
-  if (c.nsplit < 1 || c.nsplit > kMaxCluster) return false;
-  H2O_CLUSTER_DISPATCH(cluster_waves_ok_t, c);
-  return false;
+// Cluster size: the smallest power of two that leaves each CTA at most
+// kShortChunk slots (the two-consumer-warp kernel), doubled (up to 8) while
+// the grid fills less than 90 % of one wave of 7 CTAs per SM.  Measured on
+// GB300 (us per decode step, cluster sizes 1 / 2 / 4 / 8): OPT-6.7B shape
+// (256 heads, k = 512) - / 11.6 / 8.2 / 13.8; OPT-30B shape (3584 heads,
+// k = 408) 103.4 / 81.9 / 99.7 / -; 8K-prompt shape (1024 heads, k = 1690)
+// 133.8 / 123.9 / 121.7 / 114.6; long stream (32 heads, k = 256) 10.4 / 4.89
+// / 3.24 / 2.62 — the rule picks the fastest in each case.  Where a wave of
+// CTAs holds less than L2 (the OPT-30B shape at size 2: 532 heads, 111 MB),
+// its steps read the cache from L2.
+int decode_cluster_size(int nh, int k, int sms) {
+  int P = 1;
+  while (P < kMaxCluster && (k + P - 1) / P > kShortChunk) P *= 2;
+  const long long wave = 7LL * (sms > 0 ? sms : 1);
+  while (P < kMaxCluster && (long long)nh * P * 10 < wave * 9) P *= 2;
+  return P;
 }
 
 bool decode_cluster_supported(const CacheView &c) {

@@ -51,9 +51,9 @@ cudaError_t launch_decode_persistent(const CacheView &c, const DecodeStep &s, in
 // the receivers' mbarriers; no global scratch.
 bool decode_cluster_supported(const CacheView &c);
 bool decode_cluster_resident(const CacheView &c);  // each CTA's K/V rows stay in shared memory
-// The cluster grid runs in one wave, or in enough waves that a partial last
-// wave still streams at full bandwidth.
-bool decode_cluster_preferred(const CacheView &c);
+// CTAs per head (cluster size, 1..8) of the cluster form for nh heads of k
+// slots on `sms` SMs.
+int decode_cluster_size(int nh, int k, int sms);
 cudaError_t launch_decode_cluster(const CacheView &c, const DecodeStep &s, int nsteps, cudaStream_t st);
 // Split count of the decode launch for nh heads of k slots on `sms` SMs
 // (fixes the size of the split-partial scratch).

@@ -263,6 +263,16 @@ h2o_status h2o_get_error(h2o_cache_t cache);
 const char *h2o_status_str(h2o_status s);
 int h2o_last_cuda_error(void);
 
+/* Measurement helper (not part of the method): `reps` sweeps of 16-byte
+ * reads over the device buffer `buf` of `bytes` (a multiple of 16, 16-byte
+ * aligned) through L2, by 4 CTAs of 512 threads per SM, enqueued on
+ * cuda_stream.  `sink` is a device uint32 the kernel may write (so the reads
+ * are not optimised away).  Timed by the caller (events around the call), it
+ * gives the read bandwidth of a buffer of that size: above the L2 capacity the
+ * HBM read rate, below it the L2 read rate that a decode over an L2-resident
+ * K/V cache runs against.  H2O_EINVAL on bad arguments, nothing launched. */
+h2o_status h2o_probe_read(const void *buf, size_t bytes, int reps, uint32_t *sink, void *cuda_stream);
+
 /* Compiled-in target, for checks: returns 1030 for sm_103a. */
 int h2o_build_arch(void);
 

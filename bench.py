@@ -586,6 +586,15 @@ def e2e(args, w, wl, Bg, heads, dev, hQ, hK, hV, hq, hk, hv, tdt, stream, world,
         stream.wait_stream(back)  # the job ends when its outputs are on the host
         return c
 
+    # the host link alone: every input copied once from pinned memory, nothing else running
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for t in range(6):
+        dbuf[t].copy_(pin[t], non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    h2d_alone_ms = e0.elapsed_time(e1)
     n = args.steps
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(max(1, min(args.warmup, 3)) + n)]
@@ -607,8 +616,11 @@ def e2e(args, w, wl, Bg, heads, dev, hQ, hK, hV, hq, hk, hv, tdt, stream, world,
     h2d_prompt = sum(x.numel() * x.element_size() for x in pin[:3])
     h2d_dec = sum(pin[t][t0:t1].numel() * pin[t].element_size() for t in (3, 4, 5) for t0, t1 in sgroups)
     d2h = sum(hout[t0:t1].numel() * hout.element_size() for t0, t1 in sgroups)
+    all_in = sum(x.numel() * x.element_size() for x in pin)
     r = {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": h2d_prompt + h2d_dec, "d2h_bytes_per_step": d2h,
-         "ms_per_step": ms_step, "prompt_row_groups": ng, "decode_step_groups": len(sgroups)}
+         "ms_per_step": ms_step, "prompt_row_groups": ng, "decode_step_groups": len(sgroups),
+         "h2d_alone": {"ms": h2d_alone_ms, "gbs": all_in / (h2d_alone_ms / 1e3) / 1e9,
+                       "what": "one copy of every input buffer from pinned host memory, nothing else running"}}
     if streamed(w):
         r["note"] = (f"decode inputs copied chunk by chunk from one pinned host chunk of {STREAM_CHUNK} steps "
                      "(the host cannot hold the whole stream's inputs)")

@@ -254,59 +254,71 @@ __global__ void __launch_bounds__(threads_for(NC), 7) decode_cluster_kernel(cons
       const int nslab = kResident ? (nrows + TR - 1) / TR : nst;
       const int myit = sub / LPI;  // the row this lane holds after the reduction
       bool ok = true;
+      int st = g % kStages, ph = (g / kStages) & 1;  // ring stage and phase of slab g
       for (int i = 0; i < nslab; ++i) {
         const uint8_t *ks, *vs;
-        int st = 0;
         if (kResident) {
           ks = kv + (size_t)i * TR * ROWB;
           vs = kv + (size_t)chunk * ROWB + (size_t)i * TR * ROWB;
         } else {
-          st = g % kStages;
-          if (!(ok = __all_sync(0xffffffffu, mbar_wait(&s_full[st], (g / kStages) & 1)))) break;
+          if (!(ok = __all_sync(0xffffffffu, mbar_wait(&s_full[st], ph)))) break;
           ks = kv + st * 2 * kStageBytes;
           vs = ks + kStageBytes;
         }
         const int rows = min(TR, nrows - i * TR);
-        float x[ITER];
+        // One slab: full slabs (every row of the slab filled, all but a CTA's
+        // last) take a path without per-row bounds checks.
+        auto slab = [&](auto full_tag) {
+          constexpr bool kFull = decltype(full_tag)::value;
+          float x[ITER];
 #pragma unroll
-        for (int it = 0; it < ITER; ++it) {
-          const int r = warp * RPW + grp + it * kConsumers * RPW;
-          x[it] = qk.dot(ks + (r < rows ? r : 0) * ROWB + sub * Lane<S>::VB);
-        }
-        const int rm = warp * RPW + grp + myit * kConsumers * RPW;
-        const bool valid = rm < rows;
-        float lgt = xreduce<ITER, LPR>(x, sub) * qk.scale;
-        if (kFp8) lgt *= valid ? ksc[i * TR + rm] : 0.f;
-        lgt = valid ? lgt : -INFINITY;
-        if (valid && sub % LPI == 0) lg[i * TR + rm] = lgt;
-        float wmax = lgt;  // over the warp's rows of this slab
-#pragma unroll
-        for (int o = LPI; o < 32; o <<= 1) wmax = fmaxf(wmax, __shfl_xor_sync(0xffffffffu, wmax, o));
-        if (wmax > m) {  // warp-uniform: rescale only when the running max grows
-          const float sc_ = ex2(m - wmax);
-          l *= sc_;
-#pragma unroll
-          for (int e = 0; e < EPL; ++e) acc[e] *= sc_;
-          m = wmax;
-        }
-        const float prm = valid ? ex2(lgt - m) : 0.f;
-#pragma unroll
-        for (int it = 0; it < ITER; ++it) {
-          const int r = warp * RPW + grp + it * kConsumers * RPW;
-          const float pr = __shfl_sync(0xffffffffu, prm, grp * LPR + it * LPI);
-          if (r < rows) {
-            l += pr;
-            const float pv = kFp8 ? pr * vsc[i * TR + r] : pr;
-            float vx[EPL];
-            unpack_lane<S>(vs + r * ROWB + sub * Lane<S>::VB, vx);
-#pragma unroll
-            for (int e = 0; e < EPL; ++e) acc[e] = fmaf(pv, vx[e], acc[e]);
+          for (int it = 0; it < ITER; ++it) {
+            const int r = warp * RPW + grp + it * kConsumers * RPW;
+            x[it] = qk.dot(ks + (kFull || r < rows ? r : 0) * ROWB + sub * Lane<S>::VB);
           }
-        }
+          const int rm = warp * RPW + grp + myit * kConsumers * RPW;
+          const bool valid = kFull || rm < rows;
+          float lgt = xreduce<ITER, LPR>(x, sub) * qk.scale;
+          if (kFp8) lgt *= valid ? ksc[i * TR + rm] : 0.f;
+          lgt = valid ? lgt : -INFINITY;
+          if (valid && sub % LPI == 0) lg[i * TR + rm] = lgt;
+          float wmax = lgt;  // over the warp's rows of this slab
+#pragma unroll
+          for (int o = LPI; o < 32; o <<= 1) wmax = fmaxf(wmax, __shfl_xor_sync(0xffffffffu, wmax, o));
+          if (wmax > m) {  // warp-uniform: rescale only when the running max grows
+            const float sc_ = ex2(m - wmax);
+            l *= sc_;
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) acc[e] *= sc_;
+            m = wmax;
+          }
+          const float prm = valid ? ex2(lgt - m) : 0.f;
+          if (sub % LPI == 0) l += prm;  // each row's weight once, in the lane that holds it
+#pragma unroll
+          for (int it = 0; it < ITER; ++it) {
+            const int r = warp * RPW + grp + it * kConsumers * RPW;
+            const float pr = __shfl_sync(0xffffffffu, prm, grp * LPR + it * LPI);
+            if (kFull || r < rows) {
+              const float pv = kFp8 ? pr * vsc[i * TR + r] : pr;
+              float vx[EPL];
+              unpack_lane<S>(vs + r * ROWB + sub * Lane<S>::VB, vx);
+#pragma unroll
+              for (int e = 0; e < EPL; ++e) acc[e] = fmaf(pv, vx[e], acc[e]);
+            }
+          }
+        };
+        if (rows == TR)
+          slab(std::true_type{});
+        else
+          slab(std::false_type{});
         if (!kResident) {
           ++g;
           __syncwarp();
           if (lane == 0) mbar_arrive(&s_empty[st]);
+          if (++st == kStages) {
+            st = 0;
+            ph ^= 1;
+          }
         }
       }
       if (!ok && lane == 0) {
@@ -332,7 +344,7 @@ __global__ void __launch_bounds__(threads_for(NC), 7) decode_cluster_kernel(cons
         m = mn;
         if (grp == 0) {
           const float pr = ex2(dot - m);
-          l += pr;
+          if (lane == 0) l += pr;
           float vx[EPL];
           load_f32<T, EPL>(in_v + sub * EPL, vx);
 #pragma unroll
@@ -340,8 +352,9 @@ __global__ void __launch_bounds__(threads_for(NC), 7) decode_cluster_kernel(cons
         }
       }
 #pragma unroll
+      for (int o = 1; o < 32; o <<= 1) l += __shfl_xor_sync(0xffffffffu, l, o);  // row weights sit in single lanes
+#pragma unroll
       for (int o = LPR; o < 32; o <<= 1) {
-        l += __shfl_xor_sync(0xffffffffu, l, o);
 #pragma unroll
         for (int e = 0; e < EPL; ++e) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], o);
       }

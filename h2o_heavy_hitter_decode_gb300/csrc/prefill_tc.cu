@@ -5,18 +5,16 @@
 // accumulated attention score of key j is its causal column sum
 //   colsum_j = sum_{i >= j} exp(q_i.k_j / sqrt(d) - LSE_i).
 //
-// Column-sum pass (the score pass).  A CTA owns a tile of 128 keys, which is
-// the MMA's A operand (M = 128 TMEM lanes, one key per thread) and stays in
-// shared memory; query tiles of 128 stream in through a two-stage TMA ring as
-// the B operand (N = 128).  S^T = K Q^T lands in one of two TMEM accumulator
-// buffers, so the MMA of query tile j+1 runs while the epilogue warps turn
-// tile j into exp2(s * log2(e)/sqrt(d) - LSE_i * log2(e)) and add it along
-// their TMEM row: every key's sum stays in one thread, deterministic and
-// atomic-free.  Only the first query tile of a key tile touches the diagonal
-// and needs the causal mask; query rows past L are zero-filled by TMA and
-// masked by LSE = +inf.  Each CTA runs two key tiles back to back (tile p,
-// then tile nkt-1-p, reloading the resident tile in between), so every CTA
-// streams nkt + 1 query tiles whatever its place in the causal triangle.
+// Column-sum pass (the score pass, colsum_pair_tc).  A CTA owns two adjacent
+// 128-key tiles, resident in shared memory as the MMA's A operands (M = 128
+// TMEM lanes, one key per thread); query tiles of 128 stream through a TMA
+// ring as the shared B operand (N = 128) and each S^T = K Q^T lands in a
+// double-buffered TMEM accumulator of its key tile, so one key tile's MMA
+// overlaps the other's epilogue.  Each epilogue thread turns its key row into
+// exp2(s * log2(e)/sqrt(d) - LSE_i * log2(e)) and adds it into its own sum:
+// deterministic and atomic-free.  Only the first query tile of a key tile
+// touches the diagonal and needs the causal mask; query rows past L are
+// zero-filled by TMA and masked by LSE = +inf.
 //
 // LSE pass (when the caller does not want O).  The same pipeline with the
 // roles swapped: a CTA owns 128 queries (A operand, TMEM lanes) and streams
@@ -239,110 +237,6 @@ __device__ __forceinline__ bool tile_pipeline(uint8_t *smem, SmallState &st, con
   const bool ok = !*(volatile int *)&st.abort;
   if (warp == 0) tmem_dealloc(tbase, 256);
   return ok;
-}
-
-// ------------------------------------------------------------- column sums
-// A CTA takes key tile p and key tile nkt-1-p of one head (two segments of
-// the pipeline): nkt - p and p + 1 query tiles, nkt + 1 in all, so the causal
-// triangle splits into equal CTAs.
-template <int D>
-__global__ void __launch_bounds__(kThreads, 2)
-    colsum_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-              const float *__restrict__ lse, float *__restrict__ colsum, int L, int nkt, float qscale, int *err) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t *smem = align1024(smem_raw);
-  using G = TileGeo<D>;
-  float *nl2 = (float *)(smem + G::kTileBytes * (1 + kStages));  // [2][128]: -LSE*log2(e) per query
-  float *raw = nl2 + 2 * kRows;                                   // [3][128]: LSE slices in flight
-  SmallState &st = *(SmallState *)(raw + 3 * kRows);
-  if (*(volatile int *)err) return;
-  // Head-major (a head's CTAs share its Q tiles in L2).
-  const int npair = (nkt + 1) / 2;
-  const int h = blockIdx.x / npair, pr = blockIdx.x % npair;
-  const int kta = pr, ktb = nkt - 1 - pr;
-  const int k0a = kta * kRows, k0b = ktb * kRows;
-  const int na = nkt - kta, nb = (ktb != kta) ? nkt - ktb : 0;  // query tiles of each segment
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int row = (warp & 3) * 32 + lane;  // key within the tile (TMEM lane)
-  const int c_off = (warp >> 2) * 64;      // this warp's query columns
-  const float *lse_h = lse + (size_t)h * L;
-  // Column vector of streamed tile j (query tile k0 + 128 j' of its
-  // segment): -LSE * log2(e) (-inf past L, so those zero-filled query rows
-  // add nothing).  The producer lanes fetch each tile's LSE slice with
-  // asynchronous 4-byte copies two tiles ahead (a three-slot staging ring),
-  // so no global load latency sits on the path that issues the MMAs.
-  struct Prep {
-    const float *lse_h;
-    float *nl2, *raw;
-    int k0a, k0b, na, L, n;
-    __device__ int q0(int j) const { return j < na ? k0a + kRows * j : k0b + kRows * (j - na); }
-    __device__ void fetch(int j, int ln) {  // copies of tile j, one commit group
-      if (j < n) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int q = q0(j) + ln + 32 * i;
-          if (q < L) {
-            asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(
-                             sm100::smem_u32(raw + (j % 3) * kRows + ln + 32 * i)),
-                         "l"(lse_h + q)
-                         : "memory");
-          }
-        }
-      }
-      asm volatile("cp.async.commit_group;" ::: "memory");
-    }
-    __device__ void load(int j, int ln) {
-      if (j == 0) {
-        fetch(0, ln);
-        fetch(1, ln);
-      }
-    }
-    __device__ void store(int j, int ln) {  // tile j landed (at most one newer group pending)
-      asm volatile("cp.async.wait_group 1;" ::: "memory");
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int q = q0(j) + ln + 32 * i;
-        nl2[(j & 1) * kRows + ln + 32 * i] = q < L ? -raw[(j % 3) * kRows + ln + 32 * i] * kLog2e : -INFINITY;
-      }
-      fetch(j + 2, ln);
-    }
-  } prep{lse_h, nl2, raw, k0a, k0b, na, L, na + nb};
-  float acc[2] = {0.f, 0.f};  // this thread's key row, per segment
-  auto epi = [&](int seg, int j, uint32_t taddr) {
-    const float *nl = nl2 + ((seg ? na + j : j) & 1) * kRows + c_off;
-    uint32_t r[64];
-    tmem_ld64(taddr, r);
-    float a4[4] = {0.f, 0.f, 0.f, 0.f};  // four partial sums: short dependency chains
-    if (j == 0) {  // diagonal tile: query column c contributes iff c >= key row
-#pragma unroll
-      for (int i = 0; i < 64; ++i) {
-        const float e = ex2(fmaf(__uint_as_float(r[i]), qscale, nl[i]));
-        a4[i & 3] += (c_off + i >= row) ? e : 0.f;
-      }
-    } else {
-#pragma unroll
-      for (int i = 0; i < 64; ++i) a4[i & 3] += ex2(fmaf(__uint_as_float(r[i]), qscale, nl[i]));
-    }
-    const float a = (a4[0] + a4[1]) + (a4[2] + a4[3]);
-    if (seg) acc[1] += a;
-    else acc[0] += a;
-  };
-  const bool ok = tile_pipeline<D, true>(smem, st, &tmK, &tmQ, Seg{k0a, k0a, na}, Seg{k0b, k0b, nb}, h, prep, epi);
-  // the two column halves of each key row: the second half hands its sums over
-  float *half = nl2;  // [2][128], free after the pipeline
-  if (ok && warp >= 4 && warp < kEpiWarps) {
-    half[row] = acc[0];
-    half[kRows + row] = acc[1];
-  }
-  __syncthreads();
-  if (ok) {
-    if (warp < 4) {
-      if (k0a + row < L) colsum[(size_t)h * L + k0a + row] = acc[0] + half[row];
-      if (nb > 0 && k0b + row < L) colsum[(size_t)h * L + k0b + row] = acc[1] + half[kRows + row];
-    }
-  } else if (tid == 0) {
-    atomicOr(err, 4);
-  }
 }
 
 // ---------------------------------------------------------- row log-sum-exp
@@ -703,6 +597,233 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   if (warp == 0) tmem_dealloc(tbase, 512);
 }
 
+// --------------------------------------------- column sums, two key tiles
+// The score pass with two adjacent 128-key tiles per CTA (a = tile 2p,
+// b = tile 2p+1), both resident in shared memory as MMA A operands, sharing
+// every streamed query tile (B operand, a four-stage TMA ring).  For query
+// tile j the MMA warp issues S^T_a(j) and S^T_b(j) into per-key-tile double
+// TMEM accumulators (512 columns: a0, a1, b0, b1), so the tensor core works
+// on one key tile while the other key tile's epilogue runs.  Warps 0-3 are
+// key tile a's epilogue and warps 4-7 key tile b's, one thread per key row
+// (TMEM lane), all 128 query columns of a tile: each thread adds
+// exp2(s * log2(e)/sqrt(d) - LSE_q * log2(e)) over the columns into its own
+// running sum (fixed order: deterministic, no atomics).  The load warp stages
+// -LSE * log2(e) of each query tile beside its Q tile (-inf past L, so the
+// zero-filled rows add nothing).  Key tile a reads query tiles a .. nqt-1,
+// key tile b query tiles b .. nqt-1; the first tile of each is its diagonal
+// (query column c visible iff c >= key row).
+constexpr int kCsStages = 4;
+
+template <int D> struct CsGeo {
+  static constexpr int kTile = TileGeo<D>::kTileBytes;
+  static constexpr int kSmem = kTile * (2 + kCsStages) + kCsStages * kRows * 4 + 256 + 1024;
+};
+
+struct __align__(8) CsState {
+  uint64_t k_full, q_full[kCsStages], q_empty[kCsStages];
+  uint64_t acc_full[2][2], acc_empty[2][2];  // [key tile][buffer]
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kPairThreads, 1)
+    colsum_pair_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                   const float *__restrict__ lse, float *__restrict__ colsum, int L, int nqt, int npair,
+                   float qscale, int *err) {
+  using G = CsGeo<D>;
+  constexpr int kT = G::kTile;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = align1024(smem_raw);
+  uint8_t *sK = smem;                                     // key tiles a, b
+  uint8_t *sQ = smem + 2 * kT;                            // query ring
+  float *sNl = (float *)(smem + (2 + kCsStages) * kT);    // [stage][128] -LSE*log2(e)
+  CsState &st = *(CsState *)(sNl + kCsStages * kRows);
+  if (*(volatile int *)err) return;
+  // Head-major (a head's CTAs share its Q tiles in L2), heaviest pair first.
+  const int h = blockIdx.x / npair, pr = npair - 1 - blockIdx.x % npair;
+  const int kta = 2 * pr, ktb = 2 * pr + 1;
+  const bool has_b = ktb < nqt;
+  const int n = nqt - kta;  // query tiles streamed: kta .. nqt-1 (key tile b skips the first)
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+  if (tid == 0) {
+    mbar_init(&st.k_full, 1);
+    for (int s = 0; s < kCsStages; ++s) {
+      mbar_init(&st.q_full[s], 2);       // TMA bytes + the load warp's -LSE vector
+      mbar_init(&st.q_empty[s], 1 + 8);  // the MMAs' commit + every epilogue warp
+    }
+    for (int t = 0; t < 2; ++t)
+      for (int b = 0; b < 2; ++b) {
+        mbar_init(&st.acc_full[t][b], 1);
+        mbar_init(&st.acc_empty[t][b], 4);
+      }
+    mbar_init(&st.drain, 1);
+    st.abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&st.tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = st.tmem_base;
+  auto tAcc = [&](int t, int b) { return tbase + (uint32_t)((t * 2 + b) * 128); };
+
+  if (warp == kPairLoadWarp) {
+    // ------------------------------------------------------------- loads
+    bool ok = true;
+    int issued = 0;
+    if (lane == 0) {
+      mbar_expect_tx(&st.k_full, (has_b ? 2 : 1) * kT);
+#pragma unroll
+      for (int b = 0; b < TileGeo<D>::kBoxes; ++b) {
+        tma_load_3d(sK + b * kBox, &tmK, &st.k_full, b * 64, kta * kRows, h);
+        if (has_b) tma_load_3d(sK + kT + b * kBox, &tmK, &st.k_full, b * 64, ktb * kRows, h);
+      }
+    }
+    const float *lse_h = lse + (size_t)h * L;
+    for (int i = 0; i < n; ++i) {
+      const int s = i % kCsStages, qt = kta + i;
+      if (i >= kCsStages && !(ok = __all_sync(0xffffffffu, mbar_wait_backoff(&st.q_empty[s],
+                                                                             ((i / kCsStages) - 1) & 1))))
+        break;
+      if (lane == 0) {
+        mbar_expect_tx(&st.q_full[s], kT);
+#pragma unroll
+        for (int b = 0; b < TileGeo<D>::kBoxes; ++b)
+          tma_load_3d(sQ + s * kT + b * kBox, &tmQ, &st.q_full[s], b * 64, qt * kRows, h);
+      }
+      issued = i + 1;
+#pragma unroll
+      for (int u = 0; u < kRows / 32; ++u) {
+        const int q = qt * kRows + u * 32 + lane;
+        sNl[s * kRows + u * 32 + lane] = q < L ? -__ldg(lse_h + q) * kLog2e : -INFINITY;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&st.q_full[s]);
+    }
+    if (!ok && lane == 0) {
+      st.abort = 1;
+      mbar_wait(&st.k_full, 0);
+      for (int i = issued > kCsStages ? issued - kCsStages : 0; i < issued; ++i)
+        mbar_wait(&st.q_full[i % kCsStages], (i / kCsStages) & 1);
+    }
+  } else if (warp == kPairMmaWarp) {
+    // -------------------------------------------------------------- MMAs
+    if (lane == 0) {
+      bool ok = mbar_wait(&st.k_full, 0);
+      for (int i = 0; ok && i < n; ++i) {
+        const int s = i % kCsStages;
+        if (!(ok = mbar_wait(&st.q_full[s], (i / kCsStages) & 1))) break;
+        // key tile a: its i-th query tile
+        if (i >= 2 && !(ok = mbar_wait(&st.acc_empty[0][i & 1], ((i - 2) >> 1) & 1))) break;
+        tc_fence_after();
+        mma_tile<D>(tAcc(0, i & 1), smem_u32(sK), smem_u32(sQ + s * kT));
+        umma_commit(&st.acc_full[0][i & 1]);
+        // key tile b: its (i-1)-th query tile
+        if (has_b && i >= 1) {
+          const int ib = i - 1;
+          if (ib >= 2 && !(ok = mbar_wait(&st.acc_empty[1][ib & 1], ((ib - 2) >> 1) & 1))) break;
+          tc_fence_after();
+          mma_tile<D>(tAcc(1, ib & 1), smem_u32(sK + kT), smem_u32(sQ + s * kT));
+          umma_commit(&st.acc_full[1][ib & 1]);
+        }
+        umma_commit(&st.q_empty[s]);
+      }
+      if (!ok) {
+        st.abort = 1;
+        umma_commit(&st.drain);
+        mbar_wait(&st.drain, 0);
+      }
+    }
+  } else {
+    // ---------------------------------------------------------- epilogue
+    const int t = warp >> 2;        // key tile
+    const int quarter = warp & 3;   // TMEM lanes 32*quarter ..
+    const int row = quarter * 32 + lane;
+    const int kt = t ? ktb : kta;
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    float acc = 0.f;
+    bool ok = true;
+    {
+      for (int i = 0; i < n; ++i) {
+        const int s = i % kCsStages;
+        if (t == 1 && (i == 0 || !has_b)) {
+          // the first query tile belongs to key tile a only (and without a key
+          // tile b none does): release the stage, every use counts 8 warps
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&st.q_empty[s]);
+          continue;
+        }
+        const int it = t ? i - 1 : i;  // this key tile's own tile count
+        if (!(ok = wait_warp(&st.acc_full[t][it & 1], (it >> 1) & 1) &&
+                   wait_warp(&st.q_full[s], (i / kCsStages) & 1)))
+          break;
+        tc_fence_after();
+        // Two halves of 64 columns: the second half's TMEM load is in flight
+        // while the first half is summed.
+        const uint32_t ta = tAcc(t, it & 1) + lane_off;
+        uint32_t r[64], r2[64];
+        tmem_ld64(ta, r);
+        tmem_ld32(ta + 64, *reinterpret_cast<uint32_t(*)[32]>(&r2[0]));
+        tmem_ld32(ta + 96, *reinterpret_cast<uint32_t(*)[32]>(&r2[32]));
+        const float4 *nl4 = reinterpret_cast<const float4 *>(sNl + s * kRows);
+        float a4[4] = {0.f, 0.f, 0.f, 0.f};  // four partial sums: short dependency chains
+        // columns c0 .. c0+63 from v; on the diagonal column c counts iff c >= key row
+        auto sum64 = [&](const uint32_t (&v)[64], int c0) {
+          if (it == 0) {
+#pragma unroll
+            for (int c4 = 0; c4 < 16; ++c4) {
+              const float4 nv = nl4[c0 / 4 + c4];
+              const float nn[4] = {nv.x, nv.y, nv.z, nv.w};
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const float e = ex2(fmaf(__uint_as_float(v[4 * c4 + u]), qscale, nn[u]));
+                a4[u] += (c0 + 4 * c4 + u >= row) ? e : 0.f;
+              }
+            }
+          } else {
+#pragma unroll
+            for (int c4 = 0; c4 < 16; ++c4) {
+              const float4 nv = nl4[c0 / 4 + c4];
+              a4[0] += ex2(fmaf(__uint_as_float(v[4 * c4]), qscale, nv.x));
+              a4[1] += ex2(fmaf(__uint_as_float(v[4 * c4 + 1]), qscale, nv.y));
+              a4[2] += ex2(fmaf(__uint_as_float(v[4 * c4 + 2]), qscale, nv.z));
+              a4[3] += ex2(fmaf(__uint_as_float(v[4 * c4 + 3]), qscale, nv.w));
+            }
+          }
+        };
+        sum64(r, 0);
+        tmem_ld_wait();
+        tmem_regs_ready(*reinterpret_cast<uint32_t(*)[32]>(&r2[0]));
+        tmem_regs_ready(*reinterpret_cast<uint32_t(*)[32]>(&r2[32]));
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&st.acc_empty[t][it & 1]);  // the accumulator is in registers
+        sum64(r2, 64);
+        acc += (a4[0] + a4[1]) + (a4[2] + a4[3]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&st.q_empty[s]);  // done with this stage's -LSE vector
+      }
+      if (!ok) {
+        st.abort = 1;
+      } else if (t == 0 || has_b) {
+        const int key = kt * kRows + row;
+        if (key < L) colsum[(size_t)h * L + key] = acc;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (st.abort && tid == 0) atomicOr(err, 4);
+  if (warp == 0) tmem_dealloc(tbase, 512);
+}
+
 // ----------------------------------------------------------------- host side
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -733,26 +854,27 @@ bool make_map(CUtensorMap *m, const void *base, int d, int L, int nh) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Each CTA of the LSE and column-sum passes holds 256 TMEM columns, so at most
-// two may share an SM's 512: the d = 64 kernels request the d = 128 shared
-// memory footprint to keep a third CTA off the SM instead of blocking in
-// tcgen05.alloc.
+// Each CTA of the LSE pass holds 256 TMEM columns, so at most two may share
+// an SM's 512: the d = 64 kernel requests the d = 128 shared memory footprint
+// to keep a third CTA off the SM instead of blocking in tcgen05.alloc.
 constexpr int kTwoPerSmSmem = TileGeo<128>::kSmem;
 
 template <int D>
-cudaError_t colsum_t(const CacheView &c, const void *Q, const void *K, const float *lse, float *colsum, int L,
-                     cudaStream_t st) {
+cudaError_t colsum_pair_t(const CacheView &c, const void *Q, const void *K, const float *lse, float *colsum, int L,
+                          cudaStream_t st) {
   CUtensorMap mq, mk;
   if (!make_map(&mq, Q, D, L, c.nh) || !make_map(&mk, K, D, L, c.nh)) return cudaErrorInvalidValue;
-  const int smem = kTwoPerSmSmem;
-  cudaError_t e = cudaFuncSetAttribute(colsum_tc<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  const int smem = CsGeo<128>::kSmem;  // one CTA per SM (512 TMEM columns) for both widths
+  cudaError_t e = cudaFuncSetAttribute(colsum_pair_tc<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  const int nkt = (L + kRows - 1) / kRows;
-  const long long grid = (long long)((nkt + 1) / 2) * c.nh;  // key-tile pairs
-  colsum_tc<D><<<(unsigned)grid, kThreads, smem, st>>>(mq, mk, lse, colsum, L, nkt, kLog2e / sqrtf((float)D),
-                                                      c.err);
+  const int nqt = (L + kRows - 1) / kRows;
+  const int npair = (nqt + 1) / 2;
+  const long long grid = (long long)npair * c.nh;
+  colsum_pair_tc<D><<<(unsigned)grid, kPairThreads, smem, st>>>(mq, mk, lse, colsum, L, nqt, npair,
+                                                               kLog2e / sqrtf((float)D), c.err);
   return cudaGetLastError();
 }
+
 
 // One CTA per SM: 512 TMEM columns each (the d = 64 instance requests the
 // d = 128 shared-memory footprint so that no second CTA waits in
@@ -806,7 +928,7 @@ cudaError_t launch_prefill_attn_tc(const CacheView &c, const void *Q, const void
 
 cudaError_t launch_prefill_colsum_tc(const CacheView &c, const void *Q, const void *K, const float *lse,
                                      float *colsum, int L, cudaStream_t st) {
-  return c.d == 128 ? colsum_t<128>(c, Q, K, lse, colsum, L, st) : colsum_t<64>(c, Q, K, lse, colsum, L, st);
+  return c.d == 128 ? colsum_pair_t<128>(c, Q, K, lse, colsum, L, st) : colsum_pair_t<64>(c, Q, K, lse, colsum, L, st);
 }
 
 }  // namespace h2o

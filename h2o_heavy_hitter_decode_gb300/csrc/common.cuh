@@ -296,6 +296,18 @@ __device__ __forceinline__ void store_codes(uint8_t *row, int lane, uint32_t pac
     *(uint16_t *)(row + lane * 2) = (uint16_t)packed;
 }
 
+// s += w by compensated (Kahan) summation: c carries, negated, the low-order
+// part that earlier additions to s lost, so a score that is a sum of millions
+// of small weights keeps its accuracy (W. Kahan, "Further remarks on reducing
+// truncation errors", Comm. ACM 8(1), 1965).  Returns the new s.
+__device__ __forceinline__ float kahan_add(float &s, float &c, float w) {
+  const float y = w - c;
+  const float t = s + y;
+  c = (t - s) - y;
+  s = t;
+  return t;
+}
+
 // Ranking key of the cache entry at position `pos` once the query at position
 // p has attended: its accumulated score, or (score_mode 1) that score over
 // the number of queries that attended to it, p - pos + 1 (an entry, once

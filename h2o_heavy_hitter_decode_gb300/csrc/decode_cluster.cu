@@ -10,7 +10,9 @@
 // fixed ranges of `chunk` slots; CTA r owns slots [r*chunk, (r+1)*chunk).
 // Scores, position tags and the step's logits of its slots live in the CTA's
 // shared memory for the whole launch (read at the start, written back at the
-// end); K/V rows are streamed from HBM each step (4 KB cp.async.bulk slabs in
+// end); within the launch each score is a compensated (Kahan) sum of its
+// weights, folded into the stored fp32 score at the end, so a score that
+// collects millions of small weights over a long stream stays accurate; K/V rows are streamed from HBM each step (4 KB cp.async.bulk slabs in
 // a 2- or 3-stage ring fed by a producer warp, which also issues the next
 // step's first slabs while the cluster exchanges partials) or, when a CTA's
 // rows fit and the grid is co-resident, loaded once and kept in shared
@@ -126,17 +128,18 @@ __global__ void __launch_bounds__(threads_for(NC), 7) decode_cluster_kernel(cons
   const size_t hk = (size_t)h * c.k;
   const size_t step_elems = (size_t)c.nh * D;
 
-  // dynamic shared memory: [ring or resident K|V][score][pos][logit]
-  // (+ [K scale][V scale] for an fp8 cache)[every rank's acc row, P x D, read
-  // on rank 0]
+  // dynamic shared memory: [ring or resident K|V][score][pos][logit][score
+  // compensation] (+ [K scale][V scale] for an fp8 cache)[every rank's acc
+  // row, P x D, read on rank 0]
   uint8_t *kv = smem;
   const int kv_bytes = kResident ? 2 * chunk * ROWB : ring_bytes(kStages);
   float *sc = (float *)(smem + kv_bytes);
   int *ps = (int *)(sc + chunk);
   float *lg = (float *)(ps + chunk);
-  float *ksc = lg + chunk;
+  float *cm = lg + chunk;  // Kahan compensation of each owned score, for this launch
+  float *ksc = cm + chunk;
   float *vsc = ksc + chunk;
-  float *accx = (float *)(smem + ((kv_bytes + (kFp8 ? 5 : 3) * chunk * 4 + 15) & ~15));
+  float *accx = (float *)(smem + ((kv_bytes + (kFp8 ? 6 : 4) * chunk * 4 + 15) & ~15));
 
   if (tid == 0) {
     for (int i = 0; i < kStages; ++i) {
@@ -154,6 +157,7 @@ __global__ void __launch_bounds__(threads_for(NC), 7) decode_cluster_kernel(cons
   }
   for (int j = tid; j < own; j += kThreads) {
     sc[j] = c.score[hk + s0 + j];
+    cm[j] = 0.f;
     ps[j] = c.pos[hk + s0 + j];
     if (kFp8) {
       ksc[j] = c.Ksc[hk + s0 + j];
@@ -443,8 +447,10 @@ __global__ void __launch_bounds__(threads_for(NC), 7) decode_cluster_kernel(cons
     if (warp < kConsumers) {
       for (int j = tid; j < nrows; j += kConsumerThreads) {
         const float w = exp2f(lg[j] - Mg) * invL;
-        const float s_new = sc[j] + w;
+        float s_new = sc[j], cj = cm[j];
+        kahan_add(s_new, cj, w);
         sc[j] = s_new;
+        cm[j] = cj;
         const int pj = ps[j];
         if ((long long)pj <= lim && pj >= c.n_sink) {
           const ArgMin cand{rank_key(s_new, p, pj, c.score_mode), pj, s0 + j};
@@ -501,6 +507,7 @@ __global__ void __launch_bounds__(threads_for(NC), 7) decode_cluster_kernel(cons
         if (tid == 0) {
           ps[j] = p;
           sc[j] = dec_w;
+          cm[j] = 0.f;
         }
         constexpr int PER = D / 32;  // fp8: lane L quantises elements L*PER ..
         uint32_t ck = 0u, cv = 0u;
@@ -558,7 +565,7 @@ __global__ void __launch_bounds__(threads_for(NC), 7) decode_cluster_kernel(cons
   // write back the owned scores and tags; no CTA leaves while a peer could
   // still push into its shared memory
   for (int j = tid; j < own; j += kThreads) {
-    c.score[hk + s0 + j] = sc[j];
+    c.score[hk + s0 + j] = sc[j] - cm[j];  // the compensated sum, rounded once
     c.pos[hk + s0 + j] = ps[j];
     if (kFp8) {
       c.Ksc[hk + s0 + j] = ksc[j];
@@ -568,9 +575,9 @@ __global__ void __launch_bounds__(threads_for(NC), 7) decode_cluster_kernel(cons
   cluster.sync();
 }
 
-// Per-slot shared-memory words beside K/V: score, tag, logit (+ two scales
-// for an fp8 cache).
-template <typename S> constexpr int slot_words() { return is_fp8<S>() ? 5 : 3; }
+// Per-slot shared-memory words beside K/V: score, tag, logit, score
+// compensation (+ two scales for an fp8 cache).
+template <typename S> constexpr int slot_words() { return is_fp8<S>() ? 6 : 4; }
 
 template <typename S, int D> constexpr int row_bytes() { return D * (int)sizeof(S); }
 
@@ -717,7 +724,7 @@ bool decode_cluster_supported(const CacheView &c) {
   const int chunk = (c.k + c.nsplit - 1) / c.nsplit;
   const int row = c.d * (c.kv_fp8 ? 1 : c.dtype == 1 ? 2 : 4);
   const int kv = (2 * chunk * row <= kResidentMaxBytes) ? 2 * chunk * row : ring_bytes(3);
-  return kv + (c.kv_fp8 ? 5 : 3) * chunk * 4 + 16 + c.nsplit * c.d * 4 <= 200 * 1024;
+  return kv + (c.kv_fp8 ? 6 : 4) * chunk * 4 + 16 + c.nsplit * c.d * 4 <= 200 * 1024;
 }
 
 cudaError_t launch_decode_cluster(const CacheView &c, const DecodeStep &s, int nsteps, cudaStream_t st) {

@@ -59,7 +59,7 @@ struct __align__(8) SmallState {
   uint64_t a_free;            // the MMAs of the first segment are done with the resident tile
   uint64_t ld_bar[kStages];   // streamed tile landed
   uint64_t ld_free[kStages];  // the MMA that read the stage is done
-  uint64_t mma_full[2];       // accumulator (and its column vector) ready
+  uint64_t mma_full[2];       // accumulator ready
   uint64_t acc_empty[2];      // epilogue warps done with the accumulator
   uint64_t drain;
   uint32_t tmem_base;
@@ -112,17 +112,14 @@ struct Seg {
 // Shared skeleton, warp-specialised, over one or two segments that share the
 // ring and the accumulators (the streamed-tile count j runs on across the
 // segment boundary).  Warp 8 (the producer) issues the TMA loads and the MMAs
-// into two TMEM accumulators and, per tile, fills that tile's column vector
-// with `prep(j, lane)` before marking the accumulator full; warps 0-7 wait
-// for it, call `epi(segment, j_in_segment, taddr)` with the TMEM address of
-// their 32 lanes and 64-column half, and release the accumulator.  At the
-// segment boundary the producer waits for the first segment's last MMA
-// (a_free) and reloads the resident tile.  No CTA-wide barrier inside the
-// loop.
-template <int D, bool kPrep, class Prep, class Epi>
+// into two TMEM accumulators; warps 0-7 wait for an accumulator, call
+// `epi(segment, j_in_segment, taddr)` with the TMEM address of their 32 lanes
+// and 64-column half, and release it.  At the segment boundary the producer
+// waits for the first segment's last MMA (a_free) and reloads the resident
+// tile.  No CTA-wide barrier inside the loop.
+template <int D, class Epi>
 __device__ __forceinline__ bool tile_pipeline(uint8_t *smem, SmallState &st, const CUtensorMap *mapA,
-                                              const CUtensorMap *mapB, Seg s0_, Seg s1_, int h, Prep &&prep,
-                                              Epi &&epi) {
+                                              const CUtensorMap *mapB, Seg s0_, Seg s1_, int h, Epi &&epi) {
   using G = TileGeo<D>;
   const int n0 = s0_.n, n = s0_.n + s1_.n;
   auto brow = [&](int j) { return j < n0 ? s0_.s0 + kRows * j : s1_.s0 + kRows * (j - n0); };
@@ -137,7 +134,7 @@ __device__ __forceinline__ bool tile_pipeline(uint8_t *smem, SmallState &st, con
       mbar_init(&st.ld_free[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&st.mma_full[b], kPrep ? 2 : 1);
+      mbar_init(&st.mma_full[b], 1);
       mbar_init(&st.acc_empty[b], kEpiWarps);
     }
     mbar_init(&st.drain, 1);
@@ -164,9 +161,8 @@ __device__ __forceinline__ bool tile_pipeline(uint8_t *smem, SmallState &st, con
       ok = mbar_wait(&st.res_bar, 0);
     }
     ok = __shfl_sync(0xffffffffu, ok, 0);
-    if (kPrep) prep.load(0, lane);
     for (int j = 0; ok && j < n; ++j) {
-      // the whole warp observes the accumulator (and its column vector) free
+      // the whole warp observes the accumulator free
       if (j >= 2 && !(ok = wait_warp(&st.acc_empty[j & 1], ((j - 2) >> 1) & 1))) break;
       if (lane == 0) {
         if (j == n0 && j > 0) {  // segment boundary: the resident tile of the second segment
@@ -190,12 +186,6 @@ __device__ __forceinline__ bool tile_pipeline(uint8_t *smem, SmallState &st, con
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
-      if (kPrep) {  // the accumulator buffer's column vector (free: its epilogue is done)
-        prep.store(j, lane);
-        if (j + 1 < n) prep.load(j + 1, lane);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&st.mma_full[j & 1]);
-      }
       // refill the stage of tile j-1 (its MMA is done or nearly) with tile j-1+kStages
       if (lane == 0 && j >= 1 && loads < n && loads == j - 1 + kStages) {
         const int sj = (j - 1) % kStages;
@@ -258,10 +248,6 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int row = (warp & 3) * 32 + lane;  // query within the tile (TMEM lane)
   const int c_off = (warp >> 2) * 64;      // this warp's key columns
   float m = -INFINITY, l = 0.f;  // base-2 running max and sum over this thread's columns
-  struct NoPrep {
-    __device__ void load(int, int) {}
-    __device__ void store(int, int) {}
-  } prep;
   auto epi = [&](int, int j, uint32_t taddr) {
     const bool diag = (j == nk - 1);
     uint32_t r[64];
@@ -284,7 +270,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     l = l * ex2(m - mn) + sum;
     m = mn;
   };
-  const bool ok = tile_pipeline<D, false>(smem, st, &tmQ, &tmK, Seg{q0, 0, nk}, Seg{0, 0, 0}, h, prep, epi);
+  const bool ok = tile_pipeline<D>(smem, st, &tmQ, &tmK, Seg{q0, 0, nk}, Seg{0, 0, 0}, h, epi);
   if (ok && warp >= 4 && warp < kEpiWarps) {
     xch[row] = m;
     xch[kRows + row] = l;

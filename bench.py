@@ -20,7 +20,9 @@ Printed JSON line (rank 0):
   prefill   score-pass (column sums) and attention-pass TFLOP/s;
   roofline  the kernel with the largest share of the step, measured live with
             CUDA events on the launching stream (the C ABI's phase timer);
-  e2e       the same metric with host (pinned) buffers, copies timed;
+  e2e       the same metric with host (pinned) buffers, copies timed (for
+            long prompts one cache per row group, each decoded as soon as
+            its rows are prefilled, so the compute overlaps the host link);
   cpu_baseline  the fp64 oracle on the host cores on a bounded sample of heads.
 
 Several GPUs: one process per GPU (torchrun, or `--gpus N`, which starts
@@ -60,6 +62,11 @@ L2_RESIDENT_BYTES = 120e6  # caches below this stay in the 129 MB L2 across deco
 METRIC = "H2O decode tokens/s and KV-read GB/s vs HBM peak; prefill score TFLOP/s"
 DEFAULT_CONFIG = 3  # the 8K-prompt serving shape: the largest single-GPU workload
 STREAM_CHUNK = 65536  # decode steps per call when the inputs are generated on the device
+# The end-to-end leg pipelines by row groups (one cache each, decoded as soon as
+# its rows are prefilled) from this prompt length on: measured on GB300, the
+# 8K-prompt job 60.2 -> 57.6 ms; on 1-2K prompts the per-group decodes were
+# slower than one decode over all rows (OPT-6.7B shape 6.0 -> 14.8 ms).
+E2E_ROWS_MIN_PROMPT = 4096
 
 
 def peaks():
@@ -498,8 +505,13 @@ def run_ours(args, w, rank, world, local_rank):
     del qd, kd, vd, Qd, Kd, Vd, O, out  # device inputs of the resident runs: room for the e2e buffers
     caches.clear()
     if not args.no_e2e:
-        line["e2e"] = e2e(args, w, wl, Bg, heads, dev, hQ, hK, hV, hq, hk, hv, tdt, stream, world, dist,
-                          row_groups=args.e2e_row_groups, step_groups=args.e2e_step_groups)
+        rows = args.e2e_pipeline == "rows" or (args.e2e_pipeline == "auto" and w.L >= E2E_ROWS_MIN_PROMPT)
+        if rows and not streamed(w):
+            line["e2e"] = e2e_row_caches(args, w, wl, Bg, dev, hQ, hK, hV, hq, hk, hv, tdt, stream, world, dist,
+                                         row_groups=args.e2e_row_groups)
+        else:
+            line["e2e"] = e2e(args, w, wl, Bg, heads, dev, hQ, hK, hV, hq, hk, hv, tdt, stream, world, dist,
+                              row_groups=args.e2e_row_groups, step_groups=args.e2e_step_groups)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args)
     if dist:
@@ -639,6 +651,94 @@ def e2e(args, w, wl, Bg, heads, dev, hQ, hK, hV, hq, hk, hv, tdt, stream, world,
     return r
 
 
+def e2e_row_caches(args, w, wl, Bg, dev, hQ, hK, hV, hq, hk, hv, tdt, stream, world, dist, row_groups=8):
+    """Same job from pinned host buffers, pipelined by batch rows: the batch is
+    split into `row_groups` groups with one cache each (every head is
+    independent, so the arithmetic is the same as one cache over all rows).
+    A side stream copies each group's prompt rows and decode inputs in turn;
+    the compute stream prefills and decodes group g as soon as its inputs have
+    landed (while later groups are still crossing the host link), and group
+    g's outputs copy back while later groups compute.  The host buffers are
+    laid out per group (contiguous rows) before the timed region."""
+    import torch
+    from h2o_heavy_hitter_decode_gb300 import H2OCache
+    nb = wl.B
+    ng = max(1, min(row_groups, nb))
+    groups = [(nb * g // ng, nb * (g + 1) // ng) for g in range(ng)]
+    pin = [[x[b0:b1].contiguous().pin_memory() for x in (hQ, hK, hV)]
+           + [x[:, b0:b1].contiguous().pin_memory() for x in (hq, hk, hv)] for b0, b1 in groups]
+    dbuf = [[torch.empty_like(x, device=dev) for x in p] for p in pin]
+    outs = [torch.empty(p[3].shape, dtype=tdt, device=dev) for p in pin]
+    houts = [torch.empty(p[3].shape, dtype=tdt).pin_memory() for p in pin]
+    O = [torch.empty(p[0].shape, dtype=tdt, device=dev) for p in pin]
+    lse = [torch.empty(p[0].shape[:3], dtype=torch.float32, device=dev) for p in pin]
+    colsum = [torch.empty_like(x) for x in lse]
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    side = torch.cuda.Stream(device=dev)
+    back = torch.cuda.Stream(device=dev)
+
+    def job(start_ev):
+        side.wait_event(start_ev)
+        landed = []
+        with torch.cuda.stream(side):
+            for g in range(ng):
+                for t in range(6):
+                    dbuf[g][t].copy_(pin[g][t], non_blocking=True)
+                ev = torch.cuda.Event()
+                ev.record(side)
+                landed.append(ev)
+        caches = []
+        for g, (b0, b1) in enumerate(groups):
+            stream.wait_event(landed[g])
+            c = H2OCache(b1 - b0, w.H, w.d, w.k_heavy, w.k_local, tdt, device=dev, kv_fp8=is_kvfp8(w))
+            c.set_decode_form(args.decode_form)
+            c.prefill(dbuf[g][0], dbuf[g][1], dbuf[g][2], O=O[g], lse=lse[g], colsum=colsum[g])
+            c.steps(dbuf[g][3], dbuf[g][4], dbuf[g][5], out=outs[g])
+            done = torch.cuda.Event()
+            done.record(stream)
+            back.wait_event(done)
+            with torch.cuda.stream(back):
+                houts[g].copy_(outs[g], non_blocking=True)
+            caches.append(c)
+        stream.wait_stream(back)  # the job ends when its outputs are on the host
+        return caches
+
+    # the host link alone: every input copied once from pinned memory, nothing else running
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for g in range(ng):
+        for t in range(6):
+            dbuf[g][t].copy_(pin[g][t], non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    h2d_alone_ms = e0.elapsed_time(e1)
+    n = args.steps
+    nw = max(1, min(args.warmup, 3))
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nw + n)]
+    for i in range(nw):
+        ev[i][0].record(stream)
+        job(ev[i][0])
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    timed = ev[nw:]
+    for a, b in timed:
+        flush.zero_()
+        a.record(stream)
+        job(a)
+        b.record(stream)
+    torch.cuda.synchronize()
+    ms_step, value = aggregate_over_ranks(float(np.sum([a.elapsed_time(b) for a, b in timed])), n, Bg * w.T,
+                                          world, dist, dev)
+    h2d = sum(x.numel() * x.element_size() for p in pin for x in p)
+    d2h = sum(x.numel() * x.element_size() for x in houts)
+    return {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": ms_step, "pipeline": f"{ng} row groups, one cache each, each decoded once prefilled",
+            "h2d_alone": {"ms": h2d_alone_ms, "gbs": h2d / (h2d_alone_ms / 1e3) / 1e9,
+                          "what": "one copy of every input buffer from pinned host memory, nothing else running"}}
+
+
 # ------------------------------------------------------------ oracle timing
 
 CPU_SAMPLE_STEPS = 65536  # decode steps of the oracle sample (the long stream's first 65,536)
@@ -738,6 +838,10 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-row-groups", type=int, default=8, help="prompt row groups copied/prefilled in turn")
     ap.add_argument("--e2e-step-groups", type=int, default=4, help="decode step groups copied/decoded in turn")
+    ap.add_argument("--e2e-pipeline", choices=["auto", "rows", "steps"], default="auto",
+                    help="end-to-end leg: one cache per row group, each decoded once prefilled (rows), or one "
+                         "cache whose decode waits for every row's prefill (steps); auto: rows for prompts of "
+                         f"at least {E2E_ROWS_MIN_PROMPT} tokens")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3:

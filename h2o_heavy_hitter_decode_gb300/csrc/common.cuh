@@ -115,6 +115,17 @@ template <typename T, int N> __device__ __forceinline__ void load_f32_nc(const T
   for (int i = 0; i < N / V; ++i) Unpack<T>::run(ld_nc16(p + i * V), x + i * V);
 }
 
+// a[i] = p * x[i] + a[i] for a pair (i = 0, 1): one packed fp32 FMA
+// instruction, each lane rounded as a scalar fmaf would be.
+__device__ __forceinline__ void fma_pair(float &a0, float &a1, float p, float x0, float x1) {
+  unsigned long long acc, pp, xx;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(acc) : "f"(a0), "f"(a1));
+  asm("mov.b64 %0, {%1, %1};" : "=l"(pp) : "f"(p));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(xx) : "f"(x0), "f"(x1));
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(pp), "l"(xx));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a0), "=f"(a1) : "l"(acc));
+}
+
 // Two products of packed 16-bit pairs accumulated in fp32 with the
 // mixed-precision FMA (fp32 accumulator, f16 / bf16 multiplicands): element 0
 // of each operand is its low half.  Products of two bf16 (or two f16) values

@@ -307,7 +307,7 @@ __global__ void __launch_bounds__(threads_for(NC), 7) decode_cluster_kernel(cons
               float vx[EPL];
               unpack_lane<S>(vs + r * ROWB + sub * Lane<S>::VB, vx);
 #pragma unroll
-              for (int e = 0; e < EPL; ++e) acc[e] = fmaf(pv, vx[e], acc[e]);
+              for (int e = 0; e < EPL; e += 2) fma_pair(acc[e], acc[e + 1], pv, vx[e], vx[e + 1]);
             }
           }
         };

@@ -63,18 +63,22 @@ using namespace sm100;
 constexpr int kShortChunk = 256;
 constexpr int threads_for(int nc) { return 32 * nc + 32; }  // + one producer warp
 constexpr int kMaxCluster = 8;
-constexpr int kStageBytes = 4096;  // per operand per slab
-constexpr int ring_bytes(int stages) { return stages * 2 * kStageBytes; }
+// Bytes per operand per slab: 4 KB for the lane-group layout; 8 KB (32 rows)
+// for the wide-row layout (W), where one warp takes a whole slab.
+constexpr int stage_bytes(bool wide) { return wide ? 8192 : 4096; }
+constexpr int ring_bytes(int stages, bool wide = false) { return stages * 2 * stage_bytes(wide); }
 constexpr int kResidentMaxBytes = 96 * 1024;  // K+V rows of one CTA kept in shared memory
 
-template <typename S, int D, int NC> struct Geo {
+template <typename S, int D, int NC, bool W = false> struct Geo {
   static constexpr int EPL = Lane<S>::VB / (int)sizeof(S);  // elements per lane per load
   static constexpr int LPR = D / EPL;
   static constexpr int RPW = 32 / LPR;
   static constexpr int ROWB = D * (int)sizeof(S);
-  static constexpr int TR = kStageBytes / ROWB;  // rows per slab
-  static constexpr int ITER = TR / (NC * RPW);
-  static_assert(ITER >= 1 && TR % (NC * RPW) == 0, "slab must split evenly over warps");
+  static constexpr int SB = stage_bytes(W);
+  static constexpr int TR = SB / ROWB;  // rows per slab
+  static constexpr int ITER = W ? 1 : TR / (NC * RPW);
+  static_assert(W ? (TR == 32 && ROWB == 256) : (ITER >= 1 && TR % (NC * RPW) == 0),
+                "slab must split evenly over warps (wide: 32 bf16 rows of 128)");
 };
 
 struct CArgs {
@@ -90,16 +94,25 @@ template <int NC> __device__ __forceinline__ void consumers_sync() {
 }
 
 // T: type of the step inputs and outputs; S: type of the stored K/V rows;
-// NC: consumer warps.
-template <typename T, typename S, int D, bool kResident, int kStages, int NC>
-__global__ void __launch_bounds__(threads_for(NC), 7) decode_cluster_kernel(const CArgs a) {
+// NC: consumer warps; W: wide-row layout (bf16 rows of 128, see the consumer
+// loop).
+template <typename T, typename S, int D, bool kResident, int kStages, int NC, bool W>
+__global__ void __launch_bounds__(threads_for(NC), W ? (kStages == 2 ? 5 : 4) : 7)
+    decode_cluster_kernel(const CArgs a) {
   constexpr int kConsumers = NC, kConsumerThreads = 32 * NC, kThreads = threads_for(NC);
-  using G = Geo<S, D, NC>;
+  using G = Geo<S, D, NC, W>;
+  constexpr int SB = G::SB;
   constexpr bool kFp8 = is_fp8<S>();
   constexpr int EPL = G::EPL, LPR = G::LPR, RPW = G::RPW, ROWB = G::ROWB, TR = G::TR, ITER = G::ITER;
   cg::cluster_group cluster = cg::this_cluster();
   extern __shared__ __align__(1024) uint8_t smem[];
-  __shared__ uint64_t s_full[kStages], s_empty[kStages];
+  // Full barriers: one per ring stage, or (wide layout) one per stage and
+  // consumer warp: slab g signals s_full[g % kFullBars].  In the wide layout
+  // warps take slabs in turn, so a stage's consecutive slabs go to different
+  // warps; with a barrier per (stage, warp) every barrier is waited on by one
+  // warp only, in order, and no wait can run a phase ahead of its barrier.
+  constexpr int kFullBars = W ? kStages * NC : kStages;
+  __shared__ uint64_t s_full[kFullBars], s_empty[kStages];
   __shared__ uint64_t s_inbar[2];                      // step inputs landed (one phase per use)
   __shared__ __align__(16) T s_in[2][3][D];            // q, k_t, v_t of two steps
   __shared__ float s_wm[kConsumers], s_wl[kConsumers];
@@ -132,7 +145,7 @@ __global__ void __launch_bounds__(threads_for(NC), 7) decode_cluster_kernel(cons
   // compensation] (+ [K scale][V scale] for an fp8 cache)[every rank's acc
   // row, P x D, read on rank 0]
   uint8_t *kv = smem;
-  const int kv_bytes = kResident ? 2 * chunk * ROWB : ring_bytes(kStages);
+  const int kv_bytes = kResident ? 2 * chunk * ROWB : ring_bytes(kStages, W);
   float *sc = (float *)(smem + kv_bytes);
   int *ps = (int *)(sc + chunk);
   float *lg = (float *)(ps + chunk);
@@ -142,9 +155,9 @@ __global__ void __launch_bounds__(threads_for(NC), 7) decode_cluster_kernel(cons
   float *accx = (float *)(smem + ((kv_bytes + (kFp8 ? 6 : 4) * chunk * 4 + 15) & ~15));
 
   if (tid == 0) {
+    for (int i = 0; i < kFullBars; ++i) mbar_init(&s_full[i], 1);
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(&s_full[i], 1);
-      mbar_init(&s_empty[i], kConsumers);
+      mbar_init(&s_empty[i], W ? 1 : kConsumers);  // wide: one warp takes a slab
     }
     mbar_init(&s_inbar[0], 1);
     mbar_init(&s_inbar[1], 1);
@@ -221,9 +234,10 @@ __global__ void __launch_bounds__(threads_for(NC), 7) decode_cluster_kernel(cons
           if (gp >= kStages && !mbar_wait_backoff(&s_empty[st], ((gp / kStages) - 1) & 1)) return false;
           const uint32_t bytes = (uint32_t)(min(TR, step_rows - i * TR) * ROWB);
           const size_t off = (hk + s0 + (size_t)i * TR) * ROWB;
-          mbar_expect_tx(&s_full[st], 2 * bytes);
-          bulk_load(kv + st * 2 * kStageBytes, (const uint8_t *)c.K + off, bytes, &s_full[st]);
-          bulk_load(kv + st * 2 * kStageBytes + kStageBytes, (const uint8_t *)c.V + off, bytes, &s_full[st]);
+          uint64_t *fb = &s_full[gp % kFullBars];
+          mbar_expect_tx(fb, 2 * bytes);
+          bulk_load(kv + st * 2 * SB, (const uint8_t *)c.K + off, bytes, fb);
+          bulk_load(kv + st * 2 * SB + SB, (const uint8_t *)c.V + off, bytes, fb);
           ++gp;
           return true;
         };
@@ -240,11 +254,125 @@ __global__ void __launch_bounds__(threads_for(NC), 7) decode_cluster_kernel(cons
         if (!ok) {
           s_abort = 1;
           atomicOr(c.err, 1);
-          for (int j = max(0, gp - kStages); j < gp; ++j) mbar_wait(&s_full[j % kStages], (j / kStages) & 1);
+          for (int j = max(0, gp - kStages); j < gp; ++j) mbar_wait(&s_full[j % kFullBars], (j / kFullBars) & 1);
         }
       }
       g += nst;
     } else if (!aborted) {
+      if constexpr (W) {
+      // ---- consumers, wide-row layout (bf16 rows of 128): one warp takes a
+      // whole 32-row slab (warp w the slabs w, w + NC, ...).  K: each lane
+      // computes its own row's dot product with no cross-lane reduction; lane
+      // i walks the row's sixteen 16-byte chunks in an order rotated by i
+      // (chunk (c + i) mod 16 at step c), so the eight lanes of every
+      // shared-memory phase touch eight different bank groups, and holds q
+      // rotated the same way, so register indexing stays static.  V: lane i
+      // owns output dimensions 4i .. 4i+3 and takes every row's weight by one
+      // shuffle.
+      uint32_t qr[16][4];  // q chunk (c + lane) mod 16, raw bf16 pairs
+#pragma unroll
+      for (int cch = 0; cch < 16; ++cch) {
+        const uint4 u = *(const uint4 *)(in_q + (((cch + lane) & 15) << 3));
+        qr[cch][0] = u.x; qr[cch][1] = u.y; qr[cch][2] = u.z; qr[cch][3] = u.w;
+      }
+      float m = -INFINITY, l = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
+      const int nslab = kResident ? (nrows + TR - 1) / TR : nst;
+      bool ok = true;
+      for (int i = warp; i < nslab; i += kConsumers) {
+        const int gi = g + i;
+        const int st = gi % kStages;
+        const uint8_t *ks, *vs;
+        if (kResident) {
+          ks = kv + (size_t)i * TR * ROWB;
+          vs = kv + (size_t)chunk * ROWB + (size_t)i * TR * ROWB;
+        } else {
+          if (!(ok = __all_sync(0xffffffffu, mbar_wait(&s_full[gi % kFullBars], (gi / kFullBars) & 1)))) break;
+          ks = kv + st * 2 * SB;
+          vs = ks + SB;
+        }
+        const int rows = min(TR, nrows - i * TR);
+        const bool valid = lane < rows;
+        const uint8_t *krow = ks + (valid ? lane : 0) * ROWB;
+        float d4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int cch = 0; cch < 16; ++cch) {
+          const uint4 kc = *(const uint4 *)(krow + (((cch + lane) & 15) << 4));
+          float dd = d4[cch & 3];
+          dd = fma2_bf16(qr[cch][0], kc.x, dd);
+          dd = fma2_bf16(qr[cch][1], kc.y, dd);
+          dd = fma2_bf16(qr[cch][2], kc.z, dd);
+          dd = fma2_bf16(qr[cch][3], kc.w, dd);
+          d4[cch & 3] = dd;
+        }
+        float lgt = ((d4[0] + d4[1]) + (d4[2] + d4[3])) * a.qscale;
+        lgt = valid ? lgt : -INFINITY;
+        if (valid) lg[i * TR + lane] = lgt;
+        const float wmax = warp_max(lgt);
+        if (wmax > m) {  // warp-uniform: rescale only when the running max grows
+          const float sc_ = ex2(m - wmax);
+          l *= sc_;
+#pragma unroll
+          for (int u = 0; u < 4; ++u) acc[u] *= sc_;
+          m = wmax;
+        }
+        const float pr = valid ? ex2(lgt - m) : 0.f;
+        l += pr;  // this lane's row; summed over the warp at the end
+        const uint8_t *vcol = vs + lane * 8;
+        auto vrow = [&](int r) {
+          const float w = __shfl_sync(0xffffffffu, pr, r);
+          const uint2 v = *(const uint2 *)(vcol + r * ROWB);
+          fma_pair(acc[0], acc[1], w, bf16lo(v.x), bf16hi(v.x));
+          fma_pair(acc[2], acc[3], w, bf16lo(v.y), bf16hi(v.y));
+        };
+        if (rows == TR) {
+#pragma unroll
+          for (int r = 0; r < TR; ++r) vrow(r);
+        } else {
+          for (int r = 0; r < rows; ++r) vrow(r);  // warp-uniform bound: no stale row is read
+        }
+        if (!kResident) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&s_empty[st]);
+        }
+      }
+      g += nst;
+      if (!ok && lane == 0) {
+        s_abort = 1;
+        atomicOr(c.err, 1);
+      }
+      if (rank == 0 && warp == 0) {  // the new token, from the step inputs (four dimensions per lane)
+        float qv[4], kx[4], vx[4];
+        auto ld4 = [&](const T *p4, float *x) {  // four bf16 values (8 bytes)
+          const uint2 u = *(const uint2 *)p4;
+          x[0] = bf16lo(u.x); x[1] = bf16hi(u.x); x[2] = bf16lo(u.y); x[3] = bf16hi(u.y);
+        };
+        ld4(in_q + 4 * lane, qv);
+        ld4(in_k + 4 * lane, kx);
+        float dot = 0.f;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) dot = fmaf(qv[u], kx[u], dot);
+        dot = warp_sum(dot) * a.qscale;
+        if (lane == 0) s_lgnew = dot;
+        const float mn = fmaxf(m, dot);
+        const float sc_ = ex2(m - mn);
+        l *= sc_;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) acc[u] *= sc_;
+        m = mn;
+        const float pr = ex2(dot - m);
+        if (lane == 0) l += pr;
+        ld4(in_v + 4 * lane, vx);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) acc[u] = fmaf(pr, vx[u], acc[u]);
+      }
+      l = warp_sum(l);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) s_wacc[warp][4 * lane + u] = acc[u];
+      if (lane == 0) {
+        s_wm[warp] = m;
+        s_wl[warp] = l;
+      }
+      } else {
       // ---- consumers: logits and per-warp online softmax over the owned rows.
       // A lane group (LPR lanes) takes ITER rows per slab: K dot products
       // from packed q, one transposed reduction, one exp2 per lane for the
@@ -266,8 +394,8 @@ __global__ void __launch_bounds__(threads_for(NC), 7) decode_cluster_kernel(cons
           vs = kv + (size_t)chunk * ROWB + (size_t)i * TR * ROWB;
         } else {
           if (!(ok = __all_sync(0xffffffffu, mbar_wait(&s_full[st], ph)))) break;
-          ks = kv + st * 2 * kStageBytes;
-          vs = ks + kStageBytes;
+          ks = kv + st * 2 * SB;
+          vs = ks + SB;
         }
         const int rows = min(TR, nrows - i * TR);
         // One slab: full slabs (every row of the slab filled, all but a CTA's
@@ -369,6 +497,7 @@ __global__ void __launch_bounds__(threads_for(NC), 7) decode_cluster_kernel(cons
       if (lane == 0) {
         s_wm[warp] = m;
         s_wl[warp] = l;
+      }
       }
       consumers_sync<NC>();
       // merge the warps into this CTA's partial (published for rank 0)
@@ -547,14 +676,15 @@ __global__ void __launch_bounds__(threads_for(NC), 7) decode_cluster_kernel(cons
           // step: let that copy land, then overwrite the stale row in it.
           const int gpos = g + j / TR;  // ring position of that slab (g = next step's first)
           const int st = gpos % kStages;
-          if (!__all_sync(0xffffffffu, mbar_wait(&s_full[st], (gpos / kStages) & 1)) && lane == 0) s_abort = 1;
-          uint8_t *slab = kv + st * 2 * kStageBytes;
+          if (!__all_sync(0xffffffffu, mbar_wait(&s_full[gpos % kFullBars], (gpos / kFullBars) & 1)) && lane == 0)
+            s_abort = 1;
+          uint8_t *slab = kv + st * 2 * SB;
           if (kFp8) {
             store_codes<PER>(slab + (j % TR) * ROWB, lane, ck);
-            store_codes<PER>(slab + kStageBytes + (j % TR) * ROWB, lane, cv);
+            store_codes<PER>(slab + SB + (j % TR) * ROWB, lane, cv);
           } else if (grp == 0) {
             ((uint4 *)(slab + (j % TR) * ROWB))[sub] = *(const uint4 *)(in_k + sub * EPL);
-            ((uint4 *)(slab + kStageBytes + (j % TR) * ROWB))[sub] = *(const uint4 *)(in_v + sub * EPL);
+            ((uint4 *)(slab + SB + (j % TR) * ROWB))[sub] = *(const uint4 *)(in_v + sub * EPL);
           }
         }
       }
@@ -586,24 +716,24 @@ int resident_rows_ok(int chunk) {
   return 2 * chunk * row_bytes<S, D>() <= kResidentMaxBytes;
 }
 
-template <typename S, int D, bool R, int St>
+template <typename S, int D, bool R, int St, bool W = false>
 int smem_bytes(int chunk, int P) {
-  const int base = (R ? 2 * chunk * row_bytes<S, D>() : ring_bytes(St)) + slot_words<S>() * chunk * 4;
+  const int base = (R ? 2 * chunk * row_bytes<S, D>() : ring_bytes(St, W)) + slot_words<S>() * chunk * 4;
   return ((base + 15) & ~15) + P * D * 4;  // + every rank's acc row
 }
 
 int chunk_of(const CacheView &c) { return (c.k + c.nsplit - 1) / c.nsplit; }
 
-template <typename T, typename S, int D, bool R, int St, int NC>
+template <typename T, typename S, int D, bool R, int St, int NC, bool W = false>
 cudaError_t launch_cluster_t(const CacheView &c, const DecodeStep &s, int nsteps, cudaStream_t st) {
   const int P = c.nsplit;
   CArgs a{c, s, nsteps, chunk_of(c), kLog2e / sqrtf((float)D)};
-  const int smem = smem_bytes<S, D, R, St>(a.chunk, P);
+  const int smem = smem_bytes<S, D, R, St, W>(a.chunk, P);
   if (smem > 200 * 1024) return cudaErrorInvalidValue;
   static bool attr_done[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 || !attr_done[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(decode_cluster_kernel<T, S, D, R, St, NC>,
+    cudaError_t e = cudaFuncSetAttribute(decode_cluster_kernel<T, S, D, R, St, NC, W>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_done[dev] = true;
@@ -620,29 +750,29 @@ cudaError_t launch_cluster_t(const CacheView &c, const DecodeStep &s, int nsteps
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_cluster_kernel<T, S, D, R, St, NC>, a);
+  return cudaLaunchKernelEx(&cfg, decode_cluster_kernel<T, S, D, R, St, NC, W>, a);
 }
 
 // CTAs of this instance that fit on the device at once (0 on an error).
-template <typename T, typename S, int D, bool R, int St, int NC>
+template <typename T, typename S, int D, bool R, int St, int NC, bool W = false>
 long long resident_ctas(const CacheView &c, int chunk) {
   int dev = 0, sms = 0, per_sm = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-  const int smem = smem_bytes<S, D, R, St>(chunk, c.nsplit);
+  const int smem = smem_bytes<S, D, R, St, W>(chunk, c.nsplit);
   if (smem > 200 * 1024) return 0;
-  if (cudaFuncSetAttribute(decode_cluster_kernel<T, S, D, R, St, NC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(decode_cluster_kernel<T, S, D, R, St, NC, W>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            200 * 1024) != cudaSuccess)
     return 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_cluster_kernel<T, S, D, R, St, NC>,
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_cluster_kernel<T, S, D, R, St, NC, W>,
                                                     threads_for(NC), smem) != cudaSuccess)
     return 0;
   return (long long)per_sm * sms;
 }
 
-template <typename T, typename S, int D, bool R, int St, int NC>
+template <typename T, typename S, int D, bool R, int St, int NC, bool W = false>
 bool all_resident(const CacheView &c, int chunk) {
-  const long long fit = resident_ctas<T, S, D, R, St, NC>(c, chunk);
+  const long long fit = resident_ctas<T, S, D, R, St, NC, W>(c, chunk);
   return fit > 0 && (long long)c.nh * c.nsplit <= fit;
 }
 
@@ -658,10 +788,29 @@ bool resident_nc(const CacheView &c) {
 // Streaming: a 3-stage ring, unless two stages are what lets every CTA be
 // resident at once (a partial last wave of whole-run CTAs streams at a
 // fraction of the bandwidth).
+// The wide-row layout for bf16 rows of 128 (the consumer loop's W branch).
+template <typename T, typename S, int D> constexpr bool wide_rows() {
+  return std::is_same<T, __nv_bfloat16>::value && std::is_same<S, __nv_bfloat16>::value && D == 128;
+}
+
 template <typename T, typename S, int D, int NC>
 cudaError_t dispatch_nc(const CacheView &c, const DecodeStep &s, int nsteps, cudaStream_t st) {
   const int chunk = chunk_of(c);
   if (resident_nc<T, S, D, NC>(c)) return launch_cluster_t<T, S, D, true, 1, NC>(c, s, nsteps, st);
+  if constexpr (wide_rows<T, S, D>()) {
+    // Wide rows where the grid spans at least two waves (per-CTA throughput
+    // counts more than the step's latency), with two ring stages (five CTAs
+    // per SM) for clusters of four or more, whose exchanges take longer and
+    // want more CTAs to overlap them, else three.  Measured on GB300, us per
+    // step (lane groups / wide, 3 stages / wide, 2 stages): 8K prompt
+    // (clusters of 8) 101.6 / 119.6 / 91.3; OPT-30B (clusters of 2) 74.6 /
+    // 70.8 / 73.2; OPT-6.7B (one wave) 7.53 / 8.75 / 10.3.
+    const long long grid = (long long)c.nh * c.nsplit;
+    if (chunk >= 64 && grid >= 2LL * 7 * num_sms_current_device()) {
+      if (c.nsplit >= 4) return launch_cluster_t<T, S, D, false, 2, NC, true>(c, s, nsteps, st);
+      return launch_cluster_t<T, S, D, false, 3, NC, true>(c, s, nsteps, st);
+    }
+  }
   if (!all_resident<T, S, D, false, 3, NC>(c, chunk) && all_resident<T, S, D, false, 2, NC>(c, chunk))
     return launch_cluster_t<T, S, D, false, 2, NC>(c, s, nsteps, st);
   return launch_cluster_t<T, S, D, false, 3, NC>(c, s, nsteps, st);

@@ -229,3 +229,21 @@ def test_long_stream_scores_stay_accurate():
     print("max score", max(o.values()), "max rel err", rel)
     assert rel <= 1e-5, rel
     c.check_device_error()
+
+
+# Grids of at least two waves of bf16 rows of 128 take the wide-row decode
+# layout (one row per lane for the K dot products, 32-row slabs taken by the
+# consumer warps in turn): with two ring stages for clusters of four or more
+# CTAs per head, three below.  Every head, ragged last slabs.
+WIDE = [
+    small("bf16_wide_rows_2_stages", 16, 34, 128, 1100, 24, 501, 500, "bf16"),   # clusters of 4, 251 slots
+    small("bf16_wide_rows_3_stages", 8, 138, 128, 520, 24, 205, 200, "bf16"),   # clusters of 2, 203 slots
+]
+
+
+@pytest.mark.parametrize("w", WIDE, ids=lambda w: w.name)
+def test_wide_row_decode_all_heads(w):
+    rep, cache = run_parity(w)
+    print(w.name, rep)
+    assert cache.decode_form_used() == "cluster"
+    assert rep.steps_compared >= w.T

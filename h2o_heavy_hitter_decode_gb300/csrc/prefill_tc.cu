@@ -589,20 +589,25 @@ __global__ void __launch_bounds__(kPairThreads, 1)
 // every streamed query tile (B operand, a four-stage TMA ring).  For query
 // tile j the MMA warp issues S^T_a(j) and S^T_b(j) into per-key-tile double
 // TMEM accumulators (512 columns: a0, a1, b0, b1), so the tensor core works
-// on one key tile while the other key tile's epilogue runs.  Warps 0-3 are
-// key tile a's epilogue and warps 4-7 key tile b's, one thread per key row
-// (TMEM lane), all 128 query columns of a tile: each thread adds
-// exp2(s * log2(e)/sqrt(d) - LSE_q * log2(e)) over the columns into its own
-// running sum (fixed order: deterministic, no atomics).  The load warp stages
+// on one key tile while the other key tile's epilogue runs.  Warps 0-7 are
+// key tile a's epilogue and warps 8-15 key tile b's: two threads per key row
+// (TMEM lane), 64 query columns each, each adding
+// exp2(s * log2(e)/sqrt(d) - LSE_q * log2(e)) over its columns into its own
+// running sum; the two halves of a row are added once at the end (fixed
+// order: deterministic, no atomics).  Warp 16 issues the MMAs, warp 17
+// loads.  The load warp stages
 // -LSE * log2(e) of each query tile beside its Q tile (-inf past L, so the
 // zero-filled rows add nothing).  Key tile a reads query tiles a .. nqt-1,
 // key tile b query tiles b .. nqt-1; the first tile of each is its diagonal
 // (query column c visible iff c >= key row).
 constexpr int kCsStages = 4;
+constexpr int kCsEpiWarps = 16;  // 8 per key tile: 2 per TMEM lane quarter, 64 columns each
+constexpr int kCsMmaWarp = 16, kCsLoadWarp = 17;
+constexpr int kCsThreads = 32 * 18;
 
 template <int D> struct CsGeo {
   static constexpr int kTile = TileGeo<D>::kTileBytes;
-  static constexpr int kSmem = kTile * (2 + kCsStages) + kCsStages * kRows * 4 + 256 + 1024;
+  static constexpr int kSmem = kTile * (2 + kCsStages) + kCsStages * kRows * 4 + 2 * kRows * 4 + 256 + 1024;
 };
 
 struct __align__(8) CsState {
@@ -614,7 +619,7 @@ struct __align__(8) CsState {
 };
 
 template <int D>
-__global__ void __launch_bounds__(kPairThreads, 1)
+__global__ void __launch_bounds__(kCsThreads, 1)
     colsum_pair_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const float *__restrict__ lse, float *__restrict__ colsum, int L, int nqt, int npair,
                    float qscale, int *err) {
@@ -625,7 +630,8 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   uint8_t *sK = smem;                                     // key tiles a, b
   uint8_t *sQ = smem + 2 * kT;                            // query ring
   float *sNl = (float *)(smem + (2 + kCsStages) * kT);    // [stage][128] -LSE*log2(e)
-  CsState &st = *(CsState *)(sNl + kCsStages * kRows);
+  float *sXch = sNl + kCsStages * kRows;                   // [2][128] upper-half sums of the key rows
+  CsState &st = *(CsState *)(sXch + 2 * kRows);
   if (*(volatile int *)err) return;
   // Head-major (a head's CTAs share its Q tiles in L2), heaviest pair first.
   const int h = blockIdx.x / npair, pr = npair - 1 - blockIdx.x % npair;
@@ -633,17 +639,18 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   const bool has_b = ktb < nqt;
   const int n = nqt - kta;  // query tiles streamed: kta .. nqt-1 (key tile b skips the first)
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  float cs_acc = 0.f;  // this thread's key-row sum (epilogue warps)
 
   if (tid == 0) {
     mbar_init(&st.k_full, 1);
     for (int s = 0; s < kCsStages; ++s) {
       mbar_init(&st.q_full[s], 2);       // TMA bytes + the load warp's -LSE vector
-      mbar_init(&st.q_empty[s], 1 + 8);  // the MMAs' commit + every epilogue warp
+      mbar_init(&st.q_empty[s], 1 + kCsEpiWarps);  // the MMAs' commit + every epilogue warp
     }
     for (int t = 0; t < 2; ++t)
       for (int b = 0; b < 2; ++b) {
         mbar_init(&st.acc_full[t][b], 1);
-        mbar_init(&st.acc_empty[t][b], 4);
+        mbar_init(&st.acc_empty[t][b], kCsEpiWarps / 2);
       }
     mbar_init(&st.drain, 1);
     st.abort = 0;
@@ -659,7 +666,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   const uint32_t tbase = st.tmem_base;
   auto tAcc = [&](int t, int b) { return tbase + (uint32_t)((t * 2 + b) * 128); };
 
-  if (warp == kPairLoadWarp) {
+  if (warp == kCsLoadWarp) {
     // ------------------------------------------------------------- loads
     bool ok = true;
     int issued = 0;
@@ -698,7 +705,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       for (int i = issued > kCsStages ? issued - kCsStages : 0; i < issued; ++i)
         mbar_wait(&st.q_full[i % kCsStages], (i / kCsStages) & 1);
     }
-  } else if (warp == kPairMmaWarp) {
+  } else if (warp == kCsMmaWarp) {
     // -------------------------------------------------------------- MMAs
     if (lane == 0) {
       bool ok = mbar_wait(&st.k_full, 0);
@@ -728,19 +735,20 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     }
   } else {
     // ---------------------------------------------------------- epilogue
-    const int t = warp >> 2;        // key tile
-    const int quarter = warp & 3;   // TMEM lanes 32*quarter ..
+    const int t = warp >> 3;           // key tile
+    const int half = (warp >> 2) & 1;  // query columns 64*half ..
+    const int quarter = warp & 3;      // TMEM lanes 32*quarter ..
     const int row = quarter * 32 + lane;
     const int kt = t ? ktb : kta;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    float acc = 0.f;
+    float &acc = cs_acc;
     bool ok = true;
     {
       for (int i = 0; i < n; ++i) {
         const int s = i % kCsStages;
         if (t == 1 && (i == 0 || !has_b)) {
           // the first query tile belongs to key tile a only (and without a key
-          // tile b none does): release the stage, every use counts 8 warps
+          // tile b none does): release the stage, every use counts 16 warps
           __syncwarp();
           if (lane == 0) mbar_arrive(&st.q_empty[s]);
           continue;
@@ -750,13 +758,11 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                    wait_warp(&st.q_full[s], (i / kCsStages) & 1)))
           break;
         tc_fence_after();
-        // Two halves of 64 columns: the second half's TMEM load is in flight
-        // while the first half is summed.
-        const uint32_t ta = tAcc(t, it & 1) + lane_off;
-        uint32_t r[64], r2[64];
-        tmem_ld64(ta, r);
-        tmem_ld32(ta + 64, *reinterpret_cast<uint32_t(*)[32]>(&r2[0]));
-        tmem_ld32(ta + 96, *reinterpret_cast<uint32_t(*)[32]>(&r2[32]));
+        uint32_t r[64];
+        tmem_ld64(tAcc(t, it & 1) + lane_off + (uint32_t)(half * 64), r);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&st.acc_empty[t][it & 1]);  // the accumulator is in registers
         const float4 *nl4 = reinterpret_cast<const float4 *>(sNl + s * kRows);
         float a4[4] = {0.f, 0.f, 0.f, 0.f};  // four partial sums: short dependency chains
         // columns c0 .. c0+63 from v; on the diagonal column c counts iff c >= key row
@@ -783,29 +789,24 @@ __global__ void __launch_bounds__(kPairThreads, 1)
             }
           }
         };
-        sum64(r, 0);
-        tmem_ld_wait();
-        tmem_regs_ready(*reinterpret_cast<uint32_t(*)[32]>(&r2[0]));
-        tmem_regs_ready(*reinterpret_cast<uint32_t(*)[32]>(&r2[32]));
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&st.acc_empty[t][it & 1]);  // the accumulator is in registers
-        sum64(r2, 64);
+        sum64(r, half * 64);
         acc += (a4[0] + a4[1]) + (a4[2] + a4[3]);
         __syncwarp();
         if (lane == 0) mbar_arrive(&st.q_empty[s]);  // done with this stage's -LSE vector
       }
-      if (!ok) {
-        st.abort = 1;
-      } else if (t == 0 || has_b) {
-        const int key = kt * kRows + row;
-        if (key < L) colsum[(size_t)h * L + key] = acc;
-      }
+      if (!ok) st.abort = 1;
+      else if (half == 1) sXch[t * kRows + row] = acc;  // the upper half hands its sum over
     }
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (warp < kCsEpiWarps) {
+    const int t = warp >> 3, half = (warp >> 2) & 1, row = (warp & 3) * 32 + lane;
+    const int key = (t ? ktb : kta) * kRows + row;
+    if (!st.abort && half == 0 && (t == 0 || has_b) && key < L)
+      colsum[(size_t)h * L + key] = cs_acc + sXch[t * kRows + row];
+  }
   if (st.abort && tid == 0) atomicOr(err, 4);
   if (warp == 0) tmem_dealloc(tbase, 512);
 }
@@ -856,7 +857,7 @@ cudaError_t colsum_pair_t(const CacheView &c, const void *Q, const void *K, cons
   const int nqt = (L + kRows - 1) / kRows;
   const int npair = (nqt + 1) / 2;
   const long long grid = (long long)npair * c.nh;
-  colsum_pair_tc<D><<<(unsigned)grid, kPairThreads, smem, st>>>(mq, mk, lse, colsum, L, nqt, npair,
+  colsum_pair_tc<D><<<(unsigned)grid, kCsThreads, smem, st>>>(mq, mk, lse, colsum, L, nqt, npair,
                                                                kLog2e / sqrtf((float)D), c.err);
   return cudaGetLastError();
 }

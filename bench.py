@@ -401,8 +401,8 @@ def run_ours(args, w, rank, world, local_rank):
     dec_ms = phases["decode"][0] / K
     dec_launch_ms = dec_ms / w.T  # per decode step (a multi-step form runs many steps per launch)
     form = caches[-1].decode_form_used()
-    dec_kernel = {"cluster": "decode_cluster_kernel", "cooperative": "decode_kernel",
-                  "per_step": "decode_kernel"}.get(form, "decode_kernel")
+    dec_kernel = {"cluster": "decode_cluster_kernel", "pipelined": "decode_pipe_kernel",
+                  "cooperative": "decode_kernel", "per_step": "decode_kernel"}.get(form, "decode_kernel")
     kv_gbs = kv_read_bytes(wl) / (dec_launch_ms / 1e3) / 1e9
     dec_alg_gbs = decode_alg_bytes(wl) / (dec_launch_ms / 1e3) / 1e9
     cs_ms = phases["prefill_colsum"][0] / K
@@ -832,7 +832,7 @@ def parse_args(argv=None):
                     help="several ranks: B rows each (weak) or the B rows split over them (strong)")
     ap.add_argument("--prompt-len", type=int, default=None, help="override L (profiling captures)")
     ap.add_argument("--decode-steps", type=int, default=None, help="override T (profiling captures)")
-    ap.add_argument("--decode-form", default="auto", choices=["auto", "per_step", "cooperative", "cluster"])
+    ap.add_argument("--decode-form", default="auto", choices=["auto", "per_step", "cooperative", "cluster", "pipelined"])
     ap.add_argument("--kv", choices=["native", "fp8"], default="native",
                     help="K/V cache storage: the workload's dtype, or e4m3 codes with a row scale (bf16 workloads)")
     ap.add_argument("--no-e2e", action="store_true")

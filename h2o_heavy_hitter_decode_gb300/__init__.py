@@ -314,19 +314,19 @@ class H2OCache:
                     n_split=ns.value)
 
     PHASES = ("prefill_attn", "prefill_colsum", "prefill_select", "decode")
-    DECODE_FORMS = {"auto": 0, "per_step": 1, "cooperative": 2, "cluster": 3}
+    DECODE_FORMS = {"auto": 0, "per_step": 1, "cooperative": 2, "cluster": 3, "pipelined": 4}
 
     def set_decode_form(self, form):
-        """How multi-step decode runs: "auto", "per_step", "cooperative" or
-        "cluster" (see h2o_set_decode_form)."""
+        """How multi-step decode runs: "auto", "per_step", "cooperative",
+        "cluster" or "pipelined" (see h2o_set_decode_form)."""
         f = self.DECODE_FORMS[form] if isinstance(form, str) else int(form)
         _check(lib().h2o_set_decode_form(self._h, f), "h2o_set_decode_form")
 
     def decode_form_used(self) -> str:
-        """Form of the last decode call: "per_step", "cooperative", "cluster" or "" (none yet)."""
+        """Form of the last decode call: "per_step", "cooperative", "cluster", "pipelined" or "" (none yet)."""
         f = C.c_int32()
         _check(lib().h2o_decode_form_used(self._h, C.byref(f)), "h2o_decode_form_used")
-        return {0: "", 1: "per_step", 2: "cooperative", 3: "cluster"}[f.value]
+        return {0: "", 1: "per_step", 2: "cooperative", 3: "cluster", 4: "pipelined"}[f.value]
 
     def set_policy(self, n_sink: int = 0, score_mode: int = 0):
         """Eviction variant for later calls: ``n_sink`` pinned first positions

@@ -337,9 +337,12 @@ h2o_status h2o_decode_steps(h2o_cache_t c, int n, const void *q, const void *k, 
   // launch per step.
   const int form = c->decode_form;
   const bool cluster_ok = n >= 2 && decode_cluster_supported(vc);
+  const bool pipe_ok = n >= 2 && decode_pipe_supported(vc);
   const bool coop_ok = n >= 2 && (form == 0 || form == 2) && decode_persistent_fits(c->view);
-  bool use_cluster = false, use_coop = false;
-  if (form == 3) {
+  bool use_cluster = false, use_pipe = false, use_coop = false;
+  if (form == 4) {
+    use_pipe = pipe_ok;
+  } else if (form == 3) {
     use_cluster = cluster_ok;
   } else if (form == 2) {
     use_coop = coop_ok;
@@ -349,10 +352,11 @@ h2o_status h2o_decode_steps(h2o_cache_t c, int n, const void *q, const void *k, 
     else if (coop_ok)
       use_coop = true;
   }
-  if (n >= 2 && ((form == 3 && !use_cluster) || (form == 2 && !use_coop))) return H2O_EUNSUPPORTED;
-  PhaseTimer pt(c, 3, use_cluster ? 1 : use_coop ? (n + 16383) / 16384 : n);
-  c->form_used = use_cluster ? 3 : use_coop ? 2 : 1;
-  if (use_cluster) {
+  if (n >= 2 && ((form == 4 && !use_pipe) || (form == 3 && !use_cluster) || (form == 2 && !use_coop)))
+    return H2O_EUNSUPPORTED;
+  PhaseTimer pt(c, 3, use_cluster || use_pipe ? 1 : use_coop ? (n + 16383) / 16384 : n);
+  c->form_used = use_pipe ? 4 : use_cluster ? 3 : use_coop ? 2 : 1;
+  if (use_cluster || use_pipe) {
     DecodeStep s;
     s.q = q;
     s.kn = k;
@@ -361,7 +365,7 @@ h2o_status h2o_decode_steps(h2o_cache_t c, int n, const void *q, const void *k, 
     s.evicted = evicted;
     s.n_valid = c->n_valid;
     s.p = (int)c->next_pos;
-    cudaError_t e = launch_decode_cluster(vc, s, n, c->stream);
+    cudaError_t e = use_pipe ? launch_decode_pipe(vc, s, n, c->stream) : launch_decode_cluster(vc, s, n, c->stream);
     if (e != cudaSuccess) return cuda_fail(e);
     c->next_pos += n;
     c->n_valid = (int)((int64_t)c->n_valid + n < c->k ? c->n_valid + n : c->k);
@@ -412,7 +416,7 @@ h2o_status h2o_decode_step(h2o_cache_t c, const void *q, const void *k, const vo
 }
 
 h2o_status h2o_set_decode_form(h2o_cache_t c, int form) {
-  if (!c || form < 0 || form > 3) return H2O_EINVAL;
+  if (!c || form < 0 || form > 4) return H2O_EINVAL;
   c->decode_form = form;
   return H2O_OK;
 }

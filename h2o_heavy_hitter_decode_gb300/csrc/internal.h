@@ -55,6 +55,10 @@ bool decode_cluster_resident(const CacheView &c);  // each CTA's K/V rows stay i
 // slots on `sms` SMs.
 int decode_cluster_size(int nh, int k, int sms);
 cudaError_t launch_decode_cluster(const CacheView &c, const DecodeStep &s, int nsteps, cudaStream_t st);
+// The cluster form with each step's eviction decision taken while the next
+// step's attention pass runs (decode_pipe.cu); same cluster size and layout.
+bool decode_pipe_supported(const CacheView &c);
+cudaError_t launch_decode_pipe(const CacheView &c, const DecodeStep &s, int nsteps, cudaStream_t st);
 // Split count of the decode launch for nh heads of k slots on `sms` SMs
 // (fixes the size of the split-partial scratch).
 int decode_splits(int nh, int k, int sms);

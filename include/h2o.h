@@ -140,11 +140,16 @@ h2o_status h2o_decode_steps(h2o_cache_t cache, int n, const void *q, const void 
  *      candidates move over distributed shared memory (asynchronous stores
  *      completing on the receivers' mbarriers), every CTA takes the same
  *      decision; no global scratch.
+ *   4  form 3 with each step's eviction decision taken while the next
+ *      step's attention pass runs: the next pass covers the cache before the
+ *      decision, and the decision's one changed slot is then corrected in
+ *      its partial (the evicted row's term removed, the admitted row's
+ *      added).  Same results as the other forms up to fp32 rounding.
  * A form the shape or device cannot run makes h2o_decode_steps return
  * H2O_EUNSUPPORTED (nothing launched). */
 h2o_status h2o_set_decode_form(h2o_cache_t cache, int form);
 
-/* The form (1, 2 or 3 as above) the last decode call of this cache ran with;
+/* The form (1 to 4 as above) the last decode call of this cache ran with;
  * 0 before any decode call. */
 h2o_status h2o_decode_form_used(h2o_cache_t cache, int *form);
 

@@ -32,7 +32,7 @@ CASES = [
 ]
 
 
-@pytest.mark.parametrize("form", ["per_step", "cooperative", "cluster"])
+@pytest.mark.parametrize("form", ["per_step", "cooperative", "cluster", "pipelined"])
 @pytest.mark.parametrize("w", CASES, ids=lambda w: w.name)
 def test_fp8_all_heads(w, form):
     rep, cache = run_parity(w, decode_form=form, kv_fp8=True)
@@ -40,7 +40,7 @@ def test_fp8_all_heads(w, form):
     assert rep.steps_compared >= w.T
 
 
-@pytest.mark.parametrize("form", ["per_step", "cluster"])
+@pytest.mark.parametrize("form", ["per_step", "cluster", "pipelined"])
 def test_fp8_with_policy(form):
     w = small("fp8_sinks_mean", 2, 3, 128, 300, 40, 64, 64)
     rep, cache = run_parity(w, decode_form=form, kv_fp8=True, policy=(8, 1))
@@ -51,12 +51,13 @@ def test_fp8_with_policy(form):
 @pytest.mark.parametrize("w", [small("fp8_cluster_long_chunks_resident", 1, 2, 128, 2600, 24, 1300, 1100),
                                small("fp8_d64_cluster_long_chunks_resident", 1, 2, 64, 2500, 24, 1200, 1200)],
                          ids=lambda w: w.name)
-def test_fp8_cluster_long_chunks(w):
+@pytest.mark.parametrize("form", ["cluster", "pipelined"])
+def test_fp8_cluster_long_chunks(w, form):
     """300 fp8 slots per cluster CTA: their rows (77 KB or 38 KB of codes) stay
     resident in shared memory and four consumer warps read them."""
-    rep, cache = run_parity(w, decode_form="cluster", kv_fp8=True)
-    print(w.name, rep)
-    assert cache.decode_form_used() == "cluster"
+    rep, cache = run_parity(w, decode_form=form, kv_fp8=True)
+    print(w.name, form, rep)
+    assert cache.decode_form_used() == form
     assert -(-w.k // min(cache.info()["n_split"], 8)) > 256  # slots per CTA
     assert rep.steps_compared >= w.T
 

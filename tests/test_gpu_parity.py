@@ -65,7 +65,7 @@ FORM_CASES = [SMALL[0], SMALL[1], SMALL[2], SMALL[3], SMALL[6], SMALL[9],
               small("bf16_many_heads_long_budget", 4, 6, 128, 700, 40, 200, 100, "bf16")]
 
 
-@pytest.mark.parametrize("form", ["per_step", "cooperative", "cluster"])
+@pytest.mark.parametrize("form", ["per_step", "cooperative", "cluster", "pipelined"])
 @pytest.mark.parametrize("w", FORM_CASES, ids=lambda w: w.name)
 def test_decode_forms(w, form):
     """Every multi-step decode form (per-step launches, cooperative
@@ -87,11 +87,12 @@ LONG_CHUNKS = [
 ]
 
 
+@pytest.mark.parametrize("form", ["cluster", "pipelined"])
 @pytest.mark.parametrize("w", LONG_CHUNKS, ids=lambda w: w.name)
-def test_cluster_long_chunks(w):
-    rep, cache = run_parity(w, decode_form="cluster")
-    print(w.name, rep)
-    assert cache.decode_form_used() == "cluster"
+def test_cluster_long_chunks(w, form):
+    rep, cache = run_parity(w, decode_form=form)
+    print(w.name, form, rep)
+    assert cache.decode_form_used() == form
     assert -(-w.k // min(cache.info()["n_split"], 8)) > 256  # slots per CTA
     assert rep.steps_compared >= w.T
 
@@ -241,9 +242,10 @@ WIDE = [
 ]
 
 
+@pytest.mark.parametrize("form", ["cluster", "pipelined"])
 @pytest.mark.parametrize("w", WIDE, ids=lambda w: w.name)
-def test_wide_row_decode_all_heads(w):
-    rep, cache = run_parity(w)
-    print(w.name, rep)
-    assert cache.decode_form_used() == "cluster"
+def test_wide_row_decode_all_heads(w, form):
+    rep, cache = run_parity(w, decode_form=form)
+    print(w.name, form, rep)
+    assert cache.decode_form_used() == form
     assert rep.steps_compared >= w.T

@@ -33,7 +33,7 @@ CASES = [
 PARAMS = [(w, pol) for w, pols in CASES for pol in pols]
 
 
-@pytest.mark.parametrize("form", ["per_step", "cooperative", "cluster"])
+@pytest.mark.parametrize("form", ["per_step", "cooperative", "cluster", "pipelined"])
 @pytest.mark.parametrize("w,policy", PARAMS, ids=[f"{w.name}-sink{p[0]}-mode{p[1]}" for w, p in PARAMS])
 def test_policy_all_heads(w, policy, form):
     rep, cache = run_parity(w, decode_form=form, policy=policy)

@@ -31,25 +31,25 @@ def _check(case, **kw):
     return rep, cache
 
 
-@pytest.mark.parametrize("form", ["per_step", "cooperative", "cluster"])
+@pytest.mark.parametrize("form", ["per_step", "cooperative", "cluster", "pipelined"])
 @pytest.mark.parametrize("case", TIE_CASES, ids=lambda c: c[0].name)
 def test_exact_ties_every_form(case, form):
     _, cache = _check(case, decode_form=form)
     assert cache.decode_form_used() == form
 
 
-@pytest.mark.parametrize("form", ["cooperative", "cluster"])
+@pytest.mark.parametrize("form", ["cooperative", "cluster", "pipelined"])
 def test_exact_ties_long_chunks(form):
     _check(TIE_LONG, decode_form=form)
 
 
-@pytest.mark.parametrize("form", ["per_step", "cluster"])
+@pytest.mark.parametrize("form", ["per_step", "cluster", "pipelined"])
 @pytest.mark.parametrize("case", [TIE_CASES[0], TIE_CASES[2]], ids=lambda c: c[0].name)
 def test_exact_ties_fp8_cache(case, form):
     _check(case, decode_form=form, kv_fp8=True)
 
 
 @pytest.mark.parametrize("policy", [(4, 0), (0, 1), (3, 1)], ids=["sinks", "mean", "sinks_mean"])
-@pytest.mark.parametrize("form", ["cooperative", "cluster"])
+@pytest.mark.parametrize("form", ["cooperative", "cluster", "pipelined"])
 def test_exact_ties_policies(policy, form):
     _check(TIE_CASES[0], decode_form=form, policy=policy)

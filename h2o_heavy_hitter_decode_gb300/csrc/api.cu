@@ -331,10 +331,6 @@ h2o_status h2o_decode_steps(h2o_cache_t c, int n, const void *q, const void *k, 
   const size_t step = (size_t)c->nh * c->d * c->esize;
   CacheView vc = c->view;  // cluster form: one cluster of <= 8 CTAs per head
   vc.nsplit = decode_cluster_size(c->nh, c->k, num_sms_current_device());
-  // Automatic choice (measured on GB300 with the cluster size above: the
-  // cluster form was the fastest on every workload): the cluster form, else
-  // the cooperative grid when all (head, split) CTAs fit at once, else one
-  // launch per step.
   const int form = c->decode_form;
   const bool cluster_ok = n >= 2 && decode_cluster_supported(vc);
   const bool pipe_ok = n >= 2 && decode_pipe_supported(vc);
@@ -347,7 +343,17 @@ h2o_status h2o_decode_steps(h2o_cache_t c, int n, const void *q, const void *k, 
   } else if (form == 2) {
     use_coop = coop_ok;
   } else if (form == 0) {
-    if (cluster_ok)
+    // Automatic: the pipelined cluster form where the rows stream through
+    // the slab ring, the plain cluster form where they stay resident in
+    // shared memory (there the per-step exchange chain, not the attention
+    // pass, bounds a step, and the pipelined form's single protocol warp
+    // makes that chain no shorter), else the cooperative grid, else one
+    // launch per step.  Measured on GB300, us per step (cluster /
+    // pipelined): 8K prompt 90.1 / 77.7, OPT-30B 69.3 / 64.6, OPT-6.7B
+    // 7.33 / 6.92, long stream (resident) 2.51 / 2.57.
+    if (pipe_ok && !decode_cluster_resident(vc))
+      use_pipe = true;
+    else if (cluster_ok)
       use_cluster = true;
     else if (coop_ok)
       use_coop = true;

@@ -16,9 +16,10 @@
 //     softmax) over the rows of S_{t-1}: the slabs carry every decision up to
 //     step t-3, and the slot that step t-2 changed is read from that
 //     decision's pending copy of its new row;
-//   * meanwhile one warp (the protocol warp, which also feeds the slab ring)
-//     finishes step t-1: (m, l) exchange, exact weights into the scores,
-//     argmin, candidate exchange, decision;
+//   * meanwhile one warp (the protocol warp) finishes step t-1: (m, l)
+//     exchange, exact weights into the scores, argmin, candidate exchange,
+//     decision; a producer warp feeds the slab ring and writes decisions
+//     back to the cache rows;
 //   * when the consumers hand over step t's partial (m, l, acc), the protocol
 //     warp applies decision t-1 to it: it removes the evicted row's term (its
 //     logit at step t is in the step's logit buffer; its V row was saved at
@@ -28,7 +29,7 @@
 // CTA's partial mass.  When it is more (the entry evicted as the least
 // attended takes most of the next query's attention in this CTA), the CTA's
 // partial is recomputed from the step's stored logits and the V rows.
-// Decisions reach the cache rows in HBM three steps late: the protocol warp
+// Decisions reach the cache rows in HBM three steps late: the producer warp
 // writes decision u's row only after every slab of step u+1 has landed (those
 // must still see the old row) and before it issues the first slab of step
 // u+3.  A CTA whose rows stay resident in shared memory writes HBM at the
@@ -50,7 +51,7 @@ namespace {
 using namespace sm100;
 
 constexpr int kShortChunk = 256;                                 // <= : two consumer warps, else four
-constexpr int threads_for(int nc) { return 32 * nc + 32; }        // + the protocol warp
+constexpr int threads_for(int nc) { return 32 * nc + 64; }        // + the protocol and producer warps
 constexpr int kMaxCluster = 8;
 constexpr int stage_bytes(bool wide) { return wide ? 8192 : 4096; }
 constexpr int ring_bytes(int stages, bool wide = false) { return stages * 2 * stage_bytes(wide); }
@@ -105,6 +106,15 @@ template <typename S, int N> __device__ __forceinline__ void row_part(const void
   }
 }
 
+// Warp maximum of a float by one integer min/max reduction: the bit
+// pattern, with the magnitude bits of negative values flipped, orders like
+// the value (-inf lowest; no NaN arrives here).
+__device__ __forceinline__ float warp_max_ordered(float v) {
+  const int i = __float_as_int(v);
+  const int k = __reduce_max_sync(0xffffffffu, i >= 0 ? i : i ^ 0x7fffffff);
+  return __int_as_float(k >= 0 ? k : k ^ 0x7fffffff);
+}
+
 // Warp copy of `bytes` (a multiple of 64) from src to dst, 4-byte words.
 __device__ __forceinline__ void warp_copy(void *dst, const void *src, int bytes, int lane) {
   for (int o = lane * 4; o < bytes; o += 128) *(uint32_t *)((uint8_t *)dst + o) = *(const uint32_t *)((const uint8_t *)src + o);
@@ -113,7 +123,7 @@ __device__ __forceinline__ void warp_copy(void *dst, const void *src, int bytes,
 // T: type of the step inputs and outputs; S: type of the stored K/V rows;
 // NC: consumer warps; W: wide-row layout (bf16 rows of 128).
 template <typename T, typename S, int D, bool kResident, int kStages, int NC, bool W>
-__global__ void __launch_bounds__(threads_for(NC), W ? (kStages == 2 ? 5 : 4) : 7)
+__global__ void __launch_bounds__(threads_for(NC), W ? (kStages == 2 ? 4 : 3) : (NC == 2 ? 7 : 5))
     decode_pipe_kernel(const PArgs a) {
   constexpr int kThreads = threads_for(NC);
   using G = Geo<S, D, NC, W>;
@@ -147,7 +157,7 @@ __global__ void __launch_bounds__(threads_for(NC), W ? (kStages == 2 ? 5 : 4) : 
   __shared__ float s_pksc[kBufs], s_pvsc[kBufs];
   __shared__ __align__(16) uint8_t s_pend[kBufs][2][ROWB];
   __shared__ __align__(16) uint8_t s_oldrow[ROWB];  // the evicted slot's V row (streaming form)
-  __shared__ int s_gfirst[4];                       // ring position of step u's first slab
+  __shared__ int s_tp, s_pw;  // decisions made; decisions written back to the cache rows in HBM
   __shared__ int s_abort;
 
   const CacheView &c = a.c;
@@ -197,6 +207,8 @@ __global__ void __launch_bounds__(threads_for(NC), W ? (kStages == 2 ? 5 : 4) : 
     mbar_init(&s_bacc, 1);
     mbar_init(&s_bcand, 1);
     s_abort = 0;
+    s_tp = 0;
+    s_pw = 0;
     fence_mbar_init();
   }
   for (int j = tid; j < own; j += kThreads) {
@@ -281,7 +293,9 @@ __global__ void __launch_bounds__(threads_for(NC), W ? (kStages == 2 ? 5 : 4) : 
           const uint4 u = *(const uint4 *)(in_q + (((cch + lane) & 15) << 3));
           qr[cch][0] = u.x; qr[cch][1] = u.y; qr[cch][2] = u.z; qr[cch][3] = u.w;
         }
-        float m = -INFINITY, l = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
+        // two accumulator sets (even and odd rows) halve the dependent chain
+        // of the V rows' FMAs
+        float m = -INFINITY, l = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};
         for (int i = (warp + NC - g % NC) % NC; i < nslab; i += NC) {
           const int gi = g + i;
           const int st = gi % kStages;
@@ -313,12 +327,15 @@ __global__ void __launch_bounds__(threads_for(NC), W ? (kStages == 2 ? 5 : 4) : 
           float lgt = ((d4[0] + d4[1]) + (d4[2] + d4[3])) * a.qscale;
           lgt = valid ? lgt : -INFINITY;
           if (valid) lg[i * TR + lane] = lgt;
-          const float wmax = warp_max(lgt);
+          const float wmax = warp_max_ordered(lgt);
           if (wmax > m) {
             const float sc_ = ex2(m - wmax);
             l *= sc_;
 #pragma unroll
-            for (int u = 0; u < 4; ++u) acc[u] *= sc_;
+            for (int u = 0; u < 4; ++u) {
+              acc[u] *= sc_;
+              acc2[u] *= sc_;
+            }
             m = wmax;
           }
           const float pr = valid ? ex2(lgt - m) : 0.f;
@@ -328,8 +345,9 @@ __global__ void __launch_bounds__(threads_for(NC), W ? (kStages == 2 ? 5 : 4) : 
           auto vrow = [&](int r) {
             const float w = __shfl_sync(FULL, pwv, r);
             const uint2 v = *(const uint2 *)(vcol + r * ROWB);
-            fma_pair(acc[0], acc[1], w, bf16lo(v.x), bf16hi(v.x));
-            fma_pair(acc[2], acc[3], w, bf16lo(v.y), bf16hi(v.y));
+            float *ac = (r & 1) ? acc2 : acc;
+            fma_pair(ac[0], ac[1], w, bf16lo(v.x), bf16hi(v.x));
+            fma_pair(ac[2], ac[3], w, bf16lo(v.y), bf16hi(v.y));
           };
           if (rows == TR) {
 #pragma unroll
@@ -350,7 +368,7 @@ __global__ void __launch_bounds__(threads_for(NC), W ? (kStages == 2 ? 5 : 4) : 
         }
         l = warp_sum(l);
 #pragma unroll
-        for (int u = 0; u < 4; ++u) wacc[4 * lane + u] = acc[u];
+        for (int u = 0; u < 4; ++u) wacc[4 * lane + u] = acc[u] + acc2[u];
         if (lane == 0) {
           s_wm[t & 1][warp] = m;
           s_wl[t & 1][warp] = l;
@@ -394,9 +412,7 @@ __global__ void __launch_bounds__(threads_for(NC), W ? (kStages == 2 ? 5 : 4) : 
             if (kFp8) lgt *= valid ? (rm == plane ? pks : ksc[i * TR + rm]) : 0.f;
             lgt = valid ? lgt : -INFINITY;
             if (valid && sub % LPI == 0) lg[i * TR + rm] = lgt;
-            float wmax = lgt;
-#pragma unroll
-            for (int o = LPI; o < 32; o <<= 1) wmax = fmaxf(wmax, __shfl_xor_sync(FULL, wmax, o));
+            const float wmax = warp_max_ordered(lgt);  // over the warp's rows of this slab
             if (wmax > m) {
               const float sc_ = ex2(m - wmax);
               l *= sc_;
@@ -460,84 +476,13 @@ __global__ void __launch_bounds__(threads_for(NC), W ? (kStages == 2 ? 5 : 4) : 
       __syncwarp();
       if (lane == 0) mbar_arrive(&s_part[t & 1]);
     }
-  } else {
+  } else if (warp == NC) {
     // =================================================================
-    // Protocol warp: feeds the slab ring (lane 0 issues) whenever it waits,
-    // and runs every step's exchanges and decision.
+    // Protocol warp: every step's exchanges and decision.
     int tp = 0;  // decisions made
-    int pu = 0, pi = 0, gp = 0;  // ring feed: step being issued, its next slab, next ring position
-    bool prepped = false;
-    int pw = 0;  // decisions written back to the cache rows in HBM (streaming form)
     bool failed = false;
+    auto wait_bar = [&](uint64_t *bar, uint32_t par) -> bool { return __all_sync(FULL, mbar_wait(bar, par)); };
 
-    auto test = [&](uint64_t *bar, uint32_t par) -> bool { return __all_sync(FULL, mbar_test(bar, par)); };
-    // Decision u's new row to the cache rows in HBM (streaming form).
-    auto write_back = [&](int u) {
-      const int q = u % kBufs;
-      const int j = s_pslot[q];
-      if (j >= 0) {
-        const size_t off = (hk + s0 + j) * (size_t)ROWB;
-        warp_copy((uint8_t *)c.K + off, s_pend[q][0], ROWB, lane);
-        warp_copy((uint8_t *)c.V + off, s_pend[q][1], ROWB, lane);
-        asm volatile("fence.proxy.async.global;" ::: "memory");  // before later bulk reads of the row
-      }
-      __syncwarp();
-      pw = u + 1;
-    };
-    // Issue every slab the ring has room for (non-blocking).
-    auto pump = [&]() {
-      if constexpr (!kResident) {
-        while (pu < a.nsteps && !failed) {
-          if (!prepped) {
-            // Step pu's slabs must carry decisions up to pu-3 and none after:
-            // decision pu-3 is written back once every slab of step pu-2 (the
-            // last step that reads its old row from a slab) has landed and
-            // step pu-2's partial has taken the saved copy of the row it
-            // replaced (the bulk read of that row has completed).
-            if (pu >= 3 && tp < pu - 1) return;
-            if (pu >= 3) {
-              const int x1 = s_gfirst[(pu - 1) & 3];
-              for (int x = max(s_gfirst[(pu - 2) & 3], gp - kStages); x < x1; ++x)
-                if (!test(&s_full[x % kFullBars], (x / kFullBars) & 1)) return;
-              write_back(pu - 3);
-            }
-            if (lane == 0) s_gfirst[pu & 3] = gp;
-            __syncwarp();
-            prepped = true;
-            pi = 0;
-          }
-          const int rows = rows_after(pu > 0 ? pu - 1 : 0);
-          const int nst = (rows + TR - 1) / TR;
-          while (pi < nst) {
-            const int st = gp % kStages;
-            if (gp >= kStages && !test(&s_empty[st], ((gp / kStages) - 1) & 1)) return;
-            if (lane == 0) {
-              const uint32_t bytes = (uint32_t)(min(TR, rows - pi * TR) * ROWB);
-              const size_t off = (hk + s0 + (size_t)pi * TR) * ROWB;
-              uint64_t *fb = &s_full[gp % kFullBars];
-              mbar_expect_tx(fb, 2 * bytes);
-              bulk_load(kv + st * 2 * SB, (const uint8_t *)c.K + off, bytes, fb);
-              bulk_load(kv + st * 2 * SB + SB, (const uint8_t *)c.V + off, bytes, fb);
-            }
-            ++gp;
-            ++pi;
-          }
-          ++pu;
-          prepped = false;
-        }
-      }
-    };
-    // Bounded wait that keeps the ring fed.
-    auto wait_pump = [&](uint64_t *bar, uint32_t par) -> bool {
-      for (uint32_t i = 0; i < kSpinLimit; ++i) {
-        if (test(bar, par)) return true;
-        pump();
-        __nanosleep(32);
-      }
-      return false;
-    };
-
-    pump();
     for (int t = 0; t < a.nsteps && !failed; ++t) {
       if (*(volatile int *)&s_abort) {
         failed = true;
@@ -549,7 +494,7 @@ __global__ void __launch_bounds__(threads_for(NC), W ? (kStages == 2 ? 5 : 4) : 
         if (rank == 0) mbar_expect_tx(&s_bacc, P * D * 4);
       }
       const int q = t % kBufs;
-      if (!wait_pump(&s_inbar[q], (t / kBufs) & 1) || !wait_pump(&s_part[t & 1], (t >> 1) & 1)) {
+      if (!wait_bar(&s_inbar[q], (t / kBufs) & 1) || !wait_bar(&s_part[t & 1], (t >> 1) & 1)) {
         failed = true;
         break;
       }
@@ -580,7 +525,7 @@ __global__ void __launch_bounds__(threads_for(NC), W ? (kStages == 2 ? 5 : 4) : 
             if (kResident) {
               orow = kv + (size_t)chunk * ROWB + (size_t)j * ROWB;
             } else {
-              if (!wait_pump(&s_oldv, (t - 1) & 1)) {
+              if (!wait_bar(&s_oldv, (t - 1) & 1)) {
                 failed = true;
                 break;
               }
@@ -692,7 +637,7 @@ __global__ void __launch_bounds__(threads_for(NC), W ? (kStages == 2 ? 5 : 4) : 
                       make_uint4(__float_as_uint(M), __float_as_uint(l), __float_as_uint(lgnew), 0u),
                       mapa(&s_bml, lane));
       }
-      if (!wait_pump(&s_bml, t & 1) || (rank == 0 && !wait_pump(&s_bacc, t & 1))) {
+      if (!wait_bar(&s_bml, t & 1) || (rank == 0 && !wait_bar(&s_bacc, t & 1))) {
         failed = true;
         break;
       }
@@ -731,6 +676,7 @@ __global__ void __launch_bounds__(threads_for(NC), W ? (kStages == 2 ? 5 : 4) : 
       const int nr = rows_after(t);
       const long long lim = (long long)p - c.kl;
       ArgMin best{INFINITY, INT_MAX, -2};
+#pragma unroll 4
       for (int j = lane; j < nr; j += 32) {
         const float w = exp2f(lg[j] - Mg) * invL;
         float s_new = sc[j], cj = cm[j];
@@ -753,7 +699,7 @@ __global__ void __launch_bounds__(threads_for(NC), W ? (kStages == 2 ? 5 : 4) : 
         st_async_v4(mapa(&s_candx[rank], lane),
                     make_uint4(__float_as_uint(best.s), (uint32_t)best.p, (uint32_t)best.slot, 0u),
                     mapa(&s_bcand, lane));
-      if (!wait_pump(&s_bcand, t & 1)) {
+      if (!wait_bar(&s_bcand, t & 1)) {
         failed = true;
         break;
       }
@@ -779,14 +725,15 @@ __global__ void __launch_bounds__(threads_for(NC), W ? (kStages == 2 ? 5 : 4) : 
       if (lane == 0 && rank == 0 && a.s.evicted) a.s.evicted[(size_t)t * c.nh + h] = ev;
       // pending buffer q is free once decision t-3 is in the cache rows
       if (!kResident) {
-        for (uint32_t i = 0; pw <= t - 3; ++i) {
+        for (uint32_t i = 0; *(volatile int *)&s_pw <= t - 3; ++i) {
           if (i >= kSpinLimit || *(volatile int *)&s_abort) {
             failed = true;
             break;
           }
-          pump();
+          __nanosleep(32);
         }
         if (failed) break;
+        __threadfence_block();
       }
       const bool mine = e >= s0 && e < s0 + own;
       const int j = e - s0;
@@ -847,6 +794,8 @@ __global__ void __launch_bounds__(threads_for(NC), W ? (kStages == 2 ? 5 : 4) : 
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(&s_dec[t & 3]);
+        __threadfence_block();
+        *(volatile int *)&s_tp = t + 1;
         if (t + kBufs < a.nsteps) fetch_inputs(t + kBufs);  // buffer q: step t is done with it
       }
       tp = t + 1;
@@ -862,21 +811,90 @@ __global__ void __launch_bounds__(threads_for(NC), W ? (kStages == 2 ? 5 : 4) : 
         vsc[j] = s_pvsc[q];
       }
     }
-    if (!kResident) {
-      // The last decisions to the cache rows in HBM, once every slab landed
-      // and the last saved V row arrived (a copy must not be in flight when
-      // the CTA exits).
-      bool drained = true;
-      for (int x = max(0, gp - kStages); x < gp; ++x)
-        drained = drained && __all_sync(FULL, mbar_wait(&s_full[x % kFullBars], (x / kFullBars) & 1));
-      if (tp > 0) drained = drained && __all_sync(FULL, mbar_wait(&s_oldv, (tp - 1) & 1));
-      if (drained && !failed)
-        for (int u = pw; u < tp; ++u) write_back(u);
-      if (!drained && lane == 0) atomicOr(c.err, 1);
-    }
     // inputs fetched for steps that never ran (an aborted call) must land too
     if (lane == 0)
       for (int u = tp; u < a.nsteps && u < tp + kBufs; ++u) mbar_wait(&s_inbar[u % kBufs], (u / kBufs) & 1);
+  } else if (!kResident) {
+    // =================================================================
+    // Producer warp (streaming form): the slabs of every step, in ring
+    // order (lane 0 issues), and each decision's row written back to the
+    // cache rows in HBM (the whole warp).
+    bool ok = true;
+    int gp = 0, pw = 0;
+    int gfirst[4] = {0, 0, 0, 0};  // ring position of the first slab of steps u-3 .. u (index u % 4)
+    // Bounded wait for `target` decisions made.
+    auto wait_decisions = [&](int target) -> bool {
+      for (uint32_t i = 0; i < kSpinLimit; ++i) {
+        if (*(volatile int *)&s_tp >= target) {
+          __threadfence_block();
+          return true;
+        }
+        if (*(volatile int *)&s_abort) return false;
+        __nanosleep(64);
+      }
+      return false;
+    };
+    auto write_back = [&](int u) {
+      const int q = u % kBufs;
+      const int j = s_pslot[q];
+      if (j >= 0) {
+        const size_t off = (hk + s0 + j) * (size_t)ROWB;
+        warp_copy((uint8_t *)c.K + off, s_pend[q][0], ROWB, lane);
+        warp_copy((uint8_t *)c.V + off, s_pend[q][1], ROWB, lane);
+        asm volatile("fence.proxy.async.global;" ::: "memory");  // before later bulk reads of the row
+      }
+      __syncwarp();
+      pw = u + 1;
+      __threadfence_block();
+      if (lane == 0) *(volatile int *)&s_pw = pw;
+    };
+    for (int u = 0; u < a.nsteps && ok; ++u) {
+      if (*(volatile int *)&s_abort) break;
+      if (u >= 3) {
+        // Step u's slabs carry decisions up to u-3 and none after.  Decision
+        // u-3 is written back once step u-2's partial has taken the saved
+        // copy of the row it replaced (decision u-2 made) and every slab of
+        // step u-2 (the last step that reads its old row from a slab) has
+        // landed.
+        ok = wait_decisions(u - 1);
+        for (int x = max(gfirst[(u - 2) & 3], gp - kStages); ok && x < gfirst[(u - 1) & 3]; ++x)
+          ok = __all_sync(FULL, mbar_wait(&s_full[x % kFullBars], (x / kFullBars) & 1));
+        if (!ok) break;
+        write_back(u - 3);
+      }
+      gfirst[u & 3] = gp;
+      const int rows = rows_after(u > 0 ? u - 1 : 0);
+      const int nst = (rows + TR - 1) / TR;
+      for (int i = 0; i < nst && ok; ++i) {
+        const int st = gp % kStages;
+        if (gp >= kStages) ok = __all_sync(FULL, mbar_wait_backoff(&s_empty[st], ((gp / kStages) - 1) & 1));
+        if (ok && lane == 0) {
+          const uint32_t bytes = (uint32_t)(min(TR, rows - i * TR) * ROWB);
+          const size_t off = (hk + s0 + (size_t)i * TR) * ROWB;
+          uint64_t *fb = &s_full[gp % kFullBars];
+          mbar_expect_tx(fb, 2 * bytes);
+          bulk_load(kv + st * 2 * SB, (const uint8_t *)c.K + off, bytes, fb);
+          bulk_load(kv + st * 2 * SB + SB, (const uint8_t *)c.V + off, bytes, fb);
+        }
+        if (ok) ++gp;
+      }
+    }
+    // Every issued slab lands before the CTA exits; the last decisions go to
+    // the cache rows once they are made and the last saved V row (a bulk
+    // read of the row being replaced) has arrived.
+    bool drained = true;
+    for (int x = max(0, gp - kStages); x < gp; ++x)
+      drained = drained && __all_sync(FULL, mbar_wait(&s_full[x % kFullBars], (x / kFullBars) & 1));
+    if (ok && drained && wait_decisions(a.nsteps)) {
+      if (__all_sync(FULL, mbar_wait(&s_oldv, (a.nsteps - 1) & 1)))
+        for (int u = pw; u < a.nsteps; ++u) write_back(u);
+      else
+        drained = false;
+    }
+    if ((!ok || !drained) && lane == 0) {
+      s_abort = 1;
+      atomicOr(c.err, 1);
+    }
   }
   __syncthreads();
   // write back the owned scores and tags; no CTA leaves while a peer could
@@ -957,7 +975,8 @@ template <typename T, typename S, int D> constexpr bool wide_rows() {
 
 // The same instance choice as the cluster form: rows resident in shared
 // memory when they fit and the grid is co-resident; the wide-row layout for
-// bf16 rows of 128 on grids of two waves or more; else lane groups with a
+// bf16 rows of 128 on grids of two waves or more (two ring stages: a third
+// would cost a CTA per SM); else lane groups with a
 // three-stage ring, or two stages when that makes the grid co-resident.
 template <typename T, typename S, int D, int NC>
 cudaError_t dispatch_nc(const CacheView &c, const DecodeStep &s, int nsteps, cudaStream_t st) {
@@ -966,10 +985,8 @@ cudaError_t dispatch_nc(const CacheView &c, const DecodeStep &s, int nsteps, cud
     return launch_t<T, S, D, true, 1, NC>(c, s, nsteps, st);
   if constexpr (wide_rows<T, S, D>()) {
     const long long grid = (long long)c.nh * c.nsplit;
-    if (chunk >= 64 && grid >= 2LL * 7 * num_sms_current_device()) {
-      if (c.nsplit >= 4) return launch_t<T, S, D, false, 2, NC, true>(c, s, nsteps, st);
-      return launch_t<T, S, D, false, 3, NC, true>(c, s, nsteps, st);
-    }
+    if (chunk >= 64 && grid >= 2LL * 7 * num_sms_current_device())
+      return launch_t<T, S, D, false, 2, NC, true>(c, s, nsteps, st);
   }
   if (!all_resident<T, S, D, false, 3, NC>(c, chunk) && all_resident<T, S, D, false, 2, NC>(c, chunk))
     return launch_t<T, S, D, false, 2, NC>(c, s, nsteps, st);

@@ -343,15 +343,11 @@ h2o_status h2o_decode_steps(h2o_cache_t c, int n, const void *q, const void *k, 
   } else if (form == 2) {
     use_coop = coop_ok;
   } else if (form == 0) {
-    // Automatic: the pipelined cluster form where the rows stream through
-    // the slab ring, the plain cluster form where they stay resident in
-    // shared memory (there the per-step exchange chain, not the attention
-    // pass, bounds a step, and the pipelined form's single protocol warp
-    // makes that chain no shorter), else the cooperative grid, else one
-    // launch per step.  Measured on GB300, us per step (cluster /
-    // pipelined): 8K prompt 90.1 / 77.7, OPT-30B 69.3 / 64.6, OPT-6.7B
-    // 7.33 / 6.92, long stream (resident) 2.51 / 2.57.
-    if (pipe_ok && !decode_cluster_resident(vc))
+    // Automatic: the pipelined cluster form, else the cluster form, else
+    // the cooperative grid, else one launch per step.  Measured on GB300, us
+    // per decode step (cluster / pipelined): 8K prompt 90.1 / 79.0, OPT-30B
+    // 69.3 / 63.9, OPT-6.7B 7.33 / 6.91, long stream 2.51 / 2.36.
+    if (pipe_ok)
       use_pipe = true;
     else if (cluster_ok)
       use_cluster = true;

@@ -144,7 +144,7 @@ __global__ void __launch_bounds__(threads_for(NC), W ? (kStages == 2 ? 4 : 3) : 
   __shared__ uint64_t s_part[2];       // a step's consumer partials (NC arrivals)
   __shared__ uint64_t s_dec[4];        // decision of step u made (phase u / 4 of s_dec[u % 4])
   __shared__ uint64_t s_oldv;          // evicted V row saved (one phase per decision)
-  __shared__ __align__(8) uint64_t s_bml, s_bacc, s_bcand;
+  __shared__ __align__(8) uint64_t s_bml, s_bacc[2], s_bcand;  // acc rows of step u complete on s_bacc[u & 1]
   __shared__ __align__(16) T s_in[kBufs][3][D];  // q, k_t, v_t of step u in buffer u % 3
   __shared__ float s_wm[2][NC], s_wl[2][NC];
   __shared__ __align__(16) float s_wacc[2][NC][D];
@@ -174,7 +174,7 @@ __global__ void __launch_bounds__(threads_for(NC), W ? (kStages == 2 ? 4 : 3) : 
 
   // dynamic shared memory: [ring or resident K|V][score][pos][score
   // compensation][logits of two steps] (+ [K scale][V scale])[every rank's
-  // acc row, P x D, read on rank 0]
+  // acc rows of two steps, 2 x P x D, read on rank 0]
   uint8_t *kv = smem;
   const int kv_bytes = kResident ? 2 * chunk * ROWB : ring_bytes(kStages, W);
   float *sc = (float *)(smem + kv_bytes);
@@ -204,7 +204,8 @@ __global__ void __launch_bounds__(threads_for(NC), W ? (kStages == 2 ? 4 : 3) : 
     for (int i = 0; i < 4; ++i) mbar_init(&s_dec[i], 1);
     mbar_init(&s_oldv, 1);
     mbar_init(&s_bml, 1);
-    mbar_init(&s_bacc, 1);
+    mbar_init(&s_bacc[0], 1);
+    mbar_init(&s_bacc[1], 1);
     mbar_init(&s_bcand, 1);
     s_abort = 0;
     s_tp = 0;
@@ -482,6 +483,17 @@ __global__ void __launch_bounds__(threads_for(NC), W ? (kStages == 2 ? 4 : 3) : 
     int tp = 0;  // decisions made
     bool failed = false;
     auto wait_bar = [&](uint64_t *bar, uint32_t par) -> bool { return __all_sync(FULL, mbar_wait(bar, par)); };
+    // log2-domain logit of a step's new token against its own query
+    auto new_logit = [&](const T *qq, const T *kk) -> float {
+      float qv[CPL], kx[CPL];
+      row_part<T, CPL>(qq, lane, qv);
+      row_part<T, CPL>(kk, lane, kx);
+      float dot = 0.f;
+#pragma unroll
+      for (int u = 0; u < CPL; ++u) dot = fmaf(qv[u], kx[u], dot);
+      return warp_sum(dot) * a.qscale;
+    };
+    float lg_next = 0.f;  // rank 0: the next step's new-token logit
 
     for (int t = 0; t < a.nsteps && !failed; ++t) {
       if (*(volatile int *)&s_abort) {
@@ -491,7 +503,7 @@ __global__ void __launch_bounds__(threads_for(NC), W ? (kStages == 2 ? 4 : 3) : 
       if (lane == 0) {  // bytes this CTA receives during step t's exchanges
         mbar_expect_tx(&s_bml, P * 16);
         mbar_expect_tx(&s_bcand, P * 16);
-        if (rank == 0) mbar_expect_tx(&s_bacc, P * D * 4);
+        if (rank == 0) mbar_expect_tx(&s_bacc[t & 1], P * D * 4);
       }
       const int q = t % kBufs;
       if (!wait_bar(&s_inbar[q], (t / kBufs) & 1) || !wait_bar(&s_part[t & 1], (t >> 1) & 1)) {
@@ -574,10 +586,6 @@ __global__ void __launch_bounds__(threads_for(NC), W ? (kStages == 2 ? 4 : 3) : 
             }
           }
           __syncwarp();
-          if (kResident) {  // the resident copy takes the new row (no consumer reads slot j this step)
-            warp_copy(kv + (size_t)j * ROWB, s_pend[q1][0], ROWB, lane);
-            warp_copy(kv + (size_t)chunk * ROWB + (size_t)j * ROWB, s_pend[q1][1], ROWB, lane);
-          }
           if (kFp8 && lane == 0) {
             ksc[j] = s_pksc[q1];
             vsc[j] = s_pvsc[q1];
@@ -603,16 +611,12 @@ __global__ void __launch_bounds__(threads_for(NC), W ? (kStages == 2 ? 4 : 3) : 
           if (lane == 0) lg[j] = dot;
         }
       }
-      // ---- rank 0: the step's new token, from the step inputs
+      // ---- rank 0: the step's new token, from the step inputs (its logit
+      // taken in advance while the previous step waited for candidates)
       float lgnew = 0.f;
       if (rank == 0) {
-        float qv[CPL], kx[CPL], vx[CPL];
-        row_part<T, CPL>(in_q, lane, qv);
-        row_part<T, CPL>(in_k, lane, kx);
-        float dot = 0.f;
-#pragma unroll
-        for (int u = 0; u < CPL; ++u) dot = fmaf(qv[u], kx[u], dot);
-        lgnew = warp_sum(dot) * a.qscale;
+        float vx[CPL];
+        lgnew = t == 0 ? new_logit(in_q, in_k) : lg_next;
         const float mn = fmaxf(M, lgnew);
         const float scl = (M == -INFINITY) ? 0.f : exp2f(M - mn);
         const float pn = exp2f(lgnew - mn);
@@ -624,7 +628,7 @@ __global__ void __launch_bounds__(threads_for(NC), W ? (kStages == 2 ? 4 : 3) : 
       }
       // ---- exchange 1: acc row to rank 0, (m, l, new-token logit) to every rank
       {
-        const uint32_t dst = mapa(&accx[rank * D + lane * CPL], 0), bar0 = mapa(&s_bacc, 0);
+        const uint32_t dst = mapa(&accx[((t & 1) * P + rank) * D + lane * CPL], 0), bar0 = mapa(&s_bacc[t & 1], 0);
         if constexpr (CPL == 4) {
           st_async_v4(dst, make_uint4(__float_as_uint(acc[0]), __float_as_uint(acc[1]), __float_as_uint(acc[2]),
                                       __float_as_uint(acc[3])),
@@ -637,7 +641,20 @@ __global__ void __launch_bounds__(threads_for(NC), W ? (kStages == 2 ? 4 : 3) : 
                       make_uint4(__float_as_uint(M), __float_as_uint(l), __float_as_uint(lgnew), 0u),
                       mapa(&s_bml, lane));
       }
-      if (!wait_bar(&s_bml, t & 1) || (rank == 0 && !wait_bar(&s_bacc, t & 1))) {
+      if (kResident && t >= 1 && s_pslot[(t - 1) % kBufs] >= 0) {
+        // Decision t-1's row into the resident copy and the cache rows in
+        // HBM, off the exchange's path: the consumers read slot j from the
+        // pending copy until decision t is made, and nothing in this launch
+        // reads the rows in HBM.
+        const int q1 = (t - 1) % kBufs, j = s_pslot[q1];
+        warp_copy(kv + (size_t)j * ROWB, s_pend[q1][0], ROWB, lane);
+        warp_copy(kv + (size_t)chunk * ROWB + (size_t)j * ROWB, s_pend[q1][1], ROWB, lane);
+        const size_t off = (hk + s0 + j) * (size_t)ROWB;
+        warp_copy((uint8_t *)c.K + off, s_pend[q1][0], ROWB, lane);
+        warp_copy((uint8_t *)c.V + off, s_pend[q1][1], ROWB, lane);
+        __syncwarp();
+      }
+      if (!wait_bar(&s_bml, t & 1)) {
         failed = true;
         break;
       }
@@ -657,21 +674,6 @@ __global__ void __launch_bounds__(threads_for(NC), W ? (kStages == 2 ? 4 : 3) : 
       for (int o = kMaxCluster / 2; o; o >>= 1) Lg += __shfl_xor_sync(FULL, Lg, o);
       Mg = __shfl_sync(FULL, Mg, 0);
       const float invL = 1.f / __shfl_sync(FULL, Lg, 0);
-      if (rank == 0) {  // the step's output row
-        float o[CPL];
-#pragma unroll
-        for (int u = 0; u < CPL; ++u) o[u] = 0.f;
-        for (int r = 0; r < P; ++r) {
-          const float f = __shfl_sync(FULL, fr, r);
-          if (f != 0.f) {
-#pragma unroll
-            for (int u = 0; u < CPL; ++u) o[u] = fmaf(f, accx[r * D + lane * CPL + u], o[u]);
-          }
-        }
-        T *out = (T *)a.s.out + (size_t)t * step_elems + (size_t)h * D;
-#pragma unroll
-        for (int u = 0; u < CPL; ++u) out[lane * CPL + u] = from_f32<T>(o[u] * invL);
-      }
       // ---- exact weights into the scores of S_t; local argmin
       const int nr = rows_after(t);
       const long long lim = (long long)p - c.kl;
@@ -699,6 +701,37 @@ __global__ void __launch_bounds__(threads_for(NC), W ? (kStages == 2 ? 4 : 3) : 
         st_async_v4(mapa(&s_candx[rank], lane),
                     make_uint4(__float_as_uint(best.s), (uint32_t)best.p, (uint32_t)best.slot, 0u),
                     mapa(&s_bcand, lane));
+      if (rank == 0) {
+        // The step's output row, off the path to the decision: the acc rows
+        // of step t sit in buffer t & 1, which the ranks refill only with
+        // step t+2's rows, after this CTA's candidate of step t+1.
+        if (!wait_bar(&s_bacc[t & 1], (t >> 1) & 1)) {
+          failed = true;
+          break;
+        }
+        const float *ax = accx + (t & 1) * P * D;
+        float o[CPL];
+#pragma unroll
+        for (int u = 0; u < CPL; ++u) o[u] = 0.f;
+        for (int r = 0; r < P; ++r) {
+          const float f = __shfl_sync(FULL, fr, r);
+          if (f != 0.f) {
+#pragma unroll
+            for (int u = 0; u < CPL; ++u) o[u] = fmaf(f, ax[r * D + lane * CPL + u], o[u]);
+          }
+        }
+        T *out = (T *)a.s.out + (size_t)t * step_elems + (size_t)h * D;
+#pragma unroll
+        for (int u = 0; u < CPL; ++u) out[lane * CPL + u] = from_f32<T>(o[u] * invL);
+      }
+      if (rank == 0 && t + 1 < a.nsteps) {  // the next step's new-token logit, while candidates travel
+        const int qn = (t + 1) % kBufs;
+        if (!wait_bar(&s_inbar[qn], ((t + 1) / kBufs) & 1)) {
+          failed = true;
+          break;
+        }
+        lg_next = new_logit(s_in[qn][0], s_in[qn][1]);
+      }
       if (!wait_bar(&s_bcand, t & 1)) {
         failed = true;
         break;
@@ -765,10 +798,7 @@ __global__ void __launch_bounds__(threads_for(NC), W ? (kStages == 2 ? 4 : 3) : 
         }
         __syncwarp();
         if (kResident) {
-          // rows in HBM at once (nothing in this launch reads them back)
-          const size_t off = (hk + e) * (size_t)ROWB;
-          warp_copy((uint8_t *)c.K + off, s_pend[q][0], ROWB, lane);
-          warp_copy((uint8_t *)c.V + off, s_pend[q][1], ROWB, lane);
+          // the row goes to the resident copy and HBM during the next step
         } else if (n >= c.k) {
           // The row S_t holds in slot j (its V is needed when decision t is
           // applied to step t+1): the pending copy of decision t-1 or t-2 if
@@ -804,11 +834,18 @@ __global__ void __launch_bounds__(threads_for(NC), W ? (kStages == 2 ? 4 : 3) : 
       s_abort = 1;
       atomicOr(c.err, 1);
     }
-    if (kFp8 && tp > 0 && lane == 0) {  // the row scales of the last decision (no next step applies it)
+    if (tp > 0 && !failed) {  // the last decision (no next step applies it)
       const int q = (tp - 1) % kBufs, j = s_pslot[q];
       if (j >= 0) {
-        ksc[j] = s_pksc[q];
-        vsc[j] = s_pvsc[q];
+        if (kFp8 && lane == 0) {
+          ksc[j] = s_pksc[q];
+          vsc[j] = s_pvsc[q];
+        }
+        if (kResident) {
+          const size_t off = (hk + s0 + j) * (size_t)ROWB;
+          warp_copy((uint8_t *)c.K + off, s_pend[q][0], ROWB, lane);
+          warp_copy((uint8_t *)c.V + off, s_pend[q][1], ROWB, lane);
+        }
       }
     }
     // inputs fetched for steps that never ran (an aborted call) must land too
@@ -919,7 +956,7 @@ template <typename S, int D> constexpr int row_bytes() { return D * (int)sizeof(
 template <typename S, int D, bool R, int St, bool W = false>
 int smem_bytes(int chunk, int P) {
   const int base = (R ? 2 * chunk * row_bytes<S, D>() : ring_bytes(St, W)) + slot_words<S>() * chunk * 4;
-  return ((base + 15) & ~15) + P * D * 4;
+  return ((base + 15) & ~15) + 2 * P * D * 4;  // + every rank's acc rows of two steps
 }
 
 int chunk_of(const CacheView &c) { return (c.k + c.nsplit - 1) / c.nsplit; }
@@ -1007,7 +1044,7 @@ bool decode_pipe_supported(const CacheView &c) {
   const int chunk = (c.k + c.nsplit - 1) / c.nsplit;
   const int row = c.d * (c.kv_fp8 ? 1 : c.dtype == 1 ? 2 : 4);
   const int kv = (2 * chunk * row <= kResidentMaxBytes) ? 2 * chunk * row : ring_bytes(3);
-  return kv + (c.kv_fp8 ? 7 : 5) * chunk * 4 + 16 + c.nsplit * c.d * 4 <= 200 * 1024;
+  return kv + (c.kv_fp8 ? 7 : 5) * chunk * 4 + 16 + 2 * c.nsplit * c.d * 4 <= 200 * 1024;
 }
 
 cudaError_t launch_decode_pipe(const CacheView &c, const DecodeStep &s, int nsteps, cudaStream_t st) {

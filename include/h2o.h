@@ -129,8 +129,9 @@ h2o_status h2o_decode_steps(h2o_cache_t cache, int n, const void *q, const void 
 
 /* How h2o_decode_steps runs n >= 2 steps (all forms compute the same thing;
  * single steps always use form 1):
- *   0  automatic (default): 4 if the shape allows it, else 3, else 2 when
- *      all its CTAs fit on the device at once, else 1;
+ *   0  automatic (default): 4 for a bf16 or fp32 cache and 3 for an fp8
+ *      cache if the shape allows it, else 2 when all its CTAs fit on the
+ *      device at once, else 1;
  *   1  one launch per step, chained with programmatic dependent launch;
  *   2  one cooperative launch: each (head, split) CTA loops over the steps,
  *      waiting (bounded, acquire) only on its own head's previous step;

@@ -62,11 +62,13 @@ L2_RESIDENT_BYTES = 120e6  # caches below this stay in the 129 MB L2 across deco
 METRIC = "H2O decode tokens/s and KV-read GB/s vs HBM peak; prefill score TFLOP/s"
 DEFAULT_CONFIG = 3  # the 8K-prompt serving shape: the largest single-GPU workload
 STREAM_CHUNK = 65536  # decode steps per call when the inputs are generated on the device
-# The end-to-end leg pipelines by row groups (one cache each, decoded as soon as
-# its rows are prefilled) from this prompt length on: measured on GB300, the
-# 8K-prompt job 60.2 -> 57.6 ms; on 1-2K prompts the per-group decodes were
-# slower than one decode over all rows (OPT-6.7B shape 6.0 -> 14.8 ms).
-E2E_ROWS_MIN_PROMPT = 4096
+# The end-to-end leg pipelines by rows (prompt row groups prefilled as they
+# land into a few caches, each decoded once its rows are prefilled) when each
+# cache still holds this many heads: its decode grid then fills the GPU.
+# Measured on GB300 (ms per job, one cache whose decode waits for every row /
+# rows into 2 caches): 8K prompt 57.3 / 52.1, OPT-30B shape 100.9 / 90.3;
+# OPT-6.7B shape (128 heads per cache) 5.75 / 8.12.
+E2E_ROWS_MIN_HEADS = 512
 
 
 def peaks():
@@ -505,10 +507,11 @@ def run_ours(args, w, rank, world, local_rank):
     del qd, kd, vd, Qd, Kd, Vd, O, out  # device inputs of the resident runs: room for the e2e buffers
     caches.clear()
     if not args.no_e2e:
-        rows = args.e2e_pipeline == "rows" or (args.e2e_pipeline == "auto" and w.L >= E2E_ROWS_MIN_PROMPT)
+        rows = args.e2e_pipeline == "rows" or (
+            args.e2e_pipeline == "auto" and wl.B * w.H // max(1, args.e2e_decode_groups) >= E2E_ROWS_MIN_HEADS)
         if rows and not streamed(w):
             line["e2e"] = e2e_row_caches(args, w, wl, Bg, dev, hQ, hK, hV, hq, hk, hv, tdt, stream, world, dist,
-                                         row_groups=args.e2e_row_groups)
+                                         row_groups=args.e2e_row_groups, decode_groups=args.e2e_decode_groups)
         else:
             line["e2e"] = e2e(args, w, wl, Bg, heads, dev, hQ, hK, hV, hq, hk, hv, tdt, stream, world, dist,
                               row_groups=args.e2e_row_groups, step_groups=args.e2e_step_groups)
@@ -651,55 +654,81 @@ def e2e(args, w, wl, Bg, heads, dev, hQ, hK, hV, hq, hk, hv, tdt, stream, world,
     return r
 
 
-def e2e_row_caches(args, w, wl, Bg, dev, hQ, hK, hV, hq, hk, hv, tdt, stream, world, dist, row_groups=8):
+def e2e_row_caches(args, w, wl, Bg, dev, hQ, hK, hV, hq, hk, hv, tdt, stream, world, dist, row_groups=8,
+                   decode_groups=2):
     """Same job from pinned host buffers, pipelined by batch rows: the batch is
-    split into `row_groups` groups with one cache each (every head is
-    independent, so the arithmetic is the same as one cache over all rows).
-    A side stream copies each group's prompt rows and decode inputs in turn;
-    the compute stream prefills and decodes group g as soon as its inputs have
-    landed (while later groups are still crossing the host link), and group
-    g's outputs copy back while later groups compute.  The host buffers are
-    laid out per group (contiguous rows) before the timed region."""
+    split into `decode_groups` caches (every head is independent, so the
+    arithmetic is the same as one cache over all rows), each filled by
+    `row_groups` / `decode_groups` prompt row groups.  A side stream copies
+    the row groups' prompts in turn, and each cache's decode inputs after its
+    last row group; the compute stream prefills each row group into its cache
+    (h2o_prefill_rows) as soon as its rows have landed and decodes a cache as
+    soon as all its rows are prefilled, while later rows are still crossing
+    the host link; a cache's outputs copy back while later caches compute.
+    Caches of several row groups keep the decode grids large.  The host
+    buffers are laid out per group (contiguous rows) before the timed region."""
     import torch
     from h2o_heavy_hitter_decode_gb300 import H2OCache
     nb = wl.B
-    ng = max(1, min(row_groups, nb))
-    groups = [(nb * g // ng, nb * (g + 1) // ng) for g in range(ng)]
-    pin = [[x[b0:b1].contiguous().pin_memory() for x in (hQ, hK, hV)]
-           + [x[:, b0:b1].contiguous().pin_memory() for x in (hq, hk, hv)] for b0, b1 in groups]
-    dbuf = [[torch.empty_like(x, device=dev) for x in p] for p in pin]
-    outs = [torch.empty(p[3].shape, dtype=tdt, device=dev) for p in pin]
-    houts = [torch.empty(p[3].shape, dtype=tdt).pin_memory() for p in pin]
-    O = [torch.empty(p[0].shape, dtype=tdt, device=dev) for p in pin]
-    lse = [torch.empty(p[0].shape[:3], dtype=torch.float32, device=dev) for p in pin]
+    nd = max(1, min(decode_groups, nb))
+    caches_rows = [(nb * c // nd, nb * (c + 1) // nd) for c in range(nd)]
+    per = max(1, row_groups // nd)  # prompt row groups per cache
+    groups = []  # (cache index, first row, end row)
+    for ci, (c0, c1) in enumerate(caches_rows):
+        m = max(1, min(per, c1 - c0))
+        groups += [(ci, c0 + (c1 - c0) * g // m, c0 + (c1 - c0) * (g + 1) // m) for g in range(m)]
+    ng = len(groups)
+    pin_p = [[x[b0:b1].contiguous().pin_memory() for x in (hQ, hK, hV)] for _, b0, b1 in groups]
+    pin_d = [[x[:, c0:c1].contiguous().pin_memory() for x in (hq, hk, hv)] for c0, c1 in caches_rows]
+    dbuf_p = [[torch.empty_like(x, device=dev) for x in p] for p in pin_p]
+    dbuf_d = [[torch.empty_like(x, device=dev) for x in p] for p in pin_d]
+    outs = [torch.empty(p[0].shape, dtype=tdt, device=dev) for p in pin_d]
+    houts = [torch.empty(p[0].shape, dtype=tdt).pin_memory() for p in pin_d]
+    O = [torch.empty(p[0].shape, dtype=tdt, device=dev) for p in pin_p]
+    lse = [torch.empty(p[0].shape[:3], dtype=torch.float32, device=dev) for p in pin_p]
     colsum = [torch.empty_like(x) for x in lse]
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     side = torch.cuda.Stream(device=dev)
     back = torch.cuda.Stream(device=dev)
+    last_group = {ci: max(g for g, (cj, _, _) in enumerate(groups) if cj == ci) for ci in range(nd)}
+
+    def copy_all():
+        for g, (ci, _, _) in enumerate(groups):
+            for t in range(3):
+                dbuf_p[g][t].copy_(pin_p[g][t], non_blocking=True)
+            if g == last_group[ci]:
+                for t in range(3):
+                    dbuf_d[ci][t].copy_(pin_d[ci][t], non_blocking=True)
 
     def job(start_ev):
         side.wait_event(start_ev)
         landed = []
         with torch.cuda.stream(side):
-            for g in range(ng):
-                for t in range(6):
-                    dbuf[g][t].copy_(pin[g][t], non_blocking=True)
+            for g, (ci, _, _) in enumerate(groups):
+                for t in range(3):
+                    dbuf_p[g][t].copy_(pin_p[g][t], non_blocking=True)
+                if g == last_group[ci]:
+                    for t in range(3):
+                        dbuf_d[ci][t].copy_(pin_d[ci][t], non_blocking=True)
                 ev = torch.cuda.Event()
                 ev.record(side)
                 landed.append(ev)
-        caches = []
-        for g, (b0, b1) in enumerate(groups):
-            stream.wait_event(landed[g])
-            c = H2OCache(b1 - b0, w.H, w.d, w.k_heavy, w.k_local, tdt, device=dev, kv_fp8=is_kvfp8(w))
+        caches = [H2OCache(c1 - c0, w.H, w.d, w.k_heavy, w.k_local, tdt, device=dev, kv_fp8=is_kvfp8(w))
+                  for c0, c1 in caches_rows]
+        for c in caches:
             c.set_decode_form(args.decode_form)
-            c.prefill(dbuf[g][0], dbuf[g][1], dbuf[g][2], O=O[g], lse=lse[g], colsum=colsum[g])
-            c.steps(dbuf[g][3], dbuf[g][4], dbuf[g][5], out=outs[g])
-            done = torch.cuda.Event()
-            done.record(stream)
-            back.wait_event(done)
-            with torch.cuda.stream(back):
-                houts[g].copy_(outs[g], non_blocking=True)
-            caches.append(c)
+        for g, (ci, b0, b1) in enumerate(groups):
+            stream.wait_event(landed[g])
+            c = caches[ci]
+            c.prefill_rows(b0 - caches_rows[ci][0], dbuf_p[g][0], dbuf_p[g][1], dbuf_p[g][2], O=O[g], lse=lse[g],
+                           colsum=colsum[g])
+            if g == last_group[ci]:
+                c.steps(dbuf_d[ci][0], dbuf_d[ci][1], dbuf_d[ci][2], out=outs[ci])
+                done = torch.cuda.Event()
+                done.record(stream)
+                back.wait_event(done)
+                with torch.cuda.stream(back):
+                    houts[ci].copy_(outs[ci], non_blocking=True)
         stream.wait_stream(back)  # the job ends when its outputs are on the host
         return caches
 
@@ -707,9 +736,7 @@ def e2e_row_caches(args, w, wl, Bg, dev, hQ, hK, hV, hq, hk, hv, tdt, stream, wo
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     e0.record(stream)
-    for g in range(ng):
-        for t in range(6):
-            dbuf[g][t].copy_(pin[g][t], non_blocking=True)
+    copy_all()
     e1.record(stream)
     torch.cuda.synchronize()
     h2d_alone_ms = e0.elapsed_time(e1)
@@ -731,10 +758,12 @@ def e2e_row_caches(args, w, wl, Bg, dev, hQ, hK, hV, hq, hk, hv, tdt, stream, wo
     torch.cuda.synchronize()
     ms_step, value = aggregate_over_ranks(float(np.sum([a.elapsed_time(b) for a, b in timed])), n, Bg * w.T,
                                           world, dist, dev)
-    h2d = sum(x.numel() * x.element_size() for p in pin for x in p)
+    h2d = sum(x.numel() * x.element_size() for p in pin_p + pin_d for x in p)
     d2h = sum(x.numel() * x.element_size() for x in houts)
     return {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "ms_per_step": ms_step, "pipeline": f"{ng} row groups, one cache each, each decoded once prefilled",
+            "ms_per_step": ms_step,
+            "pipeline": f"{ng} prompt row groups prefilled as they land into {nd} caches, each decoded once its "
+                        "rows are prefilled",
             "h2d_alone": {"ms": h2d_alone_ms, "gbs": h2d / (h2d_alone_ms / 1e3) / 1e9,
                           "what": "one copy of every input buffer from pinned host memory, nothing else running"}}
 
@@ -838,10 +867,13 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-row-groups", type=int, default=8, help="prompt row groups copied/prefilled in turn")
     ap.add_argument("--e2e-step-groups", type=int, default=4, help="decode step groups copied/decoded in turn")
+    ap.add_argument("--e2e-decode-groups", type=int, default=2,
+                    help="caches of the row-pipelined end-to-end leg (each decoded once its rows are prefilled)")
     ap.add_argument("--e2e-pipeline", choices=["auto", "rows", "steps"], default="auto",
-                    help="end-to-end leg: one cache per row group, each decoded once prefilled (rows), or one "
-                         "cache whose decode waits for every row's prefill (steps); auto: rows for prompts of "
-                         f"at least {E2E_ROWS_MIN_PROMPT} tokens")
+                    help="end-to-end leg: prompt row groups prefilled as they land into a few caches, each "
+                         "decoded once its rows are prefilled (rows), or one cache whose decode waits for every "
+                         f"row's prefill (steps); auto: rows when each cache holds at least {E2E_ROWS_MIN_HEADS} "
+                         "heads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3:

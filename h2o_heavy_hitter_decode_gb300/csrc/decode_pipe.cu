@@ -32,8 +32,10 @@
 // Decisions reach the cache rows in HBM three steps late: the producer warp
 // writes decision u's row only after every slab of step u+1 has landed (those
 // must still see the old row) and before it issues the first slab of step
-// u+3.  A CTA whose rows stay resident in shared memory writes HBM at the
-// decision and its resident copy when it applies the decision.
+// u+3.  A CTA whose rows stay resident in shared memory writes a decision's
+// row to its resident copy and to HBM during the next step, after that
+// step's exchange push (nothing in the launch reads the HBM rows, and the
+// consumers read the slot from the pending copy until then).
 // All waits are bounded (error flag, drain, exit); clusters never wait on one
 // another.
 #include <cooperative_groups.h>

@@ -39,3 +39,51 @@ def test_evicted_entry_dominating_next_query(case, form):
     print(w.name, form, dominated, rep)
     assert cache.decode_form_used() == form
     assert rep.steps_compared >= w.T
+
+
+CALL_SIZES = [2, 3, 1, 5, 2, 4, 3, 8]  # decode calls of 1..8 steps: every early-step and end-of-call path
+
+
+@pytest.mark.parametrize("w", [W("calls_streamed_bf16", 1, 2, 128, 2600, 28, 1300, 1100, "bf16", 48),
+                               W("calls_resident_f32", 1, 3, 64, 200, 28, 30, 20, "f32", 49)],
+                         ids=lambda w: w.name)
+def test_short_calls_match_the_oracle(w):
+    """The pipelined form over decode calls of 1 to 8 steps (its first
+    steps, the decisions still pending at the end of a call and their write
+    back all run in every call): every eviction and output against the
+    oracle's single run over all steps, then the final cache state."""
+    import numpy as np
+    import torch
+    import oracle
+    from parity_helpers import to_dev, f64, out_atol, tdtype, compare_scores, Report, permitted
+    from h2o_heavy_hitter_decode_gb300 import H2OCache
+    assert sum(CALL_SIZES) == w.T
+    Qs, Ks, Vs = synth.prompt(w)
+    qs, ks, vs = synth.decode(w, 0, w.T)
+    cv = lambda x: synth.as_f64(x, w.dtype)
+    shp = (w.B, w.H, w.L, w.d)
+    c = H2OCache(w.B, w.H, w.d, w.k_heavy, w.k_local, tdtype(w))
+    c.set_decode_form("pipelined")
+    c.prefill(to_dev(Qs, w, shp), to_dev(Ks, w, shp), to_dev(Vs, w, shp))
+    st = oracle.prefill(cv(Qs), cv(Ks), cv(Vs), w.k_heavy, w.k_local)["state"]
+    od = oracle.decode(st, w.L, cv(qs), cv(ks), cv(vs), w.k_heavy, w.k_local)
+    dshp = (w.T, w.B, w.H, w.d)
+    q, k, v = (to_dev(x, w, dshp) for x in (qs, ks, vs))
+    t0 = 0
+    for n in CALL_SIZES:
+        ev = torch.empty((n, w.B, w.H), dtype=torch.int32, device="cuda")
+        out = c.steps(q[t0:t0 + n], k[t0:t0 + n], v[t0:t0 + n], evicted=ev)
+        assert c.decode_form_used() == ("pipelined" if n >= 2 else "per_step")
+        g_ev = ev.reshape(n, w.nh).cpu().numpy()
+        bad = np.nonzero(g_ev != od["evicted"][t0:t0 + n])
+        assert bad[0].size == 0 or permitted(od["margin"][t0:t0 + n][bad]), (t0, bad)
+        assert bad[0].size == 0, "a permitted near-tie divergence: this case is built without one"
+        err = float(np.abs(f64(out).reshape(n, w.nh, w.d) - od["out"][t0:t0 + n]).max())
+        assert err <= out_atol(w.dtype), (t0, n, err)
+        t0 += n
+    ex = c.export()
+    rep = Report()
+    compare_scores(rep, ex["pos"].cpu().numpy().reshape(w.nh, w.k), ex["score"].cpu().numpy().reshape(w.nh, w.k),
+                   st, list(range(w.nh)))
+    assert rep.max_score_rel <= 1e-3, rep
+    c.check_device_error()

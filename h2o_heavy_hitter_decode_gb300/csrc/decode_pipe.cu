@@ -55,7 +55,7 @@ using namespace sm100;
 constexpr int kShortChunk = 256;                                 // <= : two consumer warps, else four
 constexpr int threads_for(int nc) { return 32 * nc + 64; }        // + the protocol and producer warps
 constexpr int kMaxCluster = 8;
-constexpr int stage_bytes(bool wide) { return wide ? 8192 : 4096; }
+constexpr int stage_bytes(bool wide) { return 4096; }  // 4 KB per operand (16 bf16 rows of 128 in the wide layout)
 constexpr int ring_bytes(int stages, bool wide = false) { return stages * 2 * stage_bytes(wide); }
 constexpr int kResidentMaxBytes = 96 * 1024;
 constexpr int kBufs = 3;  // step-input and pending-row buffers (steps t, t-1, t-2 in use)
@@ -68,7 +68,7 @@ template <typename S, int D, int NC, bool W> struct Geo {
   static constexpr int SB = stage_bytes(W);
   static constexpr int TR = SB / ROWB;
   static constexpr int ITER = W ? 1 : TR / (NC * RPW);
-  static_assert(W ? (TR == 32 && ROWB == 256) : (ITER >= 1 && TR % (NC * RPW) == 0),
+  static_assert(W ? (TR == 16 && ROWB == 256) : (ITER >= 1 && TR % (NC * RPW) == 0),
                 "slab must split evenly over warps (wide: 32 bf16 rows of 128)");
 };
 
@@ -125,7 +125,7 @@ __device__ __forceinline__ void warp_copy(void *dst, const void *src, int bytes,
 // T: type of the step inputs and outputs; S: type of the stored K/V rows;
 // NC: consumer warps; W: wide-row layout (bf16 rows of 128).
 template <typename T, typename S, int D, bool kResident, int kStages, int NC, bool W>
-__global__ void __launch_bounds__(threads_for(NC), W ? (kStages == 2 ? 4 : 3) : (NC == 2 ? 7 : 5))
+__global__ void __launch_bounds__(threads_for(NC), W ? 4 : (NC == 2 ? 7 : 5))
     decode_pipe_kernel(const PArgs a) {
   constexpr int kThreads = threads_for(NC);
   using G = Geo<S, D, NC, W>;
@@ -290,10 +290,15 @@ __global__ void __launch_bounds__(threads_for(NC), W ? (kStages == 2 ? 4 : 3) : 
         // consumer warps are not in step with one another, and each full
         // barrier (x mod (stages * NC)) must be waited on by one warp only,
         // in order, so that no wait can be satisfied by an earlier phase.
-        uint32_t qr[16][4];
+        // Two lanes per row: lane i takes row i % 16 of a 16-row slab and
+        // its dimensions 64 * (i / 16) .. +63 (eight 16-byte chunks walked in
+        // an order rotated by the row, q rotated the same way); one shuffle
+        // adds the two halves.  V: lane i owns output dimensions 4i .. 4i+3.
+        const int vr = lane & 15, hh = lane >> 4;
+        uint32_t qr[8][4];
 #pragma unroll
-        for (int cch = 0; cch < 16; ++cch) {
-          const uint4 u = *(const uint4 *)(in_q + (((cch + lane) & 15) << 3));
+        for (int cch = 0; cch < 8; ++cch) {
+          const uint4 u = *(const uint4 *)(in_q + hh * 64 + (((cch + vr) & 7) << 3));
           qr[cch][0] = u.x; qr[cch][1] = u.y; qr[cch][2] = u.z; qr[cch][3] = u.w;
         }
         // two accumulator sets (even and odd rows) halve the dependent chain
@@ -314,12 +319,12 @@ __global__ void __launch_bounds__(threads_for(NC), W ? (kStages == 2 ? 4 : 3) : 
           const int rows = min(TR, rows_t - i * TR);
           const int plane = pe - i * TR;                  // patched row of this slab, if in [0, rows)
           const bool pin = (unsigned)plane < (unsigned)rows;  // warp-uniform
-          const bool valid = lane < rows;
-          const uint8_t *krow = (pin && lane == plane) ? pk : ks + (valid ? lane : 0) * ROWB;
+          const bool valid = vr < rows;
+          const uint8_t *krow = ((pin && vr == plane) ? pk : ks + (valid ? vr : 0) * ROWB) + hh * 128;
           float d4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int cch = 0; cch < 16; ++cch) {
-            const uint4 kc = *(const uint4 *)(krow + (((cch + lane) & 15) << 4));
+          for (int cch = 0; cch < 8; ++cch) {
+            const uint4 kc = *(const uint4 *)(krow + (((cch + vr) & 7) << 4));
             float dd = d4[cch & 3];
             dd = fma2_bf16(qr[cch][0], kc.x, dd);
             dd = fma2_bf16(qr[cch][1], kc.y, dd);
@@ -327,9 +332,10 @@ __global__ void __launch_bounds__(threads_for(NC), W ? (kStages == 2 ? 4 : 3) : 
             dd = fma2_bf16(qr[cch][3], kc.w, dd);
             d4[cch & 3] = dd;
           }
-          float lgt = ((d4[0] + d4[1]) + (d4[2] + d4[3])) * a.qscale;
+          float lgt = (d4[0] + d4[1]) + (d4[2] + d4[3]);
+          lgt = (lgt + __shfl_xor_sync(FULL, lgt, 16)) * a.qscale;
           lgt = valid ? lgt : -INFINITY;
-          if (valid) lg[i * TR + lane] = lgt;
+          if (valid && hh == 0) lg[i * TR + vr] = lgt;
           const float wmax = warp_max_ordered(lgt);
           if (wmax > m) {
             const float sc_ = ex2(m - wmax);
@@ -342,8 +348,8 @@ __global__ void __launch_bounds__(threads_for(NC), W ? (kStages == 2 ? 4 : 3) : 
             m = wmax;
           }
           const float pr = valid ? ex2(lgt - m) : 0.f;
-          l += pr;
-          const float pwv = (pin && lane == plane) ? 0.f : pr;  // the patched row's V comes from its pending copy
+          if (hh == 0) l += pr;  // each row once
+          const float pwv = (pin && vr == plane) ? 0.f : pr;  // the patched row's V comes from its pending copy
           const uint8_t *vcol = vs + lane * 8;
           auto vrow = [&](int r) {
             const float w = __shfl_sync(FULL, pwv, r);
@@ -1025,7 +1031,7 @@ cudaError_t dispatch_nc(const CacheView &c, const DecodeStep &s, int nsteps, cud
   if constexpr (wide_rows<T, S, D>()) {
     const long long grid = (long long)c.nh * c.nsplit;
     if (chunk >= 64 && grid >= 2LL * 7 * num_sms_current_device())
-      return launch_t<T, S, D, false, 2, NC, true>(c, s, nsteps, st);
+      return launch_t<T, S, D, false, 4, NC, true>(c, s, nsteps, st);
   }
   if (!all_resident<T, S, D, false, 3, NC>(c, chunk) && all_resident<T, S, D, false, 2, NC>(c, chunk))
     return launch_t<T, S, D, false, 2, NC>(c, s, nsteps, st);

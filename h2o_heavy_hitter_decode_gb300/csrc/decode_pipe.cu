@@ -125,7 +125,7 @@ __device__ __forceinline__ void warp_copy(void *dst, const void *src, int bytes,
 // T: type of the step inputs and outputs; S: type of the stored K/V rows;
 // NC: consumer warps; W: wide-row layout (bf16 rows of 128).
 template <typename T, typename S, int D, bool kResident, int kStages, int NC, bool W>
-__global__ void __launch_bounds__(threads_for(NC), W ? 4 : (NC == 2 ? 7 : 5))
+__global__ void __launch_bounds__(threads_for(NC), W ? 5 : (NC == 2 ? 7 : 5))
     decode_pipe_kernel(const PArgs a) {
   constexpr int kThreads = threads_for(NC);
   using G = Geo<S, D, NC, W>;
@@ -146,7 +146,7 @@ __global__ void __launch_bounds__(threads_for(NC), W ? 4 : (NC == 2 ? 7 : 5))
   __shared__ uint64_t s_part[2];       // a step's consumer partials (NC arrivals)
   __shared__ uint64_t s_dec[4];        // decision of step u made (phase u / 4 of s_dec[u % 4])
   __shared__ uint64_t s_oldv;          // evicted V row saved (one phase per decision)
-  __shared__ __align__(8) uint64_t s_bml, s_bacc[2], s_bcand;  // acc rows of step u complete on s_bacc[u & 1]
+  __shared__ __align__(8) uint64_t s_bml, s_bacc[2], s_bcand;  // acc values of step u complete on s_bacc[u & 1]
   __shared__ __align__(16) T s_in[kBufs][3][D];  // q, k_t, v_t of step u in buffer u % 3
   __shared__ float s_wm[2][NC], s_wl[2][NC];
   __shared__ __align__(16) float s_wacc[2][NC][D];
@@ -171,12 +171,21 @@ __global__ void __launch_bounds__(threads_for(NC), W ? 4 : (NC == 2 ? 7 : 5))
   const int chunk = a.chunk;
   const int s0 = rank * chunk;
   const int own = max(0, min(c.k, s0 + chunk) - s0);
+  // Output row: rank 0 writes it from every rank's acc row, except in the
+  // wide-row layout, where each rank writes D/P of its dimensions from every
+  // rank's acc values there (a smaller exchange buffer: the shared memory
+  // goes to the ring and a fifth CTA per SM; on the short per-step chains of
+  // resident and lane-group shapes the extra exchange wait costs more).
+  constexpr bool kSplitOut = W && !kResident;
+  const int DPR = kSplitOut ? D / P : D;  // output dimensions per writing rank (P divides D)
   const size_t hk = (size_t)h * c.k;
   const size_t step_elems = (size_t)c.nh * D;
 
   // dynamic shared memory: [ring or resident K|V][score][pos][score
-  // compensation][logits of two steps] (+ [K scale][V scale])[every rank's
-  // acc rows of two steps, 2 x P x D, read on rank 0]
+  // compensation][logits of two steps] (+ [K scale][V scale])[output
+  // exchange of two steps: every rank's acc row, 2 x P x D (read on rank
+  // 0), or every rank's values of this CTA's D/P dimensions, 2 x D (wide
+  // rows)]
   uint8_t *kv = smem;
   const int kv_bytes = kResident ? 2 * chunk * ROWB : ring_bytes(kStages, W);
   float *sc = (float *)(smem + kv_bytes);
@@ -511,7 +520,10 @@ __global__ void __launch_bounds__(threads_for(NC), W ? 4 : (NC == 2 ? 7 : 5))
       if (lane == 0) {  // bytes this CTA receives during step t's exchanges
         mbar_expect_tx(&s_bml, P * 16);
         mbar_expect_tx(&s_bcand, P * 16);
-        if (rank == 0) mbar_expect_tx(&s_bacc[t & 1], P * D * 4);
+        if (kSplitOut)
+          mbar_expect_tx(&s_bacc[t & 1], D * 4);  // every rank's values of this CTA's D/P dimensions
+        else if (rank == 0)
+          mbar_expect_tx(&s_bacc[t & 1], P * D * 4);
       }
       const int q = t % kBufs;
       if (!wait_bar(&s_inbar[q], (t / kBufs) & 1) || !wait_bar(&s_part[t & 1], (t >> 1) & 1)) {
@@ -634,9 +646,12 @@ __global__ void __launch_bounds__(threads_for(NC), W ? 4 : (NC == 2 ? 7 : 5))
         for (int u = 0; u < CPL; ++u) acc[u] = fmaf(pn, vx[u], acc[u] * scl);
         M = mn;
       }
-      // ---- exchange 1: acc row to rank 0, (m, l, new-token logit) to every rank
+      // ---- exchange 1: (m, l, new-token logit) to every rank; the acc row to
+      // rank 0, or each group of D/P dimensions to the rank that writes them
       {
-        const uint32_t dst = mapa(&accx[((t & 1) * P + rank) * D + lane * CPL], 0), bar0 = mapa(&s_bacc[t & 1], 0);
+        const int dim = lane * CPL, dst_rank = kSplitOut ? dim / DPR : 0;
+        const uint32_t dst = mapa(&accx[((t & 1) * P + rank) * DPR + dim % DPR], dst_rank),
+                       bar0 = mapa(&s_bacc[t & 1], dst_rank);
         if constexpr (CPL == 4) {
           st_async_v4(dst, make_uint4(__float_as_uint(acc[0]), __float_as_uint(acc[1]), __float_as_uint(acc[2]),
                                       __float_as_uint(acc[3])),
@@ -709,7 +724,25 @@ __global__ void __launch_bounds__(threads_for(NC), W ? 4 : (NC == 2 ? 7 : 5))
         st_async_v4(mapa(&s_candx[rank], lane),
                     make_uint4(__float_as_uint(best.s), (uint32_t)best.p, (uint32_t)best.slot, 0u),
                     mapa(&s_bcand, lane));
-      if (rank == 0) {
+      if (kSplitOut) {
+        // This CTA's dimensions of the step's output row, off the path to the
+        // decision: step t's values sit in buffer t & 1, which the ranks
+        // refill only with step t+2's, after this CTA's candidate of step t+1.
+        if (!wait_bar(&s_bacc[t & 1], (t >> 1) & 1)) {
+          failed = true;
+          break;
+        }
+        const float *ax = accx + (t & 1) * P * DPR;
+        T *out = (T *)a.s.out + (size_t)t * step_elems + (size_t)h * D + rank * DPR;
+        for (int d0 = 0; d0 < DPR; d0 += 32) {
+          float o = 0.f;
+          for (int r = 0; r < P; ++r) {
+            const float f = __shfl_sync(FULL, fr, r);
+            if (d0 + lane < DPR && f != 0.f) o = fmaf(f, ax[r * DPR + d0 + lane], o);
+          }
+          if (d0 + lane < DPR) out[d0 + lane] = from_f32<T>(o * invL);
+        }
+      } else if (rank == 0) {
         // The step's output row, off the path to the decision: the acc rows
         // of step t sit in buffer t & 1, which the ranks refill only with
         // step t+2's rows, after this CTA's candidate of step t+1.
@@ -964,7 +997,7 @@ template <typename S, int D> constexpr int row_bytes() { return D * (int)sizeof(
 template <typename S, int D, bool R, int St, bool W = false>
 int smem_bytes(int chunk, int P) {
   const int base = (R ? 2 * chunk * row_bytes<S, D>() : ring_bytes(St, W)) + slot_words<S>() * chunk * 4;
-  return ((base + 15) & ~15) + 2 * P * D * 4;  // + every rank's acc rows of two steps
+  return ((base + 15) & ~15) + 2 * (W && !R ? 1 : P) * D * 4;  // + the output exchange buffer of two steps
 }
 
 int chunk_of(const CacheView &c) { return (c.k + c.nsplit - 1) / c.nsplit; }

@@ -292,9 +292,7 @@ __global__ void __launch_bounds__(threads_for(NC), W ? 5 : (NC == 2 ? 7 : 5))
       const int nslab = (rows_t + TR - 1) / TR;
       float *wacc = s_wacc[t & 1][warp];
       if constexpr (W) {
-        // Wide rows: one warp per 32-row slab, lane i takes row i's whole dot
-        // product (sixteen 16-byte chunks in an order rotated by i, q rotated
-        // the same way) and output dimensions 4i .. 4i+3 of the V rows.  The
+        // Wide rows: one warp per 16-row slab (layout below).  The
         // slab at ring position x goes to warp x mod NC whatever its step:
         // consumer warps are not in step with one another, and each full
         // barrier (x mod (stages * NC)) must be waited on by one warp only,
@@ -1053,9 +1051,9 @@ template <typename T, typename S, int D> constexpr bool wide_rows() {
 
 // The same instance choice as the cluster form: rows resident in shared
 // memory when they fit and the grid is co-resident; the wide-row layout for
-// bf16 rows of 128 on grids of two waves or more (two ring stages: a third
-// would cost a CTA per SM); else lane groups with a
-// three-stage ring, or two stages when that makes the grid co-resident.
+// bf16 rows of 128 on grids of two waves or more (four stages of 16-row
+// slabs); else lane groups with a three-stage ring, or two stages when that
+// makes the grid co-resident.
 template <typename T, typename S, int D, int NC>
 cudaError_t dispatch_nc(const CacheView &c, const DecodeStep &s, int nsteps, cudaStream_t st) {
   const int chunk = chunk_of(c);

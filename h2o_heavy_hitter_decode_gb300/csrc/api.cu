@@ -333,7 +333,9 @@ h2o_status h2o_decode_steps(h2o_cache_t c, int n, const void *q, const void *k, 
   vc.nsplit = decode_cluster_size(c->nh, c->k, num_sms_current_device());
   const int form = c->decode_form;
   const bool cluster_ok = n >= 2 && decode_cluster_supported(vc);
-  const bool pipe_ok = n >= 2 && decode_pipe_supported(vc);
+  CacheView vp = vc;  // pipelined form: its own cluster size
+  vp.nsplit = decode_pipe_cluster_size(c->view, num_sms_current_device());
+  const bool pipe_ok = n >= 2 && decode_pipe_supported(vp);
   const bool coop_ok = n >= 2 && (form == 0 || form == 2) && decode_persistent_fits(c->view);
   bool use_cluster = false, use_pipe = false, use_coop = false;
   if (form == 4) {
@@ -370,7 +372,7 @@ h2o_status h2o_decode_steps(h2o_cache_t c, int n, const void *q, const void *k, 
     s.evicted = evicted;
     s.n_valid = c->n_valid;
     s.p = (int)c->next_pos;
-    cudaError_t e = use_pipe ? launch_decode_pipe(vc, s, n, c->stream) : launch_decode_cluster(vc, s, n, c->stream);
+    cudaError_t e = use_pipe ? launch_decode_pipe(vp, s, n, c->stream) : launch_decode_cluster(vc, s, n, c->stream);
     if (e != cudaSuccess) return cuda_fail(e);
     c->next_pos += n;
     c->n_valid = (int)((int64_t)c->n_valid + n < c->k ? c->n_valid + n : c->k);

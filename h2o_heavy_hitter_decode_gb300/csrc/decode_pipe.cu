@@ -1049,19 +1049,17 @@ template <typename T, typename S, int D> constexpr bool wide_rows() {
   return std::is_same<T, __nv_bfloat16>::value && std::is_same<S, __nv_bfloat16>::value && D == 128;
 }
 
-// The same instance choice as the cluster form: rows resident in shared
-// memory when they fit and the grid is co-resident; the wide-row layout for
-// bf16 rows of 128 on grids of two waves or more (four stages of 16-row
-// slabs); else lane groups with a three-stage ring, or two stages when that
-// makes the grid co-resident.
+// Rows resident in shared memory when they fit and the grid is
+// co-resident; the wide-row layout (four stages of 16-row slabs) for bf16
+// rows of 128 and at least 64 slots per CTA; else lane groups with a
+// three-stage ring, or two stages when that makes the grid co-resident.
 template <typename T, typename S, int D, int NC>
 cudaError_t dispatch_nc(const CacheView &c, const DecodeStep &s, int nsteps, cudaStream_t st) {
   const int chunk = chunk_of(c);
   if (2 * chunk * row_bytes<S, D>() <= kResidentMaxBytes && all_resident<T, S, D, true, 1, NC>(c, chunk))
     return launch_t<T, S, D, true, 1, NC>(c, s, nsteps, st);
   if constexpr (wide_rows<T, S, D>()) {
-    const long long grid = (long long)c.nh * c.nsplit;
-    if (chunk >= 64 && grid >= 2LL * 7 * num_sms_current_device())
+    if (chunk >= 64)
       return launch_t<T, S, D, false, 4, NC, true>(c, s, nsteps, st);
   }
   if (!all_resident<T, S, D, false, 3, NC>(c, chunk) && all_resident<T, S, D, false, 2, NC>(c, chunk))
@@ -1076,6 +1074,23 @@ cudaError_t dispatch_t(const CacheView &c, const DecodeStep &s, int nsteps, cuda
 }
 
 }  // namespace
+
+// Cluster size of the pipelined form.  Shapes that take the wide-row layout
+// (bf16 rows of 128, no fp8): the smallest power of two that leaves each CTA
+// at most 256 slots, doubled (up to 8) while the doubled grid still fits one
+// wave of five CTAs per SM.  Other shapes: the cluster form's rule.
+// Measured on GB300 (us per decode step): OPT-6.7B shape (256 heads,
+// k = 512) wide rows with clusters of 2: 6.50, lane groups with clusters of
+// 4 (the cluster form's rule): 6.91, wide rows with clusters of 4: 7.51.
+int decode_pipe_cluster_size(const CacheView &c, int sms) {
+  if (!(c.dtype == 1 && !c.kv_fp8 && c.d == 128)) return decode_cluster_size(c.nh, c.k, sms);
+  int P = 1;
+  while (P < kMaxCluster && (c.k + P - 1) / P > kShortChunk) P *= 2;
+  if ((c.k + P - 1) / P < 64) return decode_cluster_size(c.nh, c.k, sms);  // lane groups (or resident rows)
+  const long long wave = 5LL * (sms > 0 ? sms : 1);
+  while (P < kMaxCluster && (long long)c.nh * P * 2 <= wave) P *= 2;
+  return P;
+}
 
 bool decode_pipe_supported(const CacheView &c) {
   if (c.nsplit < 1 || c.nsplit > kMaxCluster) return false;

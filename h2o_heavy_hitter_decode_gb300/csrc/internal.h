@@ -58,6 +58,7 @@ cudaError_t launch_decode_cluster(const CacheView &c, const DecodeStep &s, int n
 // The cluster form with each step's eviction decision taken while the next
 // step's attention pass runs (decode_pipe.cu); same cluster size and layout.
 bool decode_pipe_supported(const CacheView &c);
+int decode_pipe_cluster_size(const CacheView &c, int sms);  // CTAs per head of the pipelined form
 cudaError_t launch_decode_pipe(const CacheView &c, const DecodeStep &s, int nsteps, cudaStream_t st);
 // Split count of the decode launch for nh heads of k slots on `sms` SMs
 // (fixes the size of the split-partial scratch).

@@ -818,11 +818,6 @@ cudaError_t dispatch_nc(const CacheView &c, const DecodeStep &s, int nsteps, cud
 
 // The consumer-warp count for a CTA that owns chunk_of(c) slots.
 template <typename T, typename S, int D>
-bool resident_t(const CacheView &c) {
-  return chunk_of(c) > kShortChunk ? resident_nc<T, S, D, 4>(c) : resident_nc<T, S, D, 2>(c);
-}
-
-template <typename T, typename S, int D>
 cudaError_t dispatch_t(const CacheView &c, const DecodeStep &s, int nsteps, cudaStream_t st) {
   return chunk_of(c) > kShortChunk ? dispatch_nc<T, S, D, 4>(c, s, nsteps, st)
                                    : dispatch_nc<T, S, D, 2>(c, s, nsteps, st);
@@ -843,12 +838,6 @@ cudaError_t dispatch_t(const CacheView &c, const DecodeStep &s, int nsteps, cuda
   } while (0)
 
 }  // namespace
-
-bool decode_cluster_resident(const CacheView &c) {
-  if (c.nsplit < 1 || c.nsplit > kMaxCluster) return false;
-  H2O_CLUSTER_DISPATCH(resident_t, c);
-  return false;
-}
 
 // Cluster size: the smallest power of two that leaves each CTA at most
 // kShortChunk slots (the two-consumer-warp kernel), doubled (up to 8) while

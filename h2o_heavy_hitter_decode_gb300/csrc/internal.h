@@ -50,7 +50,6 @@ cudaError_t launch_decode_persistent(const CacheView &c, const DecodeStep &s, in
 // at most 8): scores/tags/logits in shared memory, DSMEM pushes completing on
 // the receivers' mbarriers; no global scratch.
 bool decode_cluster_supported(const CacheView &c);
-bool decode_cluster_resident(const CacheView &c);  // each CTA's K/V rows stay in shared memory
 // CTAs per head (cluster size, 1..8) of the cluster form for nh heads of k
 // slots on `sms` SMs.
 int decode_cluster_size(int nh, int k, int sms);

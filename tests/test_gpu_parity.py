@@ -249,3 +249,22 @@ def test_wide_row_decode_all_heads(w, form):
     print(w.name, form, rep)
     assert cache.decode_form_used() == form
     assert rep.steps_compared >= w.T
+
+
+# Many heads with small caches: the pipelined form's cluster-size rule gives
+# one CTA per head (a doubled grid would not fit one wave of five CTAs per
+# SM), so each step's values never leave the CTA: no exchange between CTAs.
+# 512 heads stream their rows (wide-row layout); 416 heads keep them resident
+# in shared memory (lane groups).
+ONE_CTA = [
+    small("bf16_one_cta_per_head_streamed", 16, 32, 128, 200, 24, 64, 64, "bf16"),
+    small("bf16_one_cta_per_head_resident", 13, 32, 128, 150, 24, 70, 58, "bf16"),
+]
+
+
+@pytest.mark.parametrize("w", ONE_CTA, ids=lambda w: w.name)
+def test_one_cta_per_head_decode(w):
+    rep, cache = run_parity(w, decode_form="pipelined")
+    print(w.name, rep)
+    assert cache.decode_form_used() == "pipelined"
+    assert rep.steps_compared >= w.T

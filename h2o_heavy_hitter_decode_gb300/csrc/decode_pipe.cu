@@ -699,17 +699,32 @@ __global__ void __launch_bounds__(threads_for(NC), W ? 5 : (NC == 2 ? 7 : 5))
       const int nr = rows_after(t);
       const long long lim = (long long)p - c.kl;
       ArgMin best{INFINITY, INT_MAX, -2};
-#pragma unroll 4
-      for (int j = lane; j < nr; j += 32) {
-        const float w = exp2f(lg[j] - Mg) * invL;
-        float s_new = sc[j], cj = cm[j];
-        kahan_add(s_new, cj, w);
-        sc[j] = s_new;
-        cm[j] = cj;
-        const int pj = ps[j];
-        if ((long long)pj <= lim && pj >= c.n_sink) {
-          const ArgMin cand{rank_key(s_new, p, pj, c.score_mode), pj, s0 + j};
-          if (am_less(cand, best)) best = cand;
+      // four entries per lane at a time, all loaded before any is stored
+      for (int j0 = lane; j0 < nr; j0 += 128) {
+        float lv[4], sv[4], cv[4];
+        int pv[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int j = j0 + 32 * u;
+          if (j < nr) {
+            lv[u] = lg[j];
+            sv[u] = sc[j];
+            cv[u] = cm[j];
+            pv[u] = ps[j];
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int j = j0 + 32 * u;
+          if (j < nr) {
+            kahan_add(sv[u], cv[u], exp2f(lv[u] - Mg) * invL);
+            sc[j] = sv[u];
+            cm[j] = cv[u];
+            if ((long long)pv[u] <= lim && pv[u] >= c.n_sink) {
+              const ArgMin cand{rank_key(sv[u], p, pv[u], c.score_mode), pv[u], s0 + j};
+              if (am_less(cand, best)) best = cand;
+            }
+          }
         }
       }
       const float w_new = exp2f(__uint_as_float(s_mlx[0].z) - Mg) * invL;

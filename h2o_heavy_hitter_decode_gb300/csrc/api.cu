@@ -348,8 +348,8 @@ h2o_status h2o_decode_steps(h2o_cache_t c, int n, const void *q, const void *k, 
     // Automatic: the pipelined cluster form for bf16 and fp32 caches, the
     // cluster form for an fp8 cache, else the cooperative grid, else one
     // launch per step.  Measured on GB300, us per decode step (cluster /
-    // pipelined): 8K prompt 90.1 / 79.0, OPT-30B 69.3 / 63.9, OPT-6.7B
-    // 7.33 / 6.91, long stream 2.51 / 2.35; with an fp8 cache 8K prompt
+    // pipelined): 8K prompt 90.1 / 73.5, OPT-30B 69.3 / 57.8, OPT-6.7B
+    // 7.33 / 6.24, long stream 2.51 / 2.40; with an fp8 cache 8K prompt
     // 108.2 / 154.2, OPT-30B 97.3 / 133.6 (the pipelined kernel's lane-group
     // fp8 instance runs fewer CTAs per SM).
     if (pipe_ok && !c->view.kv_fp8)
